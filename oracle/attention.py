@@ -1,0 +1,168 @@
+"""Plain, slow, obviously-correct exact attention forward in float64.
+
+TEST INFRASTRUCTURE ONLY (see ``oracle/__init__.py``): the product path never
+imports this module.
+
+What is computed (the definition, not the tiled algorithm):
+  "FlashAttention-4 no Blackwell B200 …", section "Por que o Blackwell exige
+  mais do que multiplicações rápidas": scaled attention is
+  softmax(Q Kᵀ / √d) V.  The tiled/online method reaches exactly this result up
+  to rounding ("FlashAttention-4 em Blackwell B200 …", FAQ question 2: the
+  softmax is identical to the original attention), so the oracle is the
+  definition written out, two-pass and non-online:
+
+  for each batch b, head h and query row i
+    s_ij   = scale · Σ_c q_ic k_jc                   (float64, over the exact
+                                                      bf16 input values)
+    V_i    = { j : 0 ≤ j < Sk and (not causal or j ≤ i) }
+    M_i    = max_{j∈V_i} s_ij
+    L_i    = Σ_{j∈V_i} exp(s_ij − M_i)
+    P_ij   = exp(s_ij − M_i) / L_i  for j ∈ V_i, else 0
+    O_i    = Σ_j P_ij v_j
+    LSE_i  = M_i + ln L_i        (natural log-sum-exp of the scaled logits)
+
+Readings where the pages are silent (each also listed in the design notes):
+  * layout: Q, K, V, O are (batch, seq, heads, head_dim), the only layout the
+    pages show ("FlashAttention-3: Pipeline Assíncrono …", section
+    "Implementando FlashAttention-3 em produção"); LSE is (batch, heads, Sq).
+  * causal: key j is visible to query i iff j ≤ i (top-left alignment).
+  * a row with no visible key has O = 0 and LSE = −inf.
+  * the scale is an argument; the pages pass 1/√head_dim.
+
+Library primitives used as steps: numpy matmul (dgemm), exp, log, max, sum.
+"""
+
+from __future__ import annotations
+
+import numpy as np
+
+# Rows of Q processed per matmul, to bound memory (a chunk of scores is
+# ROW_CHUNK × Sk float64 values).
+ROW_CHUNK = 1024
+
+
+def to_f64(x) -> np.ndarray:
+    """Exact float64 copy of a bf16/fp32 torch tensor or array-like.
+
+    bf16 → fp32 → fp64 is exact, so the oracle sees the same values as the GPU.
+    """
+    try:
+        import torch  # local import: the oracle itself needs only numpy
+
+        if isinstance(x, torch.Tensor):
+            return x.detach().to("cpu", torch.float32).numpy().astype(np.float64)
+    except ImportError:  # pragma: no cover
+        pass
+    return np.asarray(x, dtype=np.float64)
+
+
+def visible_mask(rows: np.ndarray, Sk: int, causal: bool) -> np.ndarray:
+    """Boolean [len(rows), Sk]: True where key j is visible to query row i.
+
+    Visible set: 0 ≤ j < Sk, and j ≤ i when causal (top-left alignment).
+    """
+    rows = np.asarray(rows, dtype=np.int64)
+    keys = np.arange(Sk, dtype=np.int64)
+    if not causal:
+        return np.ones((rows.shape[0], Sk), dtype=bool)
+    return keys[None, :] <= rows[:, None]
+
+
+def head_scores(q: np.ndarray, k: np.ndarray, scale: float) -> np.ndarray:
+    """s = scale · q kᵀ for one head. q: [n, d], k: [Sk, d], float64."""
+    return scale * (q @ k.T)
+
+
+def head_probabilities(s: np.ndarray, mask: np.ndarray):
+    """Two-pass softmax of each row over its visible keys.
+
+    Returns (P, M, L): P [n, Sk] with zeros outside the visible set,
+    M [n] the row maximum over visible keys (−inf if none),
+    L [n] = Σ_visible exp(s − M) (0 if none).
+    """
+    masked = np.where(mask, s, -np.inf)
+    M = masked.max(axis=1)
+    finite = np.isfinite(M)
+    shift = np.where(finite, M, 0.0)
+    E = np.where(mask, np.exp(masked - shift[:, None]), 0.0)
+    L = E.sum(axis=1)
+    with np.errstate(invalid="ignore", divide="ignore"):
+        P = np.where(finite[:, None], E / np.where(finite, L, 1.0)[:, None], 0.0)
+    return P, M, L
+
+
+def attention_head(q, k, v, scale: float, causal: bool, rows=None):
+    """Exact attention for one head, float64.
+
+    q: [Sq, d], k: [Sk, d], v: [Sk, d].  ``rows`` selects query rows (default
+    all).  Returns (O [n, d], LSE [n]) for the selected rows.
+    """
+    q = np.asarray(q, dtype=np.float64)
+    k = np.asarray(k, dtype=np.float64)
+    v = np.asarray(v, dtype=np.float64)
+    Sk = k.shape[0]
+    rows = np.arange(q.shape[0]) if rows is None else np.asarray(rows, dtype=np.int64)
+    O = np.zeros((rows.shape[0], v.shape[1]), dtype=np.float64)
+    LSE = np.full((rows.shape[0],), -np.inf, dtype=np.float64)
+    for c0 in range(0, rows.shape[0], ROW_CHUNK):
+        r = rows[c0:c0 + ROW_CHUNK]
+        # Causal rows never see keys beyond their own index: only the needed
+        # key prefix is multiplied (same result, less work).
+        kmax = Sk if not causal else int(min(Sk, r.max() + 1))
+        s = head_scores(q[r], k[:kmax], scale)
+        P, M, L = head_probabilities(s, visible_mask(r, kmax, causal))
+        O[c0:c0 + r.shape[0]] = P @ v[:kmax]
+        with np.errstate(divide="ignore"):
+            LSE[c0:c0 + r.shape[0]] = np.where(np.isfinite(M), M + np.log(np.where(L > 0, L, 1.0)), -np.inf)
+    return O, LSE
+
+
+def attention_forward(q, k, v, scale: float, causal: bool):
+    """Exact attention over all batches and heads.
+
+    q: [B, Sq, H, d]; k, v: [B, Sk, H, d] (torch tensors or arrays).
+    Returns O [B, Sq, H, d] float64 and LSE [B, H, Sq] float64.
+    """
+    q, k, v = to_f64(q), to_f64(k), to_f64(v)
+    B, Sq, H, d = q.shape
+    O = np.zeros((B, Sq, H, v.shape[3]), dtype=np.float64)
+    LSE = np.zeros((B, H, Sq), dtype=np.float64)
+    for b in range(B):
+        for h in range(H):
+            O[b, :, h, :], LSE[b, h, :] = attention_head(q[b, :, h, :], k[b, :, h, :], v[b, :, h, :], scale, causal)
+    return O, LSE
+
+
+def attention_rows(q, k, v, scale: float, causal: bool, b: int, h: int, rows):
+    """Exact attention for selected query rows of one (batch, head).
+
+    Used to check full-size GPU outputs on a sample of rows.
+    Returns (O [n, d], LSE [n]) float64.
+    """
+    qh = to_f64(q[b, :, h, :]) if not isinstance(q, np.ndarray) else q[b, :, h, :]
+    kh = to_f64(k[b, :, h, :]) if not isinstance(k, np.ndarray) else k[b, :, h, :]
+    vh = to_f64(v[b, :, h, :]) if not isinstance(v, np.ndarray) else v[b, :, h, :]
+    return attention_head(qh, kh, vh, scale, causal, rows=rows)
+
+
+def combine_partials(O_parts, LSE_parts):
+    """Merge attention results computed over disjoint key ranges.
+
+    Each part r holds (O_r, LSE_r) of the same query rows over its own key
+    subset.  Since exp(LSE_r) is that subset's share of the softmax
+    denominator, the full result is LSE = ln Σ_r exp(LSE_r) and
+    O = Σ_r exp(LSE_r − LSE) · O_r.  Parts with LSE_r = −inf (no visible key)
+    contribute nothing.  Inputs: lists of arrays [..., n, d] and [..., n].
+    """
+    L = np.stack([np.asarray(x, dtype=np.float64) for x in LSE_parts])
+    Os = np.stack([np.asarray(x, dtype=np.float64) for x in O_parts])
+    M = L.max(axis=0)
+    finite = np.isfinite(M)
+    shift = np.where(finite, M, 0.0)
+    W = np.where(np.isfinite(L), np.exp(L - shift[None]), 0.0)
+    tot = W.sum(axis=0)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        LSE = np.where(finite, shift + np.log(np.where(tot > 0, tot, 1.0)), -np.inf)
+        w = np.where(finite[None], W / np.where(tot > 0, tot, 1.0)[None], 0.0)
+    O = (w[..., None] * Os).sum(axis=0)
+    return O, LSE

@@ -1,0 +1,304 @@
+"""Pins that tie the CPU oracle to something other than itself.
+
+Each ``pin_*`` function raises AssertionError when the oracle is wrong.  They
+are collected by ``test_oracle.py`` and re-run against deliberately broken
+oracles by ``test_oracle_mutants.py`` (every planted mistake must trip at
+least one pin).
+
+Sources of truth used here, none of which is the oracle's own code:
+  * brute force in pure Python (math.fsum / math.exp) on tiny inputs;
+  * the online-softmax recurrence restated independently from the Python
+    simulator of "FlashAttention-4 em Blackwell B200 …" (section 4, its
+    ``online_softmax_accumulate`` step, which keeps O normalised), extended
+    with a causal mask and run with several block sizes;
+  * closed forms (tests/golden/closed_form_cases.json) and invariants that
+    follow from the definition: rows of P sum to 1, constant V, a single key,
+    causal row 0, Q = 0, key shift, key permutation;
+  * scipy.special.softmax / logsumexp on the same score matrix.
+"""
+
+from __future__ import annotations
+
+import json
+import math
+import os
+
+import numpy as np
+from scipy import special
+
+import oracle
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "closed_form_cases.json")
+TOL = 1e-12
+
+
+def _rng(seed):
+    return np.random.default_rng(seed)
+
+
+def _bf16_like(a):
+    """Round float64 values to the bf16 grid (RNE) so inputs look like the GPU's."""
+    f = np.asarray(a, dtype=np.float32)
+    u = f.view(np.uint32).astype(np.uint64)
+    u = ((u + 0x7FFF + ((u >> 16) & 1)) >> 16) << 16
+    return u.astype(np.uint32).view(np.float32).astype(np.float64)
+
+
+def rand_head(seed, Sq, Sk, d, sigma=1.0):
+    r = _rng(seed)
+    q = _bf16_like(r.standard_normal((Sq, d)) * sigma)
+    k = _bf16_like(r.standard_normal((Sk, d)) * sigma)
+    v = _bf16_like(r.standard_normal((Sk, d)))
+    return q, k, v
+
+
+# ---------------------------------------------------------------- brute force
+def brute_force_head(q, k, v, scale, causal):
+    """Pure-Python attention for one head (lists of floats, math.fsum)."""
+    Sq, Sk, d = len(q), len(k), len(v[0])
+    O, LSE = [], []
+    for i in range(Sq):
+        vis = [j for j in range(Sk) if (not causal) or j <= i]
+        if not vis:
+            O.append([0.0] * d)
+            LSE.append(-math.inf)
+            continue
+        s = {j: scale * math.fsum(q[i][c] * k[j][c] for c in range(len(q[i]))) for j in vis}
+        m = max(s.values())
+        e = {j: math.exp(s[j] - m) for j in vis}
+        tot = math.fsum(e.values())
+        O.append([math.fsum(e[j] * v[j][c] for j in vis) / tot for c in range(d)])
+        LSE.append(m + math.log(tot))
+    return np.array(O), np.array(LSE)
+
+
+def pin_brute_force_tiny():
+    cases = [(1, 1, 8, False), (2, 2, 8, True), (3, 3, 16, True), (5, 5, 16, False),
+             (17, 17, 64, True), (17, 9, 64, False), (4, 7, 8, False), (7, 4, 8, True)]
+    for n, (Sq, Sk, d, causal) in enumerate(cases):
+        q, k, v = rand_head(100 + n, Sq, Sk, d, sigma=2.0)
+        scale = 1.0 / math.sqrt(d)
+        O, L = oracle.attention_head(q, k, v, scale, causal)
+        Ob, Lb = brute_force_head(q.tolist(), k.tolist(), v.tolist(), scale, causal)
+        assert O.shape == Ob.shape and L.shape == Lb.shape
+        fin = np.isfinite(Lb)
+        assert np.array_equal(fin, np.isfinite(L)), (Sq, Sk, causal)
+        assert np.max(np.abs(O - Ob)) <= TOL, (Sq, Sk, causal)
+        assert np.max(np.abs(L[fin] - Lb[fin])) <= TOL, (Sq, Sk, causal)
+
+
+def pin_brute_force_d64_130():
+    # 130 rows = one full 128-row tile plus a ragged tail of 2.
+    for causal in (False, True):
+        q, k, v = rand_head(7 if causal else 8, 130, 130, 64)
+        O, L = oracle.attention_head(q, k, v, 0.125, causal)
+        Ob, Lb = brute_force_head(q.tolist(), k.tolist(), v.tolist(), 0.125, causal)
+        assert np.max(np.abs(O - Ob)) <= TOL
+        assert np.max(np.abs(L - Lb)) <= TOL
+
+
+# ----------------------------------------------------------- online recurrence
+def online_recurrence_head(q, k, v, scale, causal, block):
+    """The simulator's per-block update, restated in float64 with a causal mask.
+
+    Per key block: m_new = max(m, rowmax); a = exp(m − m_new) (0 when m = −inf);
+    p = exp(s − m_new); l_new = a·l + Σp; O_new = (a·l·O + p·V) / l_new.
+    """
+    Sq, Sk = q.shape[0], k.shape[0]
+    m = np.full(Sq, -np.inf)
+    l = np.zeros(Sq)
+    O = np.zeros((Sq, v.shape[1]))
+    rows = np.arange(Sq)[:, None]
+    for j0 in range(0, Sk, block):
+        kb, vb = k[j0:j0 + block], v[j0:j0 + block]
+        s = scale * (q @ kb.T)
+        if causal:
+            s = np.where(np.arange(j0, j0 + kb.shape[0])[None, :] <= rows, s, -np.inf)
+        rowmax = s.max(axis=1)
+        m_new = np.maximum(m, rowmax)
+        a = np.where(np.isfinite(m), np.exp(m - np.where(np.isfinite(m_new), m_new, 0.0)), 0.0)
+        p = np.where(np.isfinite(m_new)[:, None], np.exp(s - np.where(np.isfinite(m_new), m_new, 0.0)[:, None]), 0.0)
+        l_new = a * l + p.sum(axis=1)
+        safe = np.where(l_new != 0, l_new, 1.0)
+        O = ((a * l)[:, None] * O + p @ vb) / safe[:, None]
+        m, l = m_new, l_new
+    lse = np.where(l > 0, m + np.log(np.where(l > 0, l, 1.0)), -np.inf)
+    return O, lse
+
+
+def pin_online_recurrence():
+    for n, (Sq, Sk, d, causal) in enumerate([(64, 64, 32, False), (64, 64, 32, True),
+                                             (200, 300, 64, False), (300, 300, 64, True),
+                                             (129, 257, 128, True)]):
+        q, k, v = rand_head(200 + n, Sq, Sk, d, sigma=3.0 if n % 2 else 1.0)
+        scale = 1.0 / math.sqrt(d)
+        O, L = oracle.attention_head(q, k, v, scale, causal)
+        for block in (1, 7, 32, 128):
+            Or, Lr = online_recurrence_head(q, k, v, scale, causal, block)
+            assert np.max(np.abs(O - Or)) <= 1e-12, (n, block)
+            assert np.max(np.abs(L - Lr)) <= 1e-12, (n, block)
+
+
+# ------------------------------------------------------------- library routines
+def pin_scipy_softmax_logsumexp():
+    for causal in (False, True):
+        q, k, v = rand_head(300 + causal, 96, 96, 64, sigma=2.0)
+        scale = 0.125
+        rows = np.arange(96)
+        s = oracle.head_scores(q, k, scale)
+        mask = oracle.visible_mask(rows, 96, causal)
+        P, M, L = oracle.head_probabilities(s, mask)
+        s_lib = scale * np.einsum("ic,jc->ij", q, k)
+        s_lib = np.where(np.tril(np.ones((96, 96), bool)) if causal else True, s_lib, -np.inf)
+        assert np.max(np.abs(P - special.softmax(s_lib, axis=1))) <= TOL
+        O, LSE = oracle.attention_head(q, k, v, scale, causal)
+        assert np.max(np.abs(LSE - special.logsumexp(s_lib, axis=1))) <= TOL
+        assert np.max(np.abs(O - special.softmax(s_lib, axis=1) @ v)) <= TOL
+
+
+# ------------------------------------------------------------------ invariants
+def pin_rows_sum_to_one():
+    for causal in (False, True):
+        q, k, _ = rand_head(400 + causal, 150, 150, 64, sigma=3.0)
+        P, _, _ = oracle.head_probabilities(oracle.head_scores(q, k, 0.125),
+                                            oracle.visible_mask(np.arange(150), 150, causal))
+        assert np.max(np.abs(P.sum(axis=1) - 1.0)) <= TOL
+        assert np.all(P >= 0)
+        if causal:
+            assert np.all(P[np.triu(np.ones((150, 150), bool), 1)] == 0)
+
+
+def pin_constant_v():
+    for causal in (False, True):
+        q, k, v = rand_head(500 + causal, 70, 70, 64, sigma=2.0)
+        c = np.linspace(-3, 3, 64)
+        v[:] = c[None, :]
+        O, _ = oracle.attention_head(q, k, v, 0.125, causal)
+        assert np.max(np.abs(O - c[None, :])) <= TOL
+
+
+def pin_single_key():
+    q, k, v = rand_head(600, 9, 1, 128, sigma=2.0)
+    scale = 1.0 / math.sqrt(128)
+    for causal in (False, True):
+        O, L = oracle.attention_head(q, k, v, scale, causal)
+        assert np.max(np.abs(O - v[0][None, :])) <= TOL
+        expect = np.array([scale * math.fsum(q[i][c] * k[0][c] for c in range(128)) for i in range(9)])
+        assert np.max(np.abs(L - expect)) <= TOL
+
+
+def pin_causal_row0():
+    q, k, v = rand_head(700, 33, 33, 64, sigma=2.0)
+    O, L = oracle.attention_head(q, k, v, 0.125, True)
+    assert np.max(np.abs(O[0] - v[0])) <= TOL
+    assert abs(L[0] - 0.125 * math.fsum(q[0][c] * k[0][c] for c in range(64))) <= TOL
+    # Row 1 sees exactly keys 0 and 1 (a two-term softmax).
+    s0 = 0.125 * math.fsum(q[1][c] * k[0][c] for c in range(64))
+    s1 = 0.125 * math.fsum(q[1][c] * k[1][c] for c in range(64))
+    w1 = 1.0 / (1.0 + math.exp(s0 - s1))
+    assert np.max(np.abs(O[1] - ((1 - w1) * v[0] + w1 * v[1]))) <= TOL
+
+
+def pin_zero_q_uniform():
+    _, k, v = rand_head(800, 40, 40, 64)
+    q = np.zeros((40, 64))
+    for causal in (False, True):
+        O, L = oracle.attention_head(q, k, v, 0.125, causal)
+        for i in range(40):
+            n = (i + 1) if causal else 40
+            assert np.max(np.abs(O[i] - v[:n].mean(axis=0))) <= TOL
+            assert abs(L[i] - math.log(n)) <= TOL
+
+
+def pin_key_shift():
+    for causal in (False, True):
+        q, k, v = rand_head(900 + causal, 50, 50, 64)
+        w = _rng(901).standard_normal(64)
+        O, L = oracle.attention_head(q, k, v, 0.125, causal)
+        O2, L2 = oracle.attention_head(q, k + w[None, :], v, 0.125, causal)
+        assert np.max(np.abs(O - O2)) <= 1e-11
+        assert np.max(np.abs((L2 - L) - 0.125 * (q @ w))) <= 1e-11
+
+
+def pin_key_permutation():
+    q, k, v = rand_head(1000, 60, 60, 64, sigma=2.0)
+    perm = _rng(1001).permutation(60)
+    O, L = oracle.attention_head(q, k, v, 0.125, False)
+    O2, L2 = oracle.attention_head(q, k[perm], v[perm], 0.125, False)
+    assert np.max(np.abs(O - O2)) <= TOL
+    assert np.max(np.abs(L - L2)) <= TOL
+
+
+def pin_closed_forms():
+    env = {"log": math.log, "tanh": math.tanh, "e": math.e, "exp": math.exp}
+    with open(GOLDEN) as f:
+        cases = json.load(f)["cases"]
+    for c in cases:
+        ev = lambda m: np.array([[eval(x, {}, env) for x in row] for row in m], dtype=np.float64)  # noqa: E731
+        q, k, v = ev(c["q"]), ev(c["k"]), ev(c["v"])
+        O, L = oracle.attention_head(q, k, v, c["scale"], c["causal"])
+        assert np.max(np.abs(O - ev(c["o"]))) <= TOL, c["name"]
+        assert np.max(np.abs(L - np.array([eval(x, {}, env) for x in c["lse"]]))) <= TOL, c["name"]
+
+
+def pin_forward_layout():
+    """attention_forward maps (batch, seq, head, dim) slices to per-head results."""
+    r = _rng(1100)
+    B, S, H, d = 2, 19, 3, 64
+    q = _bf16_like(r.standard_normal((B, S, H, d)))
+    k = _bf16_like(r.standard_normal((B, S + 4, H, d)))
+    v = _bf16_like(r.standard_normal((B, S + 4, H, d)))
+    O, L = oracle.attention_forward(q, k, v, 0.125, False)
+    assert O.shape == (B, S, H, d) and L.shape == (B, H, S)
+    for b in range(B):
+        for h in range(H):
+            Ob, Lb = brute_force_head(q[b, :, h].tolist(), k[b, :, h].tolist(), v[b, :, h].tolist(), 0.125, False)
+            assert np.max(np.abs(O[b, :, h] - Ob)) <= TOL
+            assert np.max(np.abs(L[b, h] - Lb)) <= TOL
+
+
+def pin_rows_subset():
+    q, k, v = rand_head(1200, 300, 300, 64)
+    rows = np.array([0, 1, 127, 128, 255, 299])
+    for causal in (False, True):
+        O, L = oracle.attention_head(q, k, v, 0.125, causal)
+        Os, Ls = oracle.attention_head(q, k, v, 0.125, causal, rows=rows)
+        assert np.max(np.abs(O[rows] - Os)) <= TOL and np.max(np.abs(L[rows] - Ls)) <= TOL
+        Ob, Lb = brute_force_head(q[rows].tolist(), k.tolist(), v.tolist(), 0.125, False) if not causal else (None, None)
+        if not causal:
+            assert np.max(np.abs(Os - Ob)) <= TOL and np.max(np.abs(Ls - Lb)) <= TOL
+
+
+def pin_combine_partials():
+    """Merging key-range partials reproduces the whole (non-causal and causal)."""
+    for causal in (False, True):
+        q, k, v = rand_head(1300 + causal, 80, 200, 64, sigma=2.0)
+        O, L = oracle.attention_head(q, k, v, 0.125, causal)
+        parts_o, parts_l = [], []
+        for a, b in [(0, 50), (50, 51), (51, 130), (130, 200)]:
+            rows = np.arange(80)
+            mask = oracle.visible_mask(rows, 200, causal)[:, a:b]
+            s = 0.125 * np.einsum("ic,jc->ij", q, k[a:b])
+            Ob, Lb = brute_force_masked(s, mask, v[a:b])
+            parts_o.append(Ob)
+            parts_l.append(Lb)
+        Oc, Lc = oracle.combine_partials(parts_o, parts_l)
+        assert np.max(np.abs(Oc - O)) <= 1e-12 and np.max(np.abs(Lc - L)) <= 1e-12
+
+
+def brute_force_masked(s, mask, v):
+    n = s.shape[0]
+    O = np.zeros((n, v.shape[1]))
+    L = np.full(n, -np.inf)
+    for i in range(n):
+        vis = np.nonzero(mask[i])[0]
+        if vis.size == 0:
+            continue
+        m = s[i, vis].max()
+        e = np.exp(s[i, vis] - m)
+        L[i] = m + math.log(math.fsum(e))
+        O[i] = (e @ v[vis]) / math.fsum(e)
+    return O, L
+
+
+ALL_PINS = [v for k_, v in sorted(globals().items()) if k_.startswith("pin_") and callable(v)]

@@ -1,0 +1,72 @@
+"""Plant plausible mistakes in the oracle and check that a pin catches each.
+
+Each mutant is one textual edit of ``oracle/attention.py``, executed as a
+fresh module and swapped into the ``oracle`` package for the duration of the
+test (CPU only; nothing on the GPU side is involved).
+"""
+
+import importlib.util
+import os
+import types
+
+import pytest
+
+import oracle
+import oracle_pins
+
+SRC_PATH = os.path.join(os.path.dirname(oracle.__file__), "attention.py")
+
+MUTANTS = {
+    "dropped_scale": ("return scale * (q @ k.T)", "return (q @ k.T)"),
+    "flipped_sign": ("return scale * (q @ k.T)", "return -scale * (q @ k.T)"),
+    "squared_scale": ("return scale * (q @ k.T)", "return scale * scale * (q @ k.T)"),
+    "causal_off_by_one": ("keys[None, :] <= rows[:, None]", "keys[None, :] < rows[:, None]"),
+    "causal_transposed": ("keys[None, :] <= rows[:, None]", "keys[None, :] >= rows[:, None]"),
+    "causal_ignored": ("    if not causal:\n        return np.ones", "    if True:\n        return np.ones"),
+    "pv_uses_keys": ("= P @ v[:kmax]", "= P @ k[:kmax]"),
+    "lse_log2": ("M + np.log(np.where(L > 0, L, 1.0))", "M + np.log2(np.where(L > 0, L, 1.0))"),
+    "lse_drops_max": ("M + np.log(np.where(L > 0, L, 1.0))", "np.log(np.where(L > 0, L, 1.0))"),
+    "denominator_counts_masked": ("    L = E.sum(axis=1)", "    L = np.exp(s - shift[:, None]).sum(axis=1)"),
+    "unnormalised_p": ("E / np.where(finite, L, 1.0)[:, None]", "E"),
+    "double_shift": ("np.exp(masked - shift[:, None])", "np.exp(masked - 2 * shift[:, None])"),
+    "causal_prefix_short": ("int(min(Sk, r.max() + 1))", "int(min(Sk, r.max()))"),
+    "forward_swaps_kv": ("attention_head(q[b, :, h, :], k[b, :, h, :], v[b, :, h, :]",
+                         "attention_head(q[b, :, h, :], v[b, :, h, :], k[b, :, h, :]"),
+    "forward_lse_transposed_heads": ("LSE[b, h, :] = attention_head", "LSE[b, (h + 1) % H, :] = attention_head"),
+    "combine_plain_mean": ("O = (w[..., None] * Os).sum(axis=0)", "O = Os.mean(axis=0)"),
+    "combine_lse_max_only": ("LSE = np.where(finite, shift + np.log(np.where(tot > 0, tot, 1.0)), -np.inf)",
+                             "LSE = np.where(finite, shift, -np.inf)"),
+}
+
+
+def _load_mutant(old, new):
+    with open(SRC_PATH) as f:
+        src = f.read()
+    assert src.count(old) == 1, f"mutation anchor not unique/present: {old!r}"
+    mod = types.ModuleType("oracle_attention_mutant")
+    exec(compile(src.replace(old, new), SRC_PATH + ":mutant", "exec"), mod.__dict__)
+    return mod
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_mutant_is_caught(name, monkeypatch):
+    mod = _load_mutant(*MUTANTS[name])
+    for fn in ("attention_forward", "attention_head", "attention_rows", "head_probabilities",
+               "head_scores", "visible_mask", "combine_partials"):
+        monkeypatch.setattr(oracle, fn, getattr(mod, fn))
+    caught = []
+    for pin in oracle_pins.ALL_PINS:
+        try:
+            pin()
+        except (AssertionError, ValueError, IndexError):
+            caught.append(pin.__name__)
+    assert caught, f"mutant {name} passed every pin"
+
+
+def test_unmutated_source_passes_all_pins(monkeypatch):
+    mod = _load_mutant("ROW_CHUNK = 1024", "ROW_CHUNK = 1024")
+    for fn in ("attention_forward", "attention_head", "head_probabilities", "head_scores",
+               "visible_mask", "combine_partials"):
+        monkeypatch.setattr(oracle, fn, getattr(mod, fn))
+    for pin in oracle_pins.ALL_PINS:
+        pin()
