@@ -1,0 +1,325 @@
+"""Benchmark of the exact attention forward (BF16) on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config I] [--impl ours|reference]
+
+A step is one attention forward over one batch of the chosen workload (all of
+the hot path: loads, QKᵀ, online softmax, P·V, epilogue — one kernel launch).
+Throughput is counted as 4·B·H·Sq·Sk·d FLOPs per step, halved when causal,
+divided by the kernel time measured with CUDA events on the launching stream.
+Inputs are resident in device memory before timing starts; L2 is flushed
+(a 256 MiB write) between timed steps.  ``e2e`` repeats the measurement
+through the host-buffer C-ABI entry point, with the host↔device copies of
+every step inside the timed region.
+
+Multi-GPU (torchrun, one process per GPU): every rank runs the same workload
+on its own independently seeded batch — attention heads are independent, so
+nothing is exchanged on the data path (weak scaling).  Only the timing uses a
+barrier and a max-reduction.
+
+``--impl reference`` times the CPU fp64 oracle (the reference arm of this
+comparison) on a bounded sample of the same workload.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "attention fwd TFLOPS (BF16, causal & non-causal) and % of GB300 tensor peak"
+CONTRACT_PEAK_TFLOPS = 2250.0  # BF16 dense figure the pages give for the Blackwell tensor core
+FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return json.load(f), "measured"
+    except OSError:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def load_profile_traffic(workload_name):
+    """Per-launch DRAM bytes from the committed ncu summary, if it covers this
+    workload and the current kernel build (else None)."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            data = json.load(f)
+        return data.get(workload_name)
+    except (OSError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples every 200 ms while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None or self.path is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+
+        sm = [num(r[1]) for r in rows if num(r[1]) is not None]
+        mx = [num(r[2]) for r in rows if num(r[2]) is not None]
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            for name, val in zip(names, r[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(rows)}
+
+
+def cpu_oracle_rate(w, budget_s: float, seed_offset: int = 0):
+    """Time the fp64 oracle on whole (b, h) heads of workload ``w`` until about
+    ``budget_s`` seconds of CPU work; return (TFLOP/s, sample description, cores)."""
+    import numpy as np
+
+    import oracle
+    from exact_attention_63_gb300 import inputs
+
+    small = inputs.Workload(w.name, 1, 1, w.Sq, w.Sk, w.d, w.causal, w.sigma_qk, w.sigma_v, w.seed + seed_offset)
+    q, k, v = (oracle.to_f64(t)[0, :, 0, :] for t in inputs.make_inputs(small))
+    per_head = small.flops
+    n, t = 0, 0.0
+    while t < budget_s and n < w.B * w.H:
+        t0 = time.perf_counter()
+        oracle.attention_head(q, k, v, w.scale, w.causal)
+        t += time.perf_counter() - t0
+        n += 1
+    cores = len(os.sched_getaffinity(0))
+    return per_head * n / t / 1e12, f"{n} of {w.B * w.H} heads ({w.Sq}x{w.Sk}, d={w.d}) of the workload, fp64 numpy", cores, t
+
+
+def run_reference(args, w, rank, world):
+    """The reference arm: the CPU oracle, on rank 0 only."""
+    if rank != 0:
+        return
+    budget = max(1.0, 60.0 / max(1, args.steps + args.warmup))
+    for _ in range(args.warmup):
+        cpu_oracle_rate(w, budget / 4)
+    rates, total_t = [], 0.0
+    for _ in range(args.steps):
+        r, sample, cores, t = cpu_oracle_rate(w, budget)
+        rates.append(r)
+        total_t += t
+    value = statistics.mean(rates)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": total_t / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, **{k_: getattr(w, k_) for k_ in ("B", "H", "Sq", "Sk", "d", "causal")}},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--config", type=int, default=2, help="workload index 1-5 (default 2)")
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of oracle time for cpu_baseline")
+    ap.add_argument("--poly-mask", type=lambda x: int(x, 0), default=0, help="override the exp2 split (tuning)")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    from exact_attention_63_gb300 import inputs
+
+    w = inputs.WORKLOADS[args.config]
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        run_reference(args, w, rank, world)
+        return
+
+    import torch
+    import torch.distributed as dist
+
+    from exact_attention_63_gb300 import attn
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+    attn.lib()  # fails loudly if the library is missing
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    seed = w.seed + 1000 * rank
+    q, k, v = inputs.make_inputs(w, seed=seed)
+    qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
+    od = torch.empty_like(qd)
+    ld = torch.empty((w.B, w.H, w.Sq), dtype=torch.float32, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    opts = attn.make_options(poly_exp2_mask=args.poly_mask) if args.poly_mask else None
+    stream = torch.cuda.current_stream()
+
+    def step():
+        attn.attn_fwd(qd, kd, vd, causal=w.causal, scale=w.scale, out=od, lse=ld, options=opts)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    barrier()
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    with ClockSampler(local) as clk:
+        barrier()
+        for i in range(args.steps):
+            flush.zero_()
+            starts[i].record(stream)
+            step()
+            ends[i].record(stream)
+        barrier()
+    if attn.get_status() != 0:
+        raise RuntimeError("kernel reported a device-side error")
+    times_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    total_ms = sum(times_ms)
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    flops = w.flops
+    value = flops * world * args.steps / (total_ms * 1e-3) / 1e12
+    achieved = flops / (statistics.mean(times_ms) * 1e-3) / 1e12
+
+    # ---- end to end through the host-buffer entry point
+    e2e = None
+    if not args.no_e2e:
+        qh, kh, vh = (t_.pin_memory() for t_ in (q, k, v))
+        oh = torch.empty_like(qh).pin_memory()
+        lh = torch.empty((w.B, w.H, w.Sq), dtype=torch.float32).pin_memory()
+        ws = torch.empty(attn.workspace_size(w.B, w.H, w.Sq, w.Sk, w.d), dtype=torch.uint8, device=dev)
+        for _ in range(args.warmup):
+            attn.attn_fwd_host(qh, kh, vh, oh, lh, w.causal, w.scale, ws)
+        barrier()
+        e_s = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        e_e = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        for i in range(args.steps):
+            flush.zero_()
+            e_s[i].record(stream)
+            attn.attn_fwd_host(qh, kh, vh, oh, lh, w.causal, w.scale, ws)
+            e_e[i].record(stream)
+        barrier()
+        e_ms = sum(s.elapsed_time(e) for s, e in zip(e_s, e_e))
+        if world > 1:
+            t = torch.tensor([e_ms], device=dev, dtype=torch.float64)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e_ms = float(t.item())
+        e2e = {"value": flops * world * args.steps / (e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+               "h2d_bytes_per_step": int(3 * q.numel() * 2 * world),
+               "d2h_bytes_per_step": int((q.numel() * 2 + w.B * w.H * w.Sq * 4) * world)}
+
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return
+
+    peaks, peak_kind = load_peaks()
+    peak = float(peaks["bf16_tflops"])
+    traffic = load_profile_traffic(w.name)
+    cpu = None
+    if world == 1 or rank == 0:
+        rate, sample, cores, _ = cpu_oracle_rate(w, args.cpu_budget)
+        cpu = {"value": rate, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": sample}
+    line = {
+        "metric": METRIC,
+        "value": value,
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms_per_step,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "Sq": w.Sq, "Sk": w.Sk, "d": w.d,
+                   "causal": w.causal, "sigma_qk": w.sigma_qk, "seed": w.seed,
+                   "l2": "flushed between timed steps (256 MiB write)",
+                   "parallelism": f"replicas{world}" if world > 1 else "single"},
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak, "traffic": traffic,
+                     "peak_source": f"{peak_kind} bf16_tflops (burst cuBLAS)",
+                     "frac_of_contract_2250": achieved / CONTRACT_PEAK_TFLOPS},
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": args.steps,
+        "clocks": clk.summary(),
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

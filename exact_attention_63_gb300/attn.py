@@ -1,0 +1,169 @@
+"""Thin ctypes binding over the C ABI in ``include/attn_gb300.h``.
+
+Argument marshalling only: shape/dtype checks, device pointers, the current
+CUDA stream.  All of the computation runs in the library's CUDA kernels; if
+the shared library is missing or cannot be loaded, every call raises — there
+is no fallback path.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+
+import torch
+
+_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libattn_gb300.so")
+_lib = None
+
+ATTN_OK = 0
+ERRORS = {
+    -1: "ATTN_ERR_NULL", -2: "ATTN_ERR_SHAPE", -3: "ATTN_ERR_HEAD_DIM", -4: "ATTN_ERR_SCALE",
+    -5: "ATTN_ERR_ALIGN", -6: "ATTN_ERR_ARCH", -7: "ATTN_ERR_LAUNCH", -8: "ATTN_ERR_TIMEOUT",
+    -9: "ATTN_ERR_OPTION", -10: "ATTN_ERR_WORKSPACE",
+}
+
+# Every symbol the header declares (checked by the CPU test-suite).
+EXPORTS = ["attn_fwd", "attn_fwd_ex", "attn_fwd_host", "attn_fwd_host_workspace_size", "attn_get_status",
+           "attn_strerror", "attn_last_cuda_error", "attn_version"]
+
+
+class AttnError(RuntimeError):
+    def __init__(self, code: int, msg: str):
+        super().__init__(f"{ERRORS.get(code, code)}: {msg}")
+        self.code = code
+
+
+class Options(ctypes.Structure):
+    """Mirror of ``attn_options``."""
+    _fields_ = [("struct_size", ctypes.c_size_t), ("rescale_threshold", ctypes.c_float),
+                ("poly_exp2_mask", ctypes.c_uint), ("counters", ctypes.c_void_p), ("timeout_ms", ctypes.c_uint),
+                ("test_flags", ctypes.c_uint)]
+
+
+def lib():
+    """Load the shared library (raises if it is missing)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(_LIB_PATH):
+        raise RuntimeError(f"{_LIB_PATH} is missing: build it with `python -m exact_attention_63_gb300.build`")
+    L = ctypes.CDLL(_LIB_PATH)
+    vp, i, f, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+    L.attn_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp]
+    L.attn_fwd.restype = i
+    L.attn_fwd_ex.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, ctypes.POINTER(Options), vp]
+    L.attn_fwd_ex.restype = i
+    L.attn_fwd_host.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp, sz, vp]
+    L.attn_fwd_host.restype = i
+    L.attn_fwd_host_workspace_size.argtypes = [i, i, i, i, i]
+    L.attn_fwd_host_workspace_size.restype = sz
+    L.attn_get_status.argtypes = [vp]
+    L.attn_get_status.restype = i
+    L.attn_strerror.argtypes = [i]
+    L.attn_strerror.restype = ctypes.c_char_p
+    L.attn_last_cuda_error.argtypes = []
+    L.attn_last_cuda_error.restype = ctypes.c_char_p
+    L.attn_version.argtypes = []
+    L.attn_version.restype = i
+    _lib = L
+    return L
+
+
+def _check(rc: int):
+    if rc != ATTN_OK:
+        L = lib()
+        msg = L.attn_strerror(rc).decode()
+        extra = L.attn_last_cuda_error().decode()
+        raise AttnError(rc, msg + (f" ({extra})" if extra and rc == -7 else ""))
+
+
+def _stream_handle(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _check_inputs(q, k, v):
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous() or t.dim() != 4:
+            raise ValueError(f"{name} must be a contiguous 4-D bf16 CUDA tensor (batch, seq, heads, head_dim)")
+    B, Sq, H, d = q.shape
+    if k.shape != v.shape or k.shape[0] != B or k.shape[2] != H or k.shape[3] != d:
+        raise ValueError(f"shape mismatch: q {tuple(q.shape)}, k {tuple(k.shape)}, v {tuple(v.shape)}")
+    return B, H, Sq, k.shape[1], d
+
+
+def attn_fwd(q, k, v, causal: bool = False, scale: float | None = None, out=None, lse=None, stream=None,
+             options: Options | None = None):
+    """Exact attention forward.  Returns (o [B,Sq,H,d] bf16, lse [B,H,Sq] fp32)."""
+    B, H, Sq, Sk, d = _check_inputs(q, k, v)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, H, Sq), dtype=torch.float32, device=q.device)
+    if out.shape != q.shape or out.dtype != torch.bfloat16 or not out.is_contiguous():
+        raise ValueError("out must be a contiguous bf16 tensor shaped like q")
+    if lse.shape != (B, H, Sq) or lse.dtype != torch.float32 or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous fp32 tensor of shape (B, H, Sq)")
+    L = lib()
+    with torch.cuda.device(q.device):
+        s = _stream_handle(stream)
+        if options is None:
+            rc = L.attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
+                            B, H, Sq, Sk, d, float(scale), int(bool(causal)), s)
+        else:
+            options.struct_size = ctypes.sizeof(Options)
+            rc = L.attn_fwd_ex(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
+                               B, H, Sq, Sk, d, float(scale), int(bool(causal)), ctypes.byref(options), s)
+    _check(rc)
+    return out, lse
+
+
+TEST_WITHHOLD_KV = 1
+
+
+def make_options(rescale_threshold: float = 0.0, poly_exp2_mask: int = 0, counters=None, timeout_ms: int = 0,
+                 test_flags: int = 0):
+    o = Options()
+    o.struct_size = ctypes.sizeof(Options)
+    o.rescale_threshold = rescale_threshold
+    o.poly_exp2_mask = poly_exp2_mask
+    o.counters = None if counters is None else counters.data_ptr()
+    o.timeout_ms = timeout_ms
+    o.test_flags = test_flags
+    return o
+
+
+def workspace_size(B, H, Sq, Sk, d) -> int:
+    return int(lib().attn_fwd_host_workspace_size(B, H, Sq, Sk, d))
+
+
+def attn_fwd_host(q_h, k_h, v_h, o_h, lse_h, causal: bool, scale: float, workspace, stream=None):
+    """End-to-end call on host tensors (pinned CPU bf16 q/k/v/o, fp32 lse).
+
+    ``workspace`` is a CUDA uint8 tensor of at least ``workspace_size(...)``
+    bytes.  Enqueues copies + kernel on the stream; does not synchronise.
+    """
+    B, Sq, H, d = q_h.shape
+    Sk = k_h.shape[1]
+    L = lib()
+    with torch.cuda.device(workspace.device):
+        rc = L.attn_fwd_host(q_h.data_ptr(), k_h.data_ptr(), v_h.data_ptr(), o_h.data_ptr(), lse_h.data_ptr(),
+                             B, H, Sq, Sk, d, float(scale), int(bool(causal)), workspace.data_ptr(),
+                             workspace.numel() * workspace.element_size(), _stream_handle(stream))
+    _check(rc)
+
+
+def get_status(stream=None) -> int:
+    """Synchronise the stream and return/clear the device status (0 = ok)."""
+    return int(lib().attn_get_status(_stream_handle(stream)))
+
+
+def raw_fwd(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, B, H, Sq, Sk, d, scale, causal, stream_ptr=0) -> int:
+    """Direct C-ABI call with integer pointers; returns the status code (tests)."""
+    return int(lib().attn_fwd(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, B, H, Sq, Sk, d, float(scale), int(causal),
+                              ctypes.c_void_p(stream_ptr)))

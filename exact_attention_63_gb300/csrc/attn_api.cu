@@ -1,0 +1,268 @@
+// C ABI of the attention forward library: argument checks, TMA descriptor
+// encoding, kernel dispatch and the device status word.  Declarations and
+// their contracts are in include/attn_gb300.h.
+#include <cmath>
+#include <cstdint>
+#include <cstdio>
+#include <cstring>
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include "attn_gb300.h"
+#include "attn_launch.h"
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+// One status word per device (module-scope device variable: every device that
+// loads the library gets its own copy).  Kernels OR error bits into it.
+__device__ unsigned int g_attn_status;
+
+thread_local char t_last_error[256] = "";
+
+int fail_cuda(cudaError_t e, const char* what) {
+  std::snprintf(t_last_error, sizeof(t_last_error), "%s: %s", what, cudaGetErrorString(e));
+  return ATTN_ERR_LAUNCH;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (fn == nullptr) {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  }
+  return fn;
+}
+
+// 4-D map over a dense bf16 [B, S, H, d] tensor, dims innermost first
+// (d, H, S, B); box (64, 1, 128, 1) = one 128-row × 128-byte slab.
+int encode_bshd(CUtensorMap* m, const void* ptr, int B, int S, int H, int d) {
+  auto enc = get_encode_fn();
+  if (enc == nullptr) {
+    std::snprintf(t_last_error, sizeof(t_last_error), "cuTensorMapEncodeTiled unavailable");
+    return ATTN_ERR_LAUNCH;
+  }
+  const cuuint64_t dims[4] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(S),
+                              static_cast<cuuint64_t>(B)};
+  const cuuint64_t strides[3] = {static_cast<cuuint64_t>(d) * 2, static_cast<cuuint64_t>(H) * d * 2,
+                                 static_cast<cuuint64_t>(S) * H * d * 2};
+  const cuuint32_t box[4] = {64, 1, 128, 1};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(ptr), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    std::snprintf(t_last_error, sizeof(t_last_error), "cuTensorMapEncodeTiled failed (CUresult %d)",
+                  static_cast<int>(r));
+    return ATTN_ERR_LAUNCH;
+  }
+  return ATTN_OK;
+}
+
+struct DeviceInfo {
+  int checked = 0;  // 0 unknown, 1 supported, -1 unsupported
+  unsigned int* status = nullptr;
+};
+DeviceInfo g_dev[kMaxDevices];
+
+int current_device(int* dev_out) {
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    if (e != cudaSuccess) fail_cuda(e, "cudaGetDevice");
+    return ATTN_ERR_ARCH;
+  }
+  DeviceInfo& di = g_dev[dev];
+  if (di.checked == 0) {
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+      return ATTN_ERR_ARCH;
+    if (major != 10 || minor != 3) {
+      di.checked = -1;
+    } else {
+      void* addr = nullptr;
+      e = cudaGetSymbolAddress(&addr, g_attn_status);
+      if (e != cudaSuccess) return fail_cuda(e, "cudaGetSymbolAddress(status)");
+      di.status = static_cast<unsigned int*>(addr);
+      di.checked = 1;
+    }
+  }
+  if (di.checked < 0) return ATTN_ERR_ARCH;
+  *dev_out = dev;
+  return ATTN_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int check_args(const void* q, const void* k, const void* v, const void* o, const void* lse, int B, int H, int Sq,
+               int Sk, int d, float scale) {
+  if (q == nullptr || k == nullptr || v == nullptr || o == nullptr || lse == nullptr) return ATTN_ERR_NULL;
+  if (B < 1 || H < 1 || Sq < 1 || Sk < 1) return ATTN_ERR_SHAPE;
+  const long long n_pairs = (static_cast<long long>(Sq) + 255) / 256;
+  if (static_cast<long long>(B) * H * n_pairs > 0x7FFFFFFFLL) return ATTN_ERR_SHAPE;
+  if (d != 64 && d != 128) return ATTN_ERR_HEAD_DIM;
+  if (!std::isfinite(scale) || !(scale > 0.f)) return ATTN_ERR_SCALE;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse)) return ATTN_ERR_ALIGN;
+  return ATTN_OK;
+}
+
+constexpr float kDefaultTau = 8.0f;
+constexpr unsigned int kDefaultTimeoutMs = 4000;
+
+// Default polynomial-exp2 chunk masks (bit c = 16-column chunk c of a block).
+// Chosen by measurement; see the design notes.
+constexpr uint32_t kDefaultPolyMaskD64 = 0x00u;
+constexpr uint32_t kDefaultPolyMaskD128 = 0x00u;
+
+}  // namespace
+
+extern "C" {
+
+int attn_version(void) { return 100; }
+
+const char* attn_strerror(int status) {
+  switch (status) {
+    case ATTN_OK: return "ok";
+    case ATTN_ERR_NULL: return "a required pointer is NULL";
+    case ATTN_ERR_SHAPE: return "invalid shape (B, H, Sq, Sk must be >= 1 and the grid must fit)";
+    case ATTN_ERR_HEAD_DIM: return "head dim must be 64 or 128";
+    case ATTN_ERR_SCALE: return "scale must be finite and > 0";
+    case ATTN_ERR_ALIGN: return "device pointers must be 16-byte aligned";
+    case ATTN_ERR_ARCH: return "no usable device of compute capability 10.3 (GB300)";
+    case ATTN_ERR_LAUNCH: return "CUDA call failed (see attn_last_cuda_error)";
+    case ATTN_ERR_TIMEOUT: return "a kernel pipeline wait exceeded its time limit; outputs are invalid";
+    case ATTN_ERR_OPTION: return "an attn_options field is out of range";
+    case ATTN_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+    default: return "unknown status";
+  }
+}
+
+const char* attn_last_cuda_error(void) { return t_last_error; }
+
+int attn_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Sq, int Sk, int d,
+                float scale, int causal, const attn_options* opts, cudaStream_t stream) {
+  int rc = check_args(q, k, v, o, lse, B, H, Sq, Sk, d, scale);
+  if (rc != ATTN_OK) return rc;
+  float tau = kDefaultTau;
+  uint32_t poly = (d == 64) ? kDefaultPolyMaskD64 : kDefaultPolyMaskD128;
+  unsigned long long* counters = nullptr;
+  unsigned int timeout_ms = kDefaultTimeoutMs;
+  unsigned int test_flags = 0;
+  if (opts != nullptr) {
+    if (opts->struct_size < sizeof(attn_options)) return ATTN_ERR_OPTION;
+    if (!std::isfinite(opts->rescale_threshold) || opts->rescale_threshold > 32.f) return ATTN_ERR_OPTION;
+    if (opts->rescale_threshold < 0.f) tau = 0.f;
+    else if (opts->rescale_threshold > 0.f) tau = opts->rescale_threshold;
+    if (opts->poly_exp2_mask > 0x1FFu) return ATTN_ERR_OPTION;
+    if (opts->poly_exp2_mask == 0x100u) poly = 0u;
+    else if (opts->poly_exp2_mask != 0u) poly = opts->poly_exp2_mask & 0xFFu;
+    if (opts->counters != nullptr && (reinterpret_cast<uintptr_t>(opts->counters) & 7u) != 0) return ATTN_ERR_ALIGN;
+    counters = opts->counters;
+    if (opts->timeout_ms != 0) timeout_ms = opts->timeout_ms;
+    if ((opts->test_flags & ~ATTN_TEST_WITHHOLD_KV) != 0) return ATTN_ERR_OPTION;
+    test_flags = opts->test_flags;
+  }
+  int dev = -1;
+  rc = current_device(&dev);
+  if (rc != ATTN_OK) return rc;
+
+  attn::LaunchArgs a;
+  std::memset(&a, 0, sizeof(a));
+  if ((rc = encode_bshd(&a.q, q, B, Sq, H, d)) != ATTN_OK) return rc;
+  if ((rc = encode_bshd(&a.k, k, B, Sk, H, d)) != ATTN_OK) return rc;
+  if ((rc = encode_bshd(&a.v, v, B, Sk, H, d)) != ATTN_OK) return rc;
+  if ((rc = encode_bshd(&a.o, o, B, Sq, H, d)) != ATTN_OK) return rc;
+  const int n_pairs = (Sq + 255) / 256;
+  a.p.lse = lse;
+  a.p.status = g_dev[dev].status;
+  a.p.counters = counters;
+  a.p.B = B;
+  a.p.H = H;
+  a.p.Sq = Sq;
+  a.p.Sk = Sk;
+  a.p.n_pairs = n_pairs;
+  a.p.scale_log2 = scale * 1.4426950408889634f;
+  a.p.tau = tau;
+  a.p.poly_mask = poly;
+  a.p.timeout_ns = static_cast<uint64_t>(timeout_ms) * 1000000ull;
+  a.p.test_flags = test_flags;
+  a.grid = n_pairs * B * H;
+  a.causal = causal ? 1 : 0;
+  a.device = dev;
+  a.stream = stream;
+  cudaError_t e = (d == 64) ? attn::launch_fwd_d64(a) : attn::launch_fwd_d128(a);
+  if (e != cudaSuccess) return fail_cuda(e, "attention kernel launch");
+  return ATTN_OK;
+}
+
+int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Sq, int Sk, int d,
+             float scale, int causal, cudaStream_t stream) {
+  return attn_fwd_ex(q, k, v, o, lse, B, H, Sq, Sk, d, scale, causal, nullptr, stream);
+}
+
+size_t attn_fwd_host_workspace_size(int B, int H, int Sq, int Sk, int d) {
+  if (B < 1 || H < 1 || Sq < 1 || Sk < 1 || (d != 64 && d != 128)) return 0;
+  auto up = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
+  const size_t qo = up(static_cast<size_t>(B) * Sq * H * d * 2);
+  const size_t kv = up(static_cast<size_t>(B) * Sk * H * d * 2);
+  const size_t ls = up(static_cast<size_t>(B) * H * Sq * 4);
+  return 2 * qo + 2 * kv + ls;
+}
+
+int attn_fwd_host(const void* q_h, const void* k_h, const void* v_h, void* o_h, float* lse_h, int B, int H, int Sq,
+                  int Sk, int d, float scale, int causal, void* workspace, size_t workspace_bytes,
+                  cudaStream_t stream) {
+  if (q_h == nullptr || k_h == nullptr || v_h == nullptr || o_h == nullptr || lse_h == nullptr) return ATTN_ERR_NULL;
+  if (B < 1 || H < 1 || Sq < 1 || Sk < 1) return ATTN_ERR_SHAPE;
+  if (d != 64 && d != 128) return ATTN_ERR_HEAD_DIM;
+  const size_t need = attn_fwd_host_workspace_size(B, H, Sq, Sk, d);
+  if (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 || workspace_bytes < need)
+    return ATTN_ERR_WORKSPACE;
+  auto up = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
+  const size_t qb = static_cast<size_t>(B) * Sq * H * d * 2, kb = static_cast<size_t>(B) * Sk * H * d * 2;
+  const size_t lb = static_cast<size_t>(B) * H * Sq * 4;
+  char* w = static_cast<char*>(workspace);
+  void* q_d = w;
+  void* k_d = w + up(qb);
+  void* v_d = w + up(qb) + up(kb);
+  void* o_d = w + up(qb) + 2 * up(kb);
+  float* l_d = reinterpret_cast<float*>(w + 2 * up(qb) + 2 * up(kb));
+  cudaError_t e;
+  if ((e = cudaMemcpyAsync(q_d, q_h, qb, cudaMemcpyHostToDevice, stream)) != cudaSuccess) return fail_cuda(e, "copy q");
+  if ((e = cudaMemcpyAsync(k_d, k_h, kb, cudaMemcpyHostToDevice, stream)) != cudaSuccess) return fail_cuda(e, "copy k");
+  if ((e = cudaMemcpyAsync(v_d, v_h, kb, cudaMemcpyHostToDevice, stream)) != cudaSuccess) return fail_cuda(e, "copy v");
+  int rc = attn_fwd(q_d, k_d, v_d, o_d, l_d, B, H, Sq, Sk, d, scale, causal, stream);
+  if (rc != ATTN_OK) return rc;
+  if ((e = cudaMemcpyAsync(o_h, o_d, qb, cudaMemcpyDeviceToHost, stream)) != cudaSuccess) return fail_cuda(e, "copy o");
+  if ((e = cudaMemcpyAsync(lse_h, l_d, lb, cudaMemcpyDeviceToHost, stream)) != cudaSuccess)
+    return fail_cuda(e, "copy lse");
+  return ATTN_OK;
+}
+
+int attn_get_status(cudaStream_t stream) {
+  int dev = -1;
+  int rc = current_device(&dev);
+  if (rc != ATTN_OK) return rc;
+  cudaError_t e = cudaStreamSynchronize(stream);
+  if (e != cudaSuccess) return fail_cuda(e, "cudaStreamSynchronize");
+  unsigned int v = 0;
+  if ((e = cudaMemcpyFromSymbol(&v, g_attn_status, sizeof(v))) != cudaSuccess)
+    return fail_cuda(e, "read status");
+  if (v != 0) {
+    const unsigned int zero = 0;
+    if ((e = cudaMemcpyToSymbol(g_attn_status, &zero, sizeof(zero))) != cudaSuccess)
+      return fail_cuda(e, "clear status");
+    return ATTN_ERR_TIMEOUT;
+  }
+  return ATTN_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,166 @@
+/*
+ * attn_gb300.h — C ABI of the exact attention forward library (GB300, sm_103a).
+ *
+ * The operation (every entry point below computes it):
+ *   O = softmax(scale · Q Kᵀ) V, optionally causal, and the per-row
+ *   log-sum-exp LSE.  Scaled attention softmax(QKᵀ/√d)V is defined in
+ *   "FlashAttention-4 no Blackwell B200 …", section "Por que o Blackwell exige
+ *   mais do que multiplicações rápidas"; the call shape (q, k, v, softmax_scale,
+ *   causal) and the (batch, seq, heads, head_dim) layout follow the Python call
+ *   in "FlashAttention-3: Pipeline Assíncrono …", section "Implementando
+ *   FlashAttention-3 em produção".  The kernels compute it tile by tile with
+ *   an online softmax ("FlashAttention 4: Atenção Mais Rápida …", section
+ *   "Novidades no FlashAttention 4"), so the Sq×Sk score matrix never reaches
+ *   device memory; the result equals the plain definition up to rounding.
+ *
+ * Definitions (per batch b, head h, query row i):
+ *   s_ij   = scale · Σ_c q[b,i,h,c] · k[b,j,h,c]
+ *   V_i    = { j : 0 ≤ j < Sk, and j ≤ i when causal }   (top-left alignment)
+ *   LSE_i  = ln Σ_{j∈V_i} exp(s_ij)                        (natural log)
+ *   O_i    = Σ_{j∈V_i} exp(s_ij − LSE_i) · v[b,j,h,:]
+ *   A row with no visible key (possible only when causal and Sk = 0, which the
+ *   shape checks reject) would get O = 0 and LSE = −inf.
+ *
+ * Layouts (all dense, row-major, no padding):
+ *   q   bf16  [B, Sq, H, d]      k, v  bf16  [B, Sk, H, d]
+ *   o   bf16  [B, Sq, H, d]      lse   fp32  [B, H, Sq]
+ * Arithmetic: bf16 inputs, fp32 accumulation in tensor memory, fp32 softmax,
+ * probabilities rounded to bf16 for the P·V product, row sums accumulated in
+ * fp32 from unrounded probabilities, O rounded once to bf16 (RNE).
+ *
+ * Ownership: the caller owns every buffer; the library allocates nothing per
+ * call and frees nothing.  The library keeps one 4-byte status word per
+ * device in a statically sized device variable.
+ *
+ * Asynchrony and errors: every launching call is asynchronous on `stream`
+ * (0 = the legacy default stream) and returns after the launch.  A negative
+ * return code means the call was rejected BEFORE any launch and nothing was
+ * written.  Device-side failures (a pipeline wait that exceeded its time
+ * limit) are reported later by attn_get_status().
+ *
+ * Requirements: compute capability 10.3 (GB300); d ∈ {64, 128}; device
+ * pointers 16-byte aligned (TMA requirement; 128-byte alignment is faster,
+ * and PyTorch's allocator gives 256 bytes); B, H, Sq, Sk ≥ 1.
+ */
+#ifndef ATTN_GB300_H
+#define ATTN_GB300_H
+
+#include <stddef.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Status codes.  0 = success; negative = rejected or failed. */
+enum {
+  ATTN_OK = 0,
+  ATTN_ERR_NULL = -1,      /* a required pointer is NULL */
+  ATTN_ERR_SHAPE = -2,     /* B, H, Sq or Sk < 1, or a size overflows the kernel's index range */
+  ATTN_ERR_HEAD_DIM = -3,  /* d is not 64 or 128 */
+  ATTN_ERR_SCALE = -4,     /* scale is not finite or not > 0 */
+  ATTN_ERR_ALIGN = -5,     /* a device pointer is not 16-byte aligned */
+  ATTN_ERR_ARCH = -6,      /* no device, or the current device is not compute capability 10.3 */
+  ATTN_ERR_LAUNCH = -7,    /* a CUDA call failed; attn_last_cuda_error() has the message */
+  ATTN_ERR_TIMEOUT = -8,   /* (attn_get_status) a kernel wait exceeded its limit; outputs invalid */
+  ATTN_ERR_OPTION = -9,    /* an attn_options field is out of range */
+  ATTN_ERR_WORKSPACE = -10 /* workspace missing, misaligned or smaller than required */
+};
+
+/*
+ * attn_fwd — exact attention forward on device buffers.
+ *   q, k, v : device, bf16, layouts above (read only).
+ *   o       : device, bf16 [B, Sq, H, d] (written).
+ *   lse     : device, fp32 [B, H, Sq] (written).
+ *   B, H    : batch size and number of heads (K/V have the same H).
+ *   Sq, Sk  : query and key sequence lengths (may differ; any value ≥ 1).
+ *   d       : head dimension, 64 or 128.
+ *   scale   : multiplier of QKᵀ (the pages pass 1/√d), finite and > 0.
+ *   causal  : 0 = full attention; non-zero = key j visible to query i iff j ≤ i.
+ *   stream  : CUDA stream of the caller's context.
+ * Returns ATTN_OK after launching, or a negative code without launching.
+ */
+int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+             int B, int H, int Sq, int Sk, int d, float scale, int causal,
+             cudaStream_t stream);
+
+/*
+ * Tuning and diagnostic options for attn_fwd_ex().  Zero-initialise and set
+ * struct_size = sizeof(attn_options); a zero field means "default".
+ *
+ * rescale_threshold — τ of the conditional online rescaling ("FlashAttention 4:
+ *   Atenção Mais Rápida …", section "Reescalonamento Softmax Online Mais
+ *   Inteligente"): a row's running maximum (log2 domain) is only replaced when
+ *   a new block's maximum exceeds it by more than τ; otherwise probabilities
+ *   up to 2^τ are accumulated against the stale maximum.  The result does not
+ *   depend on τ beyond rounding.  Range [0, 32]; a negative value selects
+ *   τ = 0 (rescale on every increase); 0 selects the default 8.
+ * poly_exp2_mask — which 16-column chunks of each 128-key block compute exp2
+ *   with the FMA-pipe cubic polynomial instead of the MUFU unit ("…", section
+ *   "Exponenciais de Software via Núcleos CUDA").  Bit c (0..7) selects chunk
+ *   c; 0 selects the per-head-dim default; 0x100 forces "no chunk" (all MUFU).
+ * counters — optional device pointer to 2 zero-initialised uint64 values; when
+ *   non-NULL the kernel adds the number of (row, block) rescales to
+ *   counters[0] and the number of (row, block) softmax updates to counters[1].
+ * timeout_ms — time limit of every pipeline wait inside the kernel (default
+ *   4000 ms); on expiry the kernel stops, leaves outputs invalid and flags
+ *   ATTN_ERR_TIMEOUT for attn_get_status().
+ * test_flags — for testing the wait limits only; 0 in normal use.
+ *   ATTN_TEST_WITHHOLD_KV: the loader never issues the K/V copies, so the
+ *   MMA issuer's first wait cannot complete and must run into timeout_ms; the
+ *   kernel then stops cleanly (no fault, TMEM released) and attn_get_status()
+ *   returns ATTN_ERR_TIMEOUT.  Outputs are not written.
+ */
+#define ATTN_TEST_WITHHOLD_KV 1u
+typedef struct attn_options {
+  size_t struct_size;
+  float rescale_threshold;
+  unsigned int poly_exp2_mask;
+  unsigned long long* counters;
+  unsigned int timeout_ms;
+  unsigned int test_flags;
+} attn_options;
+
+/* attn_fwd with options (opts may be NULL: same as attn_fwd). */
+int attn_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse,
+                int B, int H, int Sq, int Sk, int d, float scale, int causal,
+                const attn_options* opts, cudaStream_t stream);
+
+/*
+ * attn_fwd_host — the same operation on HOST buffers, end to end.
+ *   q_h, k_h, v_h : host bf16 inputs (layouts above); o_h, lse_h : host outputs.
+ *   workspace     : caller-owned DEVICE buffer of at least
+ *                   attn_fwd_host_workspace_size(B, H, Sq, Sk, d) bytes,
+ *                   256-byte aligned; it holds device copies of q, k, v, o, lse.
+ * Enqueues, on `stream`: three host→device copies, the attention kernel, and
+ * two device→host copies (one cudaMemcpyAsync per buffer).  The call returns
+ * after enqueueing; synchronise `stream` before reading o_h / lse_h.  Host
+ * buffers should be page-locked for the copies to be asynchronous.
+ */
+size_t attn_fwd_host_workspace_size(int B, int H, int Sq, int Sk, int d);
+int attn_fwd_host(const void* q_h, const void* k_h, const void* v_h, void* o_h, float* lse_h,
+                  int B, int H, int Sq, int Sk, int d, float scale, int causal,
+                  void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * attn_get_status — synchronises `stream`, then returns and clears the current
+ * device's status word: ATTN_OK, or ATTN_ERR_TIMEOUT if any kernel launched
+ * by this library on this device since the last call hit a wait limit, or
+ * ATTN_ERR_LAUNCH if the synchronisation itself failed.
+ */
+int attn_get_status(cudaStream_t stream);
+
+/* Static description of a status code (never NULL). */
+const char* attn_strerror(int status);
+
+/* Message of the last CUDA error seen by this thread's library calls ("" if none). */
+const char* attn_last_cuda_error(void);
+
+/* Library version as MAJOR*10000 + MINOR*100 + PATCH. */
+int attn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ATTN_GB300_H */

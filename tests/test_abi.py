@@ -1,0 +1,110 @@
+"""C-ABI library: it loads, exports every declared symbol, and rejects bad
+arguments before touching the GPU (no GPU needed for any of this)."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+from exact_attention_63_gb300 import attn
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "attn_gb300.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    if not os.path.exists(attn._LIB_PATH):
+        from exact_attention_63_gb300 import build
+
+        build.build()
+    return attn.lib()
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?[a-z_]+\**\s+\**(attn_[a-z0-9_]+)\s*\(", src, flags=re.M)))
+
+
+def test_header_declares_expected_api():
+    assert declared_functions() == sorted(attn.EXPORTS)
+
+
+def test_library_exports_every_declared_symbol(L):
+    for name in declared_functions():
+        assert hasattr(L, name), name
+
+
+def test_version_and_strerror(L):
+    assert L.attn_version() >= 100
+    for code in [0, *attn.ERRORS]:
+        assert L.attn_strerror(code)
+    assert L.attn_strerror(12345) == b"unknown status"
+
+
+A = 0x10000  # a fake, 16-byte aligned "device" address: never dereferenced
+
+
+@pytest.mark.parametrize("args,expect", [
+    ((0, A, A, A, A, 1, 1, 8, 8, 64, 0.125, 0), -1),
+    ((A, A, A, A, 0, 1, 1, 8, 8, 64, 0.125, 0), -1),
+    ((A, A, A, A, A, 0, 1, 8, 8, 64, 0.125, 0), -2),
+    ((A, A, A, A, A, 1, -1, 8, 8, 64, 0.125, 0), -2),
+    ((A, A, A, A, A, 1, 1, 0, 8, 64, 0.125, 0), -2),
+    ((A, A, A, A, A, 1, 1, 8, 0, 64, 0.125, 0), -2),
+    ((A, A, A, A, A, 65536, 65536, 4096, 8, 64, 0.125, 0), -2),
+    ((A, A, A, A, A, 1, 1, 8, 8, 96, 0.125, 0), -3),
+    ((A, A, A, A, A, 1, 1, 8, 8, 256, 0.125, 0), -3),
+    ((A, A, A, A, A, 1, 1, 8, 8, 64, float("nan"), 0), -4),
+    ((A, A, A, A, A, 1, 1, 8, 8, 64, float("inf"), 0), -4),
+    ((A, A, A, A, A, 1, 1, 8, 8, 64, 0.0, 0), -4),
+    ((A, A, A, A, A, 1, 1, 8, 8, 64, -1.0, 0), -4),
+    ((A + 8, A, A, A, A, 1, 1, 8, 8, 64, 0.125, 0), -5),
+    ((A, A, A, A, A + 4, 1, 1, 8, 8, 64, 0.125, 0), -5),
+])
+def test_rejected_before_launch(L, args, expect):
+    assert attn.raw_fwd(*args) == expect
+
+
+def test_bad_options_rejected(L):
+    o = attn.make_options(rescale_threshold=float("nan"))
+    rc = L.attn_fwd_ex(A, A, A, A, A, 1, 1, 8, 8, 64, 0.125, 0, ctypes.byref(o), None)
+    assert rc == -9
+    o = attn.make_options(rescale_threshold=40.0)
+    assert L.attn_fwd_ex(A, A, A, A, A, 1, 1, 8, 8, 64, 0.125, 0, ctypes.byref(o), None) == -9
+    o = attn.make_options(poly_exp2_mask=0x200)
+    assert L.attn_fwd_ex(A, A, A, A, A, 1, 1, 8, 8, 64, 0.125, 0, ctypes.byref(o), None) == -9
+    o = attn.make_options()
+    o.struct_size = 4
+    assert L.attn_fwd_ex(A, A, A, A, A, 1, 1, 8, 8, 64, 0.125, 0, ctypes.byref(o), None) == -9
+
+
+def test_workspace_size_and_checks(L):
+    n = attn.workspace_size(2, 3, 100, 50, 64)
+    up = lambda x: (x + 255) // 256 * 256  # noqa: E731
+    assert n == 2 * up(2 * 100 * 3 * 64 * 2) + 2 * up(2 * 50 * 3 * 64 * 2) + up(2 * 3 * 100 * 4)
+    assert attn.workspace_size(1, 1, 1, 1, 96) == 0
+    rc = L.attn_fwd_host(A, A, A, A, A, 2, 3, 100, 50, 64, 0.125, 0, A, n - 1, None)
+    assert rc == -10
+    rc = L.attn_fwd_host(A, A, A, A, A, 2, 3, 100, 50, 64, 0.125, 0, A + 16, n, None)
+    assert rc == -10
+    rc = L.attn_fwd_host(0, A, A, A, A, 2, 3, 100, 50, 64, 0.125, 0, A, n, None)
+    assert rc == -1
+
+
+def test_no_gpu_reports_arch_error(L):
+    import torch
+
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    assert attn.raw_fwd(A, A, A, A, A, 1, 1, 8, 8, 64, 0.125, 0) == -6
+
+
+def test_python_binding_rejects_cpu_tensors():
+    import torch
+
+    q = torch.zeros(1, 8, 1, 64, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        attn.attn_fwd(q, q, q)
