@@ -23,6 +23,7 @@ comparison) on a bounded sample of the same workload.
 from __future__ import annotations
 
 import argparse
+import datetime
 import json
 import math
 import os
@@ -64,7 +65,7 @@ def load_profile_traffic(workload_name):
 class ClockSampler:
     """nvidia-smi clock/throttle samples every 200 ms while running."""
 
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
@@ -79,7 +80,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "200"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+                 "-lms", "100"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
         except OSError:
             self.proc = None
         time.sleep(0.3)
@@ -93,18 +94,36 @@ class ClockSampler:
             except subprocess.TimeoutExpired:
                 self.proc.kill()
 
+    def mark(self, which):
+        setattr(self, which, time.time())
+
     def summary(self):
+        """Median SM clock and throttle reasons over the samples taken inside
+        [t_start, t_end] (marked around the timed region); if the region was
+        shorter than the sampling interval, the sample nearest to it."""
         if self.proc is None or self.path is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
         rows = []
         with open(self.path) as f:
             for line in f:
                 parts = [p.strip() for p in line.split(",")]
-                if len(parts) >= 9:
-                    rows.append(parts)
+                if len(parts) >= 10:
+                    try:
+                        ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                    except ValueError:
+                        continue
+                    rows.append((ts, parts[1:]))
         os.unlink(self.path)
         if not rows:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        t0, t1 = getattr(self, "t_start", rows[0][0]), getattr(self, "t_end", rows[-1][0])
+        inside = [r for ts, r in rows if t0 <= ts <= t1]
+        window = "timed region"
+        if not inside:
+            mid = 0.5 * (t0 + t1)
+            inside = [min(rows, key=lambda x: abs(x[0] - mid))[1]]
+            window = "nearest sample to the timed region"
+        rows = inside
 
         def num(x):
             try:
@@ -121,40 +140,53 @@ class ClockSampler:
                 if val.lower() == "active":
                     reasons.add(name)
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
-                "reasons": sorted(reasons), "samples": len(rows)}
+                "reasons": sorted(reasons), "samples": len(rows), "window": window}
 
 
-def cpu_oracle_rate(w, budget_s: float, seed_offset: int = 0):
-    """Time the fp64 oracle on whole (b, h) heads of workload ``w`` until about
-    ``budget_s`` seconds of CPU work; return (TFLOP/s, sample description, cores)."""
+def cpu_oracle_rate(w, budget_s: float, start_chunk: int = 0):
+    """Time the fp64 oracle on 128-row chunks of one head shaped like workload
+    ``w`` (same Sq, Sk, d, mask and value distribution) for about ``budget_s``
+    seconds.  FLOPs are counted per row with the same convention as the GPU
+    (4·d per visible key), so causal rows count what they see.
+    Returns (TFLOP/s, sample description, cores, seconds, chunks)."""
     import numpy as np
 
     import oracle
     from exact_attention_63_gb300 import inputs
 
-    small = inputs.Workload(w.name, 1, 1, w.Sq, w.Sk, w.d, w.causal, w.sigma_qk, w.sigma_v, w.seed + seed_offset)
+    small = inputs.Workload(w.name, 1, 1, w.Sq, w.Sk, w.d, w.causal, w.sigma_qk, w.sigma_v, w.seed)
     q, k, v = (oracle.to_f64(t)[0, :, 0, :] for t in inputs.make_inputs(small))
-    per_head = small.flops
-    n, t = 0, 0.0
-    while t < budget_s and n < w.B * w.H:
+    nch = (w.Sq + 127) // 128
+    n, t, flops = 0, 0.0, 0.0
+    while n == 0 or t < budget_s:
+        c = (start_chunk + 37 * n) % nch
+        rows = np.arange(c * 128, min(w.Sq, c * 128 + 128))
         t0 = time.perf_counter()
-        oracle.attention_head(q, k, v, w.scale, w.causal)
+        oracle.attention_head(q, k, v, w.scale, w.causal, rows=rows)
         t += time.perf_counter() - t0
+        vis = np.minimum(w.Sk, rows + 1) if w.causal else np.full(rows.shape, w.Sk)
+        flops += 4.0 * w.d * float(vis.sum())
         n += 1
     cores = len(os.sched_getaffinity(0))
-    return per_head * n / t / 1e12, f"{n} of {w.B * w.H} heads ({w.Sq}x{w.Sk}, d={w.d}) of the workload, fp64 numpy", cores, t
+    sample = (f"{n} chunks of 128 query rows of one {w.Sq}x{w.Sk} d={w.d}{' causal' if w.causal else ''} head "
+              f"(same shape and distribution as the workload), fp64 numpy, {t:.1f} s")
+    return flops / t / 1e12, sample, cores, t, n
 
 
 def run_reference(args, w, rank, world):
     """The reference arm: the CPU oracle, on rank 0 only."""
     if rank != 0:
         return
-    budget = max(1.0, 60.0 / max(1, args.steps + args.warmup))
+    # Whole run bounded to about two minutes of CPU time.
+    budget = max(0.02, 120.0 / max(1, args.steps + args.warmup))
+    chunk = 0
     for _ in range(args.warmup):
-        cpu_oracle_rate(w, budget / 4)
+        *_, n = cpu_oracle_rate(w, budget, chunk)
+        chunk += n
     rates, total_t = [], 0.0
     for _ in range(args.steps):
-        r, sample, cores, t = cpu_oracle_rate(w, budget)
+        r, sample, cores, t, n = cpu_oracle_rate(w, budget, chunk)
+        chunk += n
         rates.append(r)
         total_t += t
     value = statistics.mean(rates)
@@ -173,8 +205,8 @@ def run_reference(args, w, rank, world):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--config", type=int, default=2, help="workload index 1-5 (default 2)")
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-e2e", action="store_true")
@@ -199,6 +231,7 @@ def main():
     import torch.distributed as dist
 
     from exact_attention_63_gb300 import attn
+    from exact_attention_63_gb300 import dist as adist
 
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
@@ -211,7 +244,7 @@ def main():
             dist.barrier()
         torch.cuda.synchronize()
 
-    seed = w.seed + 1000 * rank
+    seed = adist.rank_seed(w.seed, rank)
     q, k, v = inputs.make_inputs(w, seed=seed)
     qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
     od = torch.empty_like(qd)
@@ -232,20 +265,18 @@ def main():
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     with ClockSampler(local) as clk:
         barrier()
+        clk.mark("t_start")
         for i in range(args.steps):
             flush.zero_()
             starts[i].record(stream)
             step()
             ends[i].record(stream)
         barrier()
+        clk.mark("t_end")
     if attn.get_status() != 0:
         raise RuntimeError("kernel reported a device-side error")
     times_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
-    total_ms = sum(times_ms)
-    if world > 1:
-        t = torch.tensor([total_ms], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = adist.max_over_ranks(sum(times_ms), device=dev)
     ms_per_step = total_ms / args.steps
     flops = w.flops
     value = flops * world * args.steps / (total_ms * 1e-3) / 1e12
@@ -269,11 +300,7 @@ def main():
             attn.attn_fwd_host(qh, kh, vh, oh, lh, w.causal, w.scale, ws)
             e_e[i].record(stream)
         barrier()
-        e_ms = sum(s.elapsed_time(e) for s, e in zip(e_s, e_e))
-        if world > 1:
-            t = torch.tensor([e_ms], device=dev, dtype=torch.float64)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e_ms = float(t.item())
+        e_ms = adist.max_over_ranks(sum(s.elapsed_time(e) for s, e in zip(e_s, e_e)), device=dev)
         e2e = {"value": flops * world * args.steps / (e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
                "h2d_bytes_per_step": int(3 * q.numel() * 2 * world),
                "d2h_bytes_per_step": int((q.numel() * 2 + w.B * w.H * w.Sq * 4) * world)}
@@ -287,8 +314,8 @@ def main():
     peak = float(peaks["bf16_tflops"])
     traffic = load_profile_traffic(w.name)
     cpu = None
-    if world == 1 or rank == 0:
-        rate, sample, cores, _ = cpu_oracle_rate(w, args.cpu_budget)
+    if args.cpu_budget > 0:
+        rate, sample, cores, _, _ = cpu_oracle_rate(w, args.cpu_budget)
         cpu = {"value": rate, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": sample}
     line = {
         "metric": METRIC,
