@@ -21,12 +21,15 @@ ATTN_OK = 0
 ERRORS = {
     -1: "ATTN_ERR_NULL", -2: "ATTN_ERR_SHAPE", -3: "ATTN_ERR_HEAD_DIM", -4: "ATTN_ERR_SCALE",
     -5: "ATTN_ERR_ALIGN", -6: "ATTN_ERR_ARCH", -7: "ATTN_ERR_LAUNCH", -8: "ATTN_ERR_TIMEOUT",
-    -9: "ATTN_ERR_OPTION", -10: "ATTN_ERR_WORKSPACE",
+    -9: "ATTN_ERR_OPTION", -10: "ATTN_ERR_WORKSPACE", -11: "ATTN_ERR_STATIC_LIMIT",
 }
 
 # Every symbol the header declares (checked by the CPU test-suite).
 EXPORTS = ["attn_fwd", "attn_fwd_ex", "attn_fwd_host", "attn_fwd_host_workspace_size", "attn_get_status",
-           "attn_strerror", "attn_last_cuda_error", "attn_version"]
+           "attn_strerror", "attn_last_cuda_error", "attn_version", "attn_fwd_host_static"]
+
+# Size of the library's fixed device staging area used by attn_fwd_host_static.
+STATIC_WORKSPACE_BYTES = 32 << 20
 
 
 class AttnError(RuntimeError):
@@ -59,6 +62,8 @@ def lib():
     L.attn_fwd_host.restype = i
     L.attn_fwd_host_workspace_size.argtypes = [i, i, i, i, i]
     L.attn_fwd_host_workspace_size.restype = sz
+    L.attn_fwd_host_static.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp]
+    L.attn_fwd_host_static.restype = i
     L.attn_get_status.argtypes = [vp]
     L.attn_get_status.restype = i
     L.attn_strerror.argtypes = [i]
@@ -155,6 +160,18 @@ def attn_fwd_host(q_h, k_h, v_h, o_h, lse_h, causal: bool, scale: float, workspa
         rc = L.attn_fwd_host(q_h.data_ptr(), k_h.data_ptr(), v_h.data_ptr(), o_h.data_ptr(), lse_h.data_ptr(),
                              B, H, Sq, Sk, d, float(scale), int(bool(causal)), workspace.data_ptr(),
                              workspace.numel() * workspace.element_size(), _stream_handle(stream))
+    _check(rc)
+
+
+def attn_fwd_host_static(q_h, k_h, v_h, o_h, lse_h, causal: bool, scale: float, stream=None):
+    """End-to-end call on host tensors with no device workspace from the
+    caller: the library stages the data in its own fixed 32 MiB device array
+    (for callers that cannot allocate device memory).  Does not synchronise."""
+    B, Sq, H, d = q_h.shape
+    Sk = k_h.shape[1]
+    rc = lib().attn_fwd_host_static(q_h.data_ptr(), k_h.data_ptr(), v_h.data_ptr(), o_h.data_ptr(),
+                                    lse_h.data_ptr(), B, H, Sq, Sk, d, float(scale), int(bool(causal)),
+                                    _stream_handle(stream))
     _check(rc)
 
 

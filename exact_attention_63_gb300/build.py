@@ -2,7 +2,7 @@
 
     python -m exact_attention_63_gb300.build
 
-Compiles the three translation units in parallel and links
+Compiles the translation units in parallel and links
 ``exact_attention_63_gb300/libattn_gb300.so``.  The library is linked
 against the shared CUDA runtime so it uses the same runtime instance as the
 host process (PyTorch loads ``libcudart.so.13`` too).
@@ -23,7 +23,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(ROOT, "_build")
 LIB_NAME = "libattn_gb300.so"
 LIB_PATH = os.path.join(PKG, LIB_NAME)
-SOURCES = ["attn_api.cu", "attn_fwd_d64.cu", "attn_fwd_d128.cu"]
+SOURCES = ["attn_api.cu", "attn_fwd_d64.cu", "attn_fwd_d128.cu", "attn_static.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

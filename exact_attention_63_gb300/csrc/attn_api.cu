@@ -141,6 +141,7 @@ const char* attn_strerror(int status) {
     case ATTN_ERR_TIMEOUT: return "a kernel pipeline wait exceeded its time limit; outputs are invalid";
     case ATTN_ERR_OPTION: return "an attn_options field is out of range";
     case ATTN_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+    case ATTN_ERR_STATIC_LIMIT: return "problem larger than the static workspace of attn_fwd_host_static";
     default: return "unknown status";
   }
 }

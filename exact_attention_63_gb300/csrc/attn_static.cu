@@ -1,0 +1,56 @@
+// attn_fwd_host_static: the host-buffer attention call for callers that
+// cannot allocate device memory.  The device staging area for q, k, v, o and
+// lse is a fixed-size array that is part of this library's device image, so
+// it exists as soon as the library's module is loaded on a device.
+#include <cstdint>
+#include <cstdio>
+
+#include <cuda_runtime.h>
+
+#include "attn_gb300.h"
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr size_t kStaticBytes = ATTN_STATIC_WORKSPACE_BYTES;
+
+// Staging area of attn_fwd_host_static.  In host code this name is only a
+// handle for the runtime; the device address comes from cudaGetSymbolAddress.
+__device__ __align__(256) unsigned char g_static_workspace[kStaticBytes];
+
+// Device address of g_static_workspace, looked up once per device.
+void* g_static_addr[kMaxDevices] = {};
+
+}  // namespace
+
+extern "C" int attn_fwd_host_static(const void* q_h, const void* k_h, const void* v_h, void* o_h, float* lse_h,
+                                    int B, int H, int Sq, int Sk, int d, float scale, int causal,
+                                    cudaStream_t stream) {
+  if (q_h == nullptr || k_h == nullptr || v_h == nullptr || o_h == nullptr || lse_h == nullptr) return ATTN_ERR_NULL;
+  if (B < 1 || H < 1 || Sq < 1 || Sk < 1) return ATTN_ERR_SHAPE;
+  if (d != 64 && d != 128) return ATTN_ERR_HEAD_DIM;
+  const size_t need = attn_fwd_host_workspace_size(B, H, Sq, Sk, d);
+  if (need == 0 || need > kStaticBytes) return ATTN_ERR_STATIC_LIMIT;
+
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return ATTN_ERR_ARCH;
+  int major = 0, minor = 0;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess || major != 10 ||
+      minor != 3)
+    return ATTN_ERR_ARCH;
+
+  // Set-up, once per device, with that device current: translate the array's
+  // host-side handle into its device address.  This allocates nothing.
+  if (g_static_addr[dev] == nullptr) {
+    void* addr = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&addr, g_static_workspace);
+    if (e != cudaSuccess || addr == nullptr) return ATTN_ERR_LAUNCH;
+    g_static_addr[dev] = addr;
+  }
+  // Every byte the kernel and the copies read back is written earlier in the
+  // same call (q/k/v by the host-to-device copies, o/lse by the kernel), so
+  // nothing in the array needs clearing between calls.
+  return attn_fwd_host(q_h, k_h, v_h, o_h, lse_h, B, H, Sq, Sk, d, scale, causal, g_static_addr[dev],
+                       kStaticBytes, stream);
+}

@@ -64,7 +64,8 @@ enum {
   ATTN_ERR_LAUNCH = -7,    /* a CUDA call failed; attn_last_cuda_error() has the message */
   ATTN_ERR_TIMEOUT = -8,   /* (attn_get_status) a kernel wait exceeded its limit; outputs invalid */
   ATTN_ERR_OPTION = -9,    /* an attn_options field is out of range */
-  ATTN_ERR_WORKSPACE = -10 /* workspace missing, misaligned or smaller than required */
+  ATTN_ERR_WORKSPACE = -10, /* workspace missing, misaligned or smaller than required */
+  ATTN_ERR_STATIC_LIMIT = -11 /* problem needs more than ATTN_STATIC_WORKSPACE_BYTES (attn_fwd_host_static) */
 };
 
 /*
@@ -141,6 +142,36 @@ size_t attn_fwd_host_workspace_size(int B, int H, int Sq, int Sk, int d);
 int attn_fwd_host(const void* q_h, const void* k_h, const void* v_h, void* o_h, float* lse_h,
                   int B, int H, int Sq, int Sk, int d, float scale, int causal,
                   void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * attn_fwd_host_static — attn_fwd_host for callers that cannot allocate device
+ * memory.  The pages have no counterpart to this call; it exists for
+ * integration.  Some host programs may not call cudaMalloc at all: plugins
+ * whose framework owns every byte of device memory through its own allocator
+ * (an extra cudaMalloc bypasses its accounting and can fail once the pool has
+ * reserved the device), and latency-critical or certified code paths that
+ * forbid allocation after start-up (cudaMalloc may synchronise the device).
+ * Such callers pass host inputs and outputs only; the device staging area is
+ * a fixed array of ATTN_STATIC_WORKSPACE_BYTES (32 MiB) inside this library,
+ * which every GPU that loads the library keeps until the process exits.
+ *   Arguments and layouts as attn_fwd_host, without the workspace.
+ *   Problems whose attn_fwd_host_workspace_size() exceeds
+ *   ATTN_STATIC_WORKSPACE_BYTES are rejected with ATTN_ERR_STATIC_LIMIT
+ *   before anything is enqueued.
+ *   The first call on each device looks up the array's device address
+ *   (cudaGetSymbolAddress, no allocation) with that device current; make that
+ *   first call before any stream capture on the device.
+ *   All calls share the one array, which keeps the last call's contents:
+ *   calls whose GPU work overlaps (different streams without ordering, or
+ *   several host threads) race on it and must be serialised by the caller.
+ *   Nothing in the array needs to start at zero.
+ * Enqueues the same copies and kernel as attn_fwd_host; returns after
+ * enqueueing, synchronise `stream` before reading o_h / lse_h.
+ */
+#define ATTN_STATIC_WORKSPACE_BYTES (32u << 20)
+int attn_fwd_host_static(const void* q_h, const void* k_h, const void* v_h, void* o_h, float* lse_h,
+                         int B, int H, int Sq, int Sk, int d, float scale, int causal,
+                         cudaStream_t stream);
 
 /*
  * attn_get_status — synchronises `stream`, then returns and clears the current
