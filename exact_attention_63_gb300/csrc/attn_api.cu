@@ -117,8 +117,8 @@ int check_args(const void* q, const void* k, const void* v, const void* o, const
 constexpr float kDefaultTau = 8.0f;
 constexpr unsigned int kDefaultTimeoutMs = 4000;
 
-// Default polynomial-exp2 chunk masks (bit c = 16-column chunk c of a block).
-// Chosen by measurement; see the design notes.
+// Default polynomial-exp2 chunk masks (bit c = 16-column chunk c of a block),
+// chosen by measurement on GB300 (whose MUFU unit is not the limiting pipe).
 constexpr uint32_t kDefaultPolyMaskD64 = 0x00u;
 constexpr uint32_t kDefaultPolyMaskD128 = 0x00u;
 
@@ -162,9 +162,9 @@ int attn_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse
     if (!std::isfinite(opts->rescale_threshold) || opts->rescale_threshold > 32.f) return ATTN_ERR_OPTION;
     if (opts->rescale_threshold < 0.f) tau = 0.f;
     else if (opts->rescale_threshold > 0.f) tau = opts->rescale_threshold;
-    if (opts->poly_exp2_mask > 0x1FFu) return ATTN_ERR_OPTION;
     if (opts->poly_exp2_mask == 0x100u) poly = 0u;
-    else if (opts->poly_exp2_mask != 0u) poly = opts->poly_exp2_mask & 0xFFu;
+    else if (opts->poly_exp2_mask != 0u) poly = opts->poly_exp2_mask;
+    if (!attn::poly_mask_supported(poly)) return ATTN_ERR_OPTION;
     if (opts->counters != nullptr && (reinterpret_cast<uintptr_t>(opts->counters) & 7u) != 0) return ATTN_ERR_ALIGN;
     counters = opts->counters;
     if (opts->timeout_ms != 0) timeout_ms = opts->timeout_ms;
@@ -192,14 +192,15 @@ int attn_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse
   a.p.n_pairs = n_pairs;
   a.p.scale_log2 = scale * 1.4426950408889634f;
   a.p.tau = tau;
-  a.p.poly_mask = poly;
   a.p.timeout_ns = static_cast<uint64_t>(timeout_ms) * 1000000ull;
   a.p.test_flags = test_flags;
   a.grid = n_pairs * B * H;
-  a.causal = causal ? 1 : 0;
+  a.poly = poly;
   a.device = dev;
   a.stream = stream;
-  cudaError_t e = (d == 64) ? attn::launch_fwd_d64(a) : attn::launch_fwd_d128(a);
+  cudaError_t e;
+  if (d == 64) e = causal ? attn::launch_fwd_d64_causal(a) : attn::launch_fwd_d64(a);
+  else e = causal ? attn::launch_fwd_d128_causal(a) : attn::launch_fwd_d128(a);
   if (e != cudaSuccess) return fail_cuda(e, "attention kernel launch");
   return ATTN_OK;
 }

@@ -61,7 +61,10 @@ constexpr unsigned int kStatusTimeout = 1u;
 // Wait until the phase with the given parity of `bar` has completed.  Returns
 // false (after raising the CTA abort flag and the device status bit) when the
 // time limit passes, or when another thread of the CTA has already aborted.
-static __device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, const WaitCtx& c) {
+// Inlined at every call site: an out-of-line call costs the waiting thread a
+// register save/restore on every slow path.
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, const WaitCtx& c) {
+  if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
@@ -74,11 +77,6 @@ static __device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, con
       }
     }
   }
-}
-
-__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, const WaitCtx& c) {
-  if (mbar_try_wait(bar, parity)) return true;
-  return wait_slow(bar, parity, c);
 }
 
 // -------------------------------------------------------------------- TMA

@@ -11,7 +11,8 @@
 //   warps 4-7  softmax group 1 — one thread per row of tile 1
 //   warp  8    loader — TMA loads of Q0/Q1 once, then K_j, V_j into a ring of
 //              shared-memory slots guarded by full/empty mbarriers
-//   warp  9    MMA issuer — tcgen05.mma S_t = Q_t K_jᵀ and O_t += P_t V_j,
+//   warp  9    MMA issuer (one thread) — tcgen05.mma S_t = Q_t K_jᵀ and
+//              O_t += P_t V_j for both tiles in strict alternation,
 //              accumulators in tensor memory (TMEM)
 // This is the load → MMA → softmax → rescale → store pipeline of
 // "FlashAttention 4: …", section "Novidades no FlashAttention 4" (warp
@@ -30,7 +31,7 @@
 // Ordering rules the protocol relies on:
 //  * tcgen05.mma operations issued by one thread execute in issue order, and
 //    tcgen05.commit arrives only after all earlier ones complete.  The MMA
-//    warp issues P_t(j−1)·V before S_t(j) = Q_t K_jᵀ, so S_t(j) never
+//    thread issues P_t(j−1)·V before S_t(j) = Q_t K_jᵀ, so S_t(j) never
 //    overwrites P_t(j−1) early, and when s_full[t] fires for block j the O_t
 //    update of block j−1 is finished — the softmax thread may rescale O_t.
 //  * O_t is not touched by the MMA again until p_full[t] is signalled.
@@ -47,7 +48,7 @@ constexpr int kBM = 128;       // query rows per tile (= TMEM lanes)
 constexpr int kBN = 128;       // keys per block
 constexpr int kThreads = 320;  // 8 softmax warps + loader + MMA issuer
 constexpr int kLoaderWarp = 8;
-constexpr int kMmaWarp = 9;
+constexpr int kMmaWarp = 9;    // MMA issuer; also allocates TMEM
 constexpr uint32_t kTmemCols = 512;
 
 struct FwdParams {
@@ -58,7 +59,6 @@ struct FwdParams {
   int n_pairs;             // ceil(Sq / 256)
   float scale_log2;        // scale · log2(e)
   float tau;               // rescale threshold, log2 domain
-  uint32_t poly_mask;      // bit c: 16-column chunk c uses the polynomial exp2
   uint64_t timeout_ns;
   uint32_t test_flags;     // bit 0: loader withholds K/V (exercises the wait limit)
 };
@@ -88,7 +88,9 @@ __device__ __forceinline__ void reg_fence32(uint32_t (&r)[32]) {
                  "+r"(r[i + 5]), "+r"(r[i + 6]), "+r"(r[i + 7]));
 }
 
-template <int D, bool CAUSAL>
+// POLY: bit c selects the FMA-pipe polynomial exp2 for 16-column chunk c of
+// every 128-key block (compile time, so the exp loop is one basic block).
+template <int D, bool CAUSAL, uint32_t POLY>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
@@ -219,23 +221,28 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       constexpr uint32_t idS = idesc_bf16(kBM, kBN, false);
       constexpr uint32_t idPV = idesc_bf16(kBM, D, true);
-      int consumed = 0;
+      // Descriptor bases, computed once.  Every operand of the loop is a base
+      // plus a constant (start address in 16-byte units; all shared-memory
+      // offsets stay below 256 KB, so the 14-bit field never carries).
+      const uint64_t dQ = sdesc_kmajor_sw128(sQ);
+      const uint64_t dK = sdesc_kmajor_sw128(sRing);
+      const uint64_t dV = sdesc_mnmajor_sw128(sRing, L::kSlabBytes);
+      int consumed = 0;  // ring loads seen, in the loader's order K0, V0, K1, V1, …
       int v_prev_slot = 0;
       bool ok = wait_bar(bar_q, 0, wc);
       tc_fence_after();
       for (int j = 0; j <= nmax && ok; ++j) {
         int k_slot = -1;
         for (int t = 0; t < ntiles && ok; ++t) {
+          const uint32_t tSt = tmem + L::col_s(t), tOt = tmem + L::col_o(t);
           if (j >= 1 && j <= nblk(t)) {
             // O_t (+)= P_t(j−1) · V_{j−1}
             if (!wait_bar(bar_p_full(t), (j - 1) & 1, wc)) { ok = false; break; }
             tc_fence_after();
-            const uint32_t vbase = sRing + v_prev_slot * L::kTileBytes;
+            const uint64_t dv = dV + ((v_prev_slot * L::kTileBytes) >> 4);
 #pragma unroll
-            for (int kk = 0; kk < kBN / 16; ++kk) {
-              const uint64_t bdesc = sdesc_mnmajor_sw128(vbase + kk * 2048, L::kSlabBytes);
-              mma_ts(tmem + L::col_o(t), tmem + L::col_s(t) + kk * 8, bdesc, idPV, (j > 1 || kk > 0) ? 1u : 0u);
-            }
+            for (int kk = 0; kk < kBN / 16; ++kk)
+              mma_ts(tOt, tSt + kk * 8, dv + ((kk * 2048) >> 4), idPV, (j > 1 || kk > 0) ? 1u : 0u);
             if (j == nblk(t)) mma_commit(bar_o_full(t));
           }
           if (j < nblk(t)) {
@@ -246,13 +253,12 @@ __global__ void __launch_bounds__(kThreads, 1)
               tc_fence_after();
             }
             // S_t = Q_t · K_jᵀ
-            const uint32_t qbase = sQ + t * L::kTileBytes;
-            const uint32_t kbase = sRing + k_slot * L::kTileBytes;
+            const uint64_t dq = dQ + ((t * L::kTileBytes) >> 4);
+            const uint64_t dk = dK + ((k_slot * L::kTileBytes) >> 4);
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk) {
-              const uint32_t off = (kk / 4) * L::kSlabBytes + (kk % 4) * 32;
-              mma_ss(tmem + L::col_s(t), sdesc_kmajor_sw128(qbase + off), sdesc_kmajor_sw128(kbase + off), idS,
-                     kk > 0 ? 1u : 0u);
+              const uint32_t off = ((kk / 4) * L::kSlabBytes + (kk % 4) * 32) >> 4;
+              mma_ss(tSt, dq + off, dk + off, idS, kk > 0 ? 1u : 0u);
             }
             mma_commit(bar_s_full(t));
           }
@@ -293,18 +299,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool got = wait_bar(bar_s_full(t), j & 1, wc);
         if (__any_sync(0xffffffffu, !got)) { ok = false; break; }
         tc_fence_after();
-        float s[kBN];
-        {
-          uint32_t u[32];
+        // Whole S row (128 fp32) in registers: four loads, one wait.
+        uint32_t u[kBN];
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            tmem_ld32(tS + 32 * c, u);
-            tmem_wait_ld();
-            reg_fence32(u);
+        for (int c = 0; c < 4; ++c) tmem_ld32(tS + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(&u[32 * c]));
+        tmem_wait_ld();
 #pragma unroll
-            for (int i = 0; i < 32; ++i) s[32 * c + i] = __uint_as_float(u[i]);
-          }
-        }
+        for (int c = 0; c < 4; ++c) reg_fence32(*reinterpret_cast<uint32_t(*)[32]>(&u[32 * c]));
+        float* const s = reinterpret_cast<float*>(u);
         const int k0 = j * kBN;
         if (k0 + kBN > p.Sk || (CAUSAL && k0 + kBN - 1 > q_tile)) {
 #pragma unroll
@@ -313,10 +315,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (key >= p.Sk || (CAUSAL && key > q_row)) s[c] = -INFINITY;
           }
         }
-        float mx = fmax3(s[0], s[1], s[2]);
+        // Row maximum as a tree of eight independent 16-wide chains.
+        float m8[8];
 #pragma unroll
-        for (int c = 3; c + 1 < kBN; c += 2) mx = fmax3(mx, s[c], s[c + 1]);
-        mx = fmaxf(mx, s[kBN - 1]);
+        for (int g = 0; g < 8; ++g) {
+          const float* x = s + 16 * g;
+          float a = fmax3(x[0], x[1], x[2]);
+          float b2 = fmax3(x[3], x[4], x[5]);
+          a = fmax3(a, x[6], x[7]);
+          b2 = fmax3(b2, x[8], x[9]);
+          a = fmax3(a, x[10], x[11]);
+          b2 = fmax3(b2, x[12], x[13]);
+          m8[g] = fmax3(a, b2, fmaxf(x[14], x[15]));
+        }
+        float mx = fmax3(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7]));
         mx *= sc;
         const bool need = mx > m_run + p.tau;
         if (__any_sync(0xffffffffu, need)) {
@@ -342,14 +354,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         if (p.counters != nullptr && lane == 0) atomicAdd(p.counters + 1, 32ull);
+        __syncwarp();
         const float negm = (m_run == -INFINITY) ? 0.f : -m_run;
         const uint64_t sc2 = pack2(sc, sc);
         const uint64_t nm2 = pack2(negm, negm);
-        uint64_t acc0 = 0, acc1 = 0;  // two packed partial sums (+0.0f pairs)
+        uint64_t acc[4] = {0, 0, 0, 0};  // four packed partial sums (+0.0f pairs)
 #pragma unroll
         for (int ch = 0; ch < kBN / 16; ++ch) {
           uint32_t pk[8];
-          const bool use_poly = (p.poly_mask >> ch) & 1u;
+          constexpr uint32_t kPoly = POLY;
+          const bool use_poly = (kPoly >> ch) & 1u;  // folded after unrolling
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
             const int c = ch * 16 + 2 * i;
@@ -361,15 +375,14 @@ __global__ void __launch_bounds__(kThreads, 1)
               x0 = ex2_mufu(x0);
               x1 = ex2_mufu(x1);
             }
-            if (i & 1) acc1 = fadd2(acc1, pack2(x0, x1));
-            else acc0 = fadd2(acc0, pack2(x0, x1));
+            acc[i & 3] = fadd2(acc[i & 3], pack2(x0, x1));
             pk[i] = pack_bf16x2(x0, x1);
           }
           tmem_st8(tS + ch * 8, pk);
         }
         float a0, a1, b0, b1;
-        unpack2(acc0, a0, a1);
-        unpack2(acc1, b0, b1);
+        unpack2(fadd2(acc[0], acc[1]), a0, a1);
+        unpack2(fadd2(acc[2], acc[3]), b0, b1);
         l_run += (a0 + a1) + (b0 + b1);
         tmem_wait_st();
         tc_fence_before();
@@ -416,7 +429,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int s = 0; s < L::kSlabs; ++s)
               tma_store_4d(&tm_o, src + s * L::kSlabBytes, 64 * s, h, q_tile, b);
             tma_store_commit();
-            tma_store_wait0();
+            tma_store_wait_read0();  // smem may be released; the global writes complete on their own
           }
         }
       }

@@ -1,6 +1,8 @@
 // Internal interface between the C-ABI host code (attn_api.cu) and the
-// per-head-dim kernel translation units (attn_fwd_d64.cu, attn_fwd_d128.cu).
+// kernel translation units (one per head dim × mask kind).
 #pragma once
+
+#include <cstdint>
 
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -13,15 +15,53 @@ struct LaunchArgs {
   CUtensorMap q, k, v, o;  // 4-D tiled maps, box (64, 1, 128, 1), 128-byte swizzle
   FwdParams p;
   int grid;
-  int causal;
+  uint32_t poly;           // exp2 chunk mask; one of kPolyMasks
   int device;
   cudaStream_t stream;
 };
 
-cudaError_t launch_fwd_d64(const LaunchArgs& a);
-cudaError_t launch_fwd_d128(const LaunchArgs& a);
+// The exp2 splits compiled into the library (bit c = 16-column chunk c of a
+// 128-key block uses the polynomial): none, 1/8, 1/4, 1/2, all.
+constexpr uint32_t kPolyMasks[] = {0x00u, 0x01u, 0x11u, 0x55u, 0xFFu};
 
-// Dynamic shared memory each instantiation requests.
-unsigned int fwd_smem_bytes(int d);
+inline bool poly_mask_supported(uint32_t m) {
+  for (uint32_t x : kPolyMasks)
+    if (x == m) return true;
+  return false;
+}
+
+cudaError_t launch_fwd_d64(const LaunchArgs& a);
+cudaError_t launch_fwd_d64_causal(const LaunchArgs& a);
+cudaError_t launch_fwd_d128(const LaunchArgs& a);
+cudaError_t launch_fwd_d128_causal(const LaunchArgs& a);
+
+// Launch one instantiation, setting its shared-memory opt-in the first time
+// each device uses it.
+template <int D, bool CAUSAL, uint32_t POLY>
+cudaError_t launch_one(const LaunchArgs& a) {
+  constexpr unsigned int smem = Layout<D>::kSmemBytes;
+  static volatile bool configured[64] = {};
+  if (a.device < 0 || a.device >= 64) return cudaErrorInvalidDevice;
+  if (!configured[a.device]) {
+    const cudaError_t e =
+        cudaFuncSetAttribute(attn_fwd_kernel<D, CAUSAL, POLY>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    configured[a.device] = true;
+  }
+  attn_fwd_kernel<D, CAUSAL, POLY><<<a.grid, kThreads, smem, a.stream>>>(a.q, a.k, a.v, a.o, a.p);
+  return cudaGetLastError();
+}
+
+template <int D, bool CAUSAL>
+cudaError_t launch_variant(const LaunchArgs& a) {
+  switch (a.poly) {
+    case 0x00u: return launch_one<D, CAUSAL, 0x00u>(a);
+    case 0x01u: return launch_one<D, CAUSAL, 0x01u>(a);
+    case 0x11u: return launch_one<D, CAUSAL, 0x11u>(a);
+    case 0x55u: return launch_one<D, CAUSAL, 0x55u>(a);
+    case 0xFFu: return launch_one<D, CAUSAL, 0xFFu>(a);
+    default: return cudaErrorInvalidValue;
+  }
+}
 
 }  // namespace attn

@@ -99,7 +99,9 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
  * poly_exp2_mask — which 16-column chunks of each 128-key block compute exp2
  *   with the FMA-pipe cubic polynomial instead of the MUFU unit ("…", section
  *   "Exponenciais de Software via Núcleos CUDA").  Bit c (0..7) selects chunk
- *   c; 0 selects the per-head-dim default; 0x100 forces "no chunk" (all MUFU).
+ *   c.  The splits compiled in are 0x01 (1/8), 0x11 (1/4), 0x55 (1/2) and
+ *   0xFF (all); 0x100 selects none (all MUFU); 0 selects the default for the
+ *   head dim; any other value is rejected with ATTN_ERR_OPTION.
  * counters — optional device pointer to 2 zero-initialised uint64 values; when
  *   non-NULL the kernel adds the number of (row, block) rescales to
  *   counters[0] and the number of (row, block) softmax updates to counters[1].

@@ -74,8 +74,9 @@ def test_bad_options_rejected(L):
     assert rc == -9
     o = attn.make_options(rescale_threshold=40.0)
     assert L.attn_fwd_ex(A, A, A, A, A, 1, 1, 8, 8, 64, 0.125, 0, ctypes.byref(o), None) == -9
-    o = attn.make_options(poly_exp2_mask=0x200)
-    assert L.attn_fwd_ex(A, A, A, A, A, 1, 1, 8, 8, 64, 0.125, 0, ctypes.byref(o), None) == -9
+    for bad_mask in (0x200, 0x0F, 0x03, 0x101):
+        o = attn.make_options(poly_exp2_mask=bad_mask)
+        assert L.attn_fwd_ex(A, A, A, A, A, 1, 1, 8, 8, 64, 0.125, 0, ctypes.byref(o), None) == -9
     o = attn.make_options()
     o.struct_size = 4
     assert L.attn_fwd_ex(A, A, A, A, A, 1, 1, 8, 8, 64, 0.125, 0, ctypes.byref(o), None) == -9

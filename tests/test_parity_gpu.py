@@ -72,7 +72,7 @@ OPT_CASES = [inputs.custom(1, 4, 1024, 1024, 64, False, sigma_qk=3.0, seed=41),
 
 
 @pytest.mark.parametrize("w", OPT_CASES, ids=lambda w: w.name)
-@pytest.mark.parametrize("poly", [0x100, 0xFF, 0x55, 0x0F, 0])
+@pytest.mark.parametrize("poly", [0x100, 0xFF, 0x55, 0x11, 0x01, 0])
 @pytest.mark.parametrize("tau", [-1.0, 8.0, 32.0])
 def test_exp2_paths_and_rescale_threshold(w, poly, tau):
     """Parity holds with every exp2 split (all MUFU, all polynomial, mixed) and
