@@ -69,6 +69,7 @@ int encode_bshd(CUtensorMap* m, const void* ptr, int B, int S, int H, int d) {
 struct DeviceInfo {
   int checked = 0;  // 0 unknown, 1 supported, -1 unsupported
   unsigned int* status = nullptr;
+  int sms = 0;
 };
 DeviceInfo g_dev[kMaxDevices];
 
@@ -92,6 +93,8 @@ int current_device(int* dev_out) {
       e = cudaGetSymbolAddress(&addr, g_attn_status);
       if (e != cudaSuccess) return fail_cuda(e, "cudaGetSymbolAddress(status)");
       di.status = static_cast<unsigned int*>(addr);
+      if (cudaDeviceGetAttribute(&di.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || di.sms < 1)
+        return ATTN_ERR_ARCH;
       di.checked = 1;
     }
   }
@@ -106,8 +109,8 @@ int check_args(const void* q, const void* k, const void* v, const void* o, const
                int Sk, int d, float scale) {
   if (q == nullptr || k == nullptr || v == nullptr || o == nullptr || lse == nullptr) return ATTN_ERR_NULL;
   if (B < 1 || H < 1 || Sq < 1 || Sk < 1) return ATTN_ERR_SHAPE;
-  const long long n_pairs = (static_cast<long long>(Sq) + 255) / 256;
-  if (static_cast<long long>(B) * H * n_pairs > 0x7FFFFFFFLL) return ATTN_ERR_SHAPE;
+  const long long n_qt = (static_cast<long long>(Sq) + 127) / 128;
+  if (static_cast<long long>(B) * H * n_qt > 0x7FFFFFFFLL) return ATTN_ERR_SHAPE;
   if (d != 64 && d != 128) return ATTN_ERR_HEAD_DIM;
   if (!std::isfinite(scale) || !(scale > 0.f)) return ATTN_ERR_SCALE;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse)) return ATTN_ERR_ALIGN;
@@ -180,8 +183,8 @@ int attn_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse
   if ((rc = encode_bshd(&a.q, q, B, Sq, H, d)) != ATTN_OK) return rc;
   if ((rc = encode_bshd(&a.k, k, B, Sk, H, d)) != ATTN_OK) return rc;
   if ((rc = encode_bshd(&a.v, v, B, Sk, H, d)) != ATTN_OK) return rc;
-  if ((rc = encode_bshd(&a.o, o, B, Sq, H, d)) != ATTN_OK) return rc;
-  const int n_pairs = (Sq + 255) / 256;
+  const int n_qt = (Sq + 127) / 128;
+  a.p.o = o;
   a.p.lse = lse;
   a.p.status = g_dev[dev].status;
   a.p.counters = counters;
@@ -189,12 +192,13 @@ int attn_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse
   a.p.H = H;
   a.p.Sq = Sq;
   a.p.Sk = Sk;
-  a.p.n_pairs = n_pairs;
+  a.p.n_qt = n_qt;
+  a.p.n_tiles = n_qt * B * H;
   a.p.scale_log2 = scale * 1.4426950408889634f;
   a.p.tau = tau;
   a.p.timeout_ns = static_cast<uint64_t>(timeout_ms) * 1000000ull;
   a.p.test_flags = test_flags;
-  a.grid = n_pairs * B * H;
+  a.grid = a.p.n_tiles < g_dev[dev].sms ? a.p.n_tiles : g_dev[dev].sms;
   a.poly = poly;
   a.device = dev;
   a.stream = stream;

@@ -1,40 +1,67 @@
 // Exact attention forward kernel for sm_103a (GB300).
 //
-// One CTA computes two 128-row query tiles (Q0, Q1) of one (batch, head)
-// against every visible 128-key block, with an online softmax, so the score
-// matrix never leaves the chip ("FlashAttention 4: Atenção Mais Rápida …",
-// section "Novidades no FlashAttention 4": tiles of Q, K, V streamed through
-// on-chip memory, one CTA per output block set).
+// Persistent: one CTA per SM walks a list of work tiles; a tile is 128 query
+// rows of one (batch, head), computed against every visible 128-key block
+// with an online softmax, so the score matrix never leaves the chip
+// ("FlashAttention 4: Atenção Mais Rápida …", section "Novidades no
+// FlashAttention 4": blocks of Q, K, V streamed through on-chip memory).
 //
 // Warp roles (320 threads):
-//   warps 0-3  softmax group 0 — one thread per row of tile 0
-//   warps 4-7  softmax group 1 — one thread per row of tile 1
-//   warp  8    loader — TMA loads of Q0/Q1 once, then K_j, V_j into a ring of
-//              shared-memory slots guarded by full/empty mbarriers
-//   warp  9    MMA issuer (one thread) — tcgen05.mma S_t = Q_t K_jᵀ and
-//              O_t += P_t V_j for both tiles in strict alternation,
-//              accumulators in tensor memory (TMEM)
-// This is the load → MMA → softmax → rescale → store pipeline of
-// "FlashAttention 4: …", section "Novidades no FlashAttention 4" (warp
-// specialisation), with the rescale step folded into the softmax warps: a row
-// is rescaled only when its block maximum exceeds the running maximum by more
-// than τ (section "Reescalonamento Softmax Online Mais Inteligente"), which
-// after the first blocks is rare, so a separate correction warpgroup would
-// mostly idle.  The two tiles ping-pong: while one softmax group works on its
-// S tile, the tensor core runs the other tile's P·V and next Q·Kᵀ
-// ("FlashAttention-3: …", section "Interleaving de GEMM e Softmax").
+//   warps 0-7  softmax, two warpgroups: warpgroup h owns keys [64h, 64h+64)
+//              of every 128-key block, one thread per query row (= TMEM
+//              lane).  Each half is an independent online softmax with its
+//              own running maximum, row sum and O accumulator; the halves are
+//              merged once per tile in the epilogue with the log-sum-exp rule
+//              (the merge a split over keys needs).  Splitting the columns
+//              halves each thread's serial work and puts two softmax warps on
+//              every scheduler, while no value crosses warpgroups per block.
+//   warp  8    loader — TMA loads of each tile's Q into one of two Q buffers,
+//              and of K and V tiles into a ring of shared-memory slots guarded
+//              by full/empty mbarriers, in the order the MMA issuer consumes
+//              them (K_0, K_1, then V_g, K_{g+2} for every block g, across tile
+//              boundaries), so slots free up in the order they are refilled;
+//              allocates and frees tensor memory
+//   warp  9    P·V issuer (one thread) — tcgen05.mma O_h += P_h V_j[64h:64h+64]
+//   warp 10    S issuer (one thread) — tcgen05.mma S = Q K_jᵀ
+//              Accumulators live in tensor memory.  An MMA issue stalls while
+//              the tensor core's queue is full, so a single issuer leaves the
+//              tensor core idle during each of its barrier waits; with two,
+//              one issuer's waits overlap the other's MMAs.
+// This is the load → MMA → softmax → rescale → store pipeline of "FlashAttention
+// 4: …", section "Novidades no FlashAttention 4", with the rescale step folded
+// into the softmax warps: a row is rescaled only when its block maximum
+// exceeds its running maximum by more than τ (section "Reescalonamento Softmax
+// Online Mais Inteligente"), which after the first blocks is rare.
 //
-// TMEM columns (512 allocated): S0 [0,128), S1 [128,256), O0 [256, 256+D),
-// O1 [256+D, 256+2D).  P_t (bf16, two per 32-bit column) overwrites the first
-// 64 columns of S_t after the softmax thread has read its whole S row.
+// The schedule is built around the tensor core, which runs a 128×128×16 bf16
+// MMA in 64 cycles: S is double-buffered in TMEM, so the issuer computes
+// S(j+1) and S(j+2) while the softmax still works on S(j); the softmax never
+// waits for a Q·Kᵀ, and the tensor core waits only for P.  Q is
+// double-buffered in shared memory, so the next tile's Q arrives while the
+// current tile finishes, and the issuer starts the next tile's Q·Kᵀ while the
+// softmax warps write the current tile's output.
+//
+// TMEM columns (512 allocated): S buffers [0,128) and [128,256), O_0 [256,
+// 256+D), O_1 [256+D, 256+2D).  P_h (bf16, two per 32-bit column) overwrites
+// columns [64h, 64h+32) of its S buffer, inside the half that warpgroup h has
+// already read.
 //
 // Ordering rules the protocol relies on:
-//  * tcgen05.mma operations issued by one thread execute in issue order, and
-//    tcgen05.commit arrives only after all earlier ones complete.  The MMA
-//    thread issues P_t(j−1)·V before S_t(j) = Q_t K_jᵀ, so S_t(j) never
-//    overwrites P_t(j−1) early, and when s_full[t] fires for block j the O_t
-//    update of block j−1 is finished — the softmax thread may rescale O_t.
-//  * O_t is not touched by the MMA again until p_full[t] is signalled.
+//  * tcgen05.commit arrives only after all earlier MMAs of the committing
+//    thread complete; MMAs of different threads are not ordered.  So the S
+//    issuer waits for pv_done(g) — P(g)·V has completed — before S(g+2)
+//    reuses P(g)'s buffer.
+//  * O_h is written by P_h(g)·V only after p_full(g), i.e. after both
+//    warpgroups have finished block g (including any rescale of O_h), and a
+//    rescale at block g first waits for pv_done(g−1) (the previous P·V has
+//    landed).
+//  * A parity wait is only correct while the barrier is within one phase of
+//    the phase waited for.  Every wait here has that property: the next
+//    phase needs work the waiting role has not released yet, and the
+//    previous one is implied by a barrier the role already passed (when the
+//    softmax sees S(g), P(g−2)·V has completed, because S(g) was issued after
+//    waiting for it).  The epilogue waits on o_final, completed once per tile
+//    after its last P·V.
 #pragma once
 
 #include <cstdint>
@@ -46,21 +73,24 @@ namespace attn {
 
 constexpr int kBM = 128;       // query rows per tile (= TMEM lanes)
 constexpr int kBN = 128;       // keys per block
-constexpr int kThreads = 320;  // 8 softmax warps + loader + MMA issuer
+constexpr int kThreads = 352;  // 8 softmax warps + loader + 2 MMA issuers
 constexpr int kLoaderWarp = 8;
-constexpr int kMmaWarp = 9;    // MMA issuer; also allocates TMEM
+constexpr int kPvWarp = 9;
+constexpr int kSWarp = 10;
 constexpr uint32_t kTmemCols = 512;
 
 struct FwdParams {
-  float* lse;              // [B, H, Sq]
-  unsigned int* status;    // device status word
+  void* o;                       // bf16 [B, Sq, H, D]
+  float* lse;                    // [B, H, Sq]
+  unsigned int* status;          // device status word
   unsigned long long* counters;  // optional diagnostics (may be null)
   int B, H, Sq, Sk;
-  int n_pairs;             // ceil(Sq / 256)
-  float scale_log2;        // scale · log2(e)
-  float tau;               // rescale threshold, log2 domain
+  int n_qt;                      // ceil(Sq / 128)
+  int n_tiles;                   // n_qt · B · H
+  float scale_log2;              // scale · log2(e)
+  float tau;                     // rescale threshold, log2 domain
   uint64_t timeout_ns;
-  uint32_t test_flags;     // bit 0: loader withholds K/V (exercises the wait limit)
+  uint32_t test_flags;           // bit 0: loader withholds K/V (exercises the wait limit)
 };
 
 template <int D>
@@ -69,16 +99,19 @@ struct Layout {
   static constexpr int kSlabs = D / 64;                 // 128-byte-wide column slabs per row
   static constexpr uint32_t kSlabBytes = kBM * 128;     // one 128-row slab: 16 KB
   static constexpr uint32_t kTileBytes = kSlabBytes * kSlabs;
-  static constexpr int kStages = (D == 128) ? 4 : 8;    // K/V ring slots (each holds one K or V tile)
-  static constexpr uint32_t kQOff = 0;
+  static constexpr int kStages = (D == 128) ? 4 : 10;   // K/V ring slots (each holds one K or V tile)
+  static constexpr uint32_t kQOff = 0;                  // two Q buffers
   static constexpr uint32_t kRingOff = 2 * kTileBytes;
-  static constexpr uint32_t kBarOff = kRingOff + kStages * kTileBytes;
-  // barriers: q_full, kv_full[S], kv_empty[S], s_full[2], p_full[2], o_full[2], epi[2], done
-  static constexpr int kNumBars = 1 + 2 * kStages + 2 + 2 + 2 + 2 + 1;
+  // per-row (max, sum) of each half, exchanged once per tile: [tile parity][half][row] float2
+  static constexpr uint32_t kStatsOff = kRingOff + kStages * kTileBytes;
+  static constexpr uint32_t kBarOff = kStatsOff + 2 * 2 * kBM * 8;
+  // barriers: q_full[2], q_empty[2], kv_full[S], kv_empty[S], s_full[2], p_full[2], pv_done[2],
+  //           o_final, exch_full[2], exch_empty[2], done[2]
+  static constexpr int kNumBars = 2 + 2 + 2 * kStages + 2 + 2 + 2 + 1 + 2 + 2 + 2;
   static constexpr uint32_t kMiscOff = kBarOff + 8 * kNumBars;  // tmem base (4 B) + abort flag (4 B)
   static constexpr uint32_t kSmemBytes = kMiscOff + 16 + 1024;  // + slack to align the base to 1024
-  __device__ static constexpr uint32_t col_s(int t) { return 128u * t; }
-  __device__ static constexpr uint32_t col_o(int t) { return 256u + static_cast<uint32_t>(D) * t; }
+  __device__ static constexpr uint32_t col_s(int buf) { return 128u * buf; }
+  __device__ static constexpr uint32_t col_o(int half) { return 256u + static_cast<uint32_t>(D) * half; }
 };
 
 __device__ __forceinline__ void reg_fence32(uint32_t (&r)[32]) {
@@ -88,13 +121,40 @@ __device__ __forceinline__ void reg_fence32(uint32_t (&r)[32]) {
                  "+r"(r[i + 5]), "+r"(r[i + 6]), "+r"(r[i + 7]));
 }
 
+// One work tile: 128 query rows of one (batch, head).
+struct Tile {
+  int b, h, q0, nb;  // nb = key blocks visible to the tile
+};
+
+// Tile order.  Causal: heaviest query tiles first (longest-processing-time
+// order for the static round-robin below).  Otherwise: the tiles of one head
+// are consecutive, so CTAs working side by side share that head's K/V in L2.
+template <bool CAUSAL>
+__device__ __forceinline__ Tile tile_info(int idx, const FwdParams& p) {
+  const int BH = p.B * p.H;
+  int qt, bh;
+  if (CAUSAL) {
+    qt = p.n_qt - 1 - idx / BH;
+    bh = idx % BH;
+  } else {
+    qt = idx % p.n_qt;
+    bh = idx / p.n_qt;
+  }
+  Tile t;
+  t.b = bh / p.H;
+  t.h = bh % p.H;
+  t.q0 = qt * kBM;
+  const int nk = (p.Sk + kBN - 1) / kBN;
+  t.nb = CAUSAL ? min(nk, (min(t.q0 + kBM, p.Sq) - 1) / kBN + 1) : nk;
+  return t;
+}
+
 // POLY: bit c selects the FMA-pipe polynomial exp2 for 16-column chunk c of
 // every 128-key block (compile time, so the exp loop is one basic block).
 template <int D, bool CAUSAL, uint32_t POLY>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
-                    const FwdParams p) {
+                    const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
   using L = Layout<D>;
   extern __shared__ uint8_t smem_raw[];
   // 128-byte swizzled tiles need a 1024-byte aligned base.
@@ -105,68 +165,55 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t sQ = base + L::kQOff;
   const uint32_t sRing = base + L::kRingOff;
   const uint32_t bars = base + L::kBarOff;
-  const uint32_t bar_q = bars;
-  auto bar_kv_full = [&](int s) { return bars + 8u * (1 + s); };
-  auto bar_kv_empty = [&](int s) { return bars + 8u * (1 + L::kStages + s); };
-  auto bar_s_full = [&](int t) { return bars + 8u * (1 + 2 * L::kStages + t); };
-  auto bar_p_full = [&](int t) { return bars + 8u * (3 + 2 * L::kStages + t); };
-  auto bar_o_full = [&](int t) { return bars + 8u * (5 + 2 * L::kStages + t); };
-  auto bar_epi = [&](int t) { return bars + 8u * (7 + 2 * L::kStages + t); };
-  const uint32_t bar_done = bars + 8u * (9 + 2 * L::kStages);
+  auto bar_q_full = [&](int i) { return bars + 8u * i; };
+  auto bar_q_empty = [&](int i) { return bars + 8u * (2 + i); };
+  auto bar_kv_full = [&](int s) { return bars + 8u * (4 + s); };
+  auto bar_kv_empty = [&](int s) { return bars + 8u * (4 + L::kStages + s); };
+  auto bar_s_full = [&](int i) { return bars + 8u * (4 + 2 * L::kStages + i); };
+  auto bar_p_full = [&](int i) { return bars + 8u * (6 + 2 * L::kStages + i); };
+  auto bar_pv_done = [&](int i) { return bars + 8u * (8 + 2 * L::kStages + i); };
+  const uint32_t bar_o_final = bars + 8u * (10 + 2 * L::kStages);
+  auto bar_exch_full = [&](int i) { return bars + 8u * (11 + 2 * L::kStages + i); };
+  auto bar_exch_empty = [&](int i) { return bars + 8u * (13 + 2 * L::kStages + i); };
+  auto bar_done = [&](int i) { return bars + 8u * (15 + 2 * L::kStages + i); };
+  float2* const stats = reinterpret_cast<float2*>(smem + L::kStatsOff);
   uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMiscOff);
   volatile uint32_t* const abort_flag = reinterpret_cast<volatile uint32_t*>(smem + L::kMiscOff + 4);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-
-  // ---- work item: (pair of query tiles, batch, head)
-  const int BH = p.B * p.H;
-  int pair, bh;
-  if (CAUSAL) {  // heaviest query tiles first (longest-processing-time order)
-    pair = p.n_pairs - 1 - static_cast<int>(blockIdx.x) / BH;
-    bh = static_cast<int>(blockIdx.x) % BH;
-  } else {  // the pairs of one head run side by side and share its K/V in L2
-    pair = static_cast<int>(blockIdx.x) % p.n_pairs;
-    bh = static_cast<int>(blockIdx.x) / p.n_pairs;
-  }
-  const int b = bh / p.H, h = bh % p.H;
-  const int q0 = pair * 2 * kBM;
-  const int ntiles = (p.Sq - q0 > kBM) ? 2 : 1;
-  const int nk = (p.Sk + kBN - 1) / kBN;
-  // Key blocks each tile visits (causal: up to the block holding its last row).
-  const int nblk0 = CAUSAL ? min(nk, (min(q0 + kBM, p.Sq) - 1) / kBN + 1) : nk;
-  const int nblk1 = CAUSAL ? min(nk, (min(q0 + 2 * kBM, p.Sq) - 1) / kBN + 1) : nk;
-  auto nblk = [&](int t) { return t ? nblk1 : nblk0; };
-  const int nmax = ntiles == 2 ? nblk1 : nblk0;
+  const int stride = static_cast<int>(gridDim.x);
 
   // ---- set-up
-  if (warp == kMmaWarp) {
+  if (warp == kLoaderWarp) {
     tmem_alloc(smem_u32(tmem_slot), kTmemCols);
     tmem_relinquish();
     tc_fence_before();
   }
   if (threadIdx.x == 0) {
     *abort_flag = 0u;
-    mbar_init(bar_q, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(bar_q_full(i), 1);
+      mbar_init(bar_q_empty(i), 1);
+      mbar_init(bar_s_full(i), 1);
+      mbar_init(bar_p_full(i), 2 * kBM);  // both warpgroups
+      mbar_init(bar_pv_done(i), 1);
+      mbar_init(bar_done(i), 1);
+      mbar_init(bar_exch_full(i), 2 * kBM);
+      mbar_init(bar_exch_empty(i), 2 * kBM);
+    }
     for (int s = 0; s < L::kStages; ++s) {
       mbar_init(bar_kv_full(s), 1);
       mbar_init(bar_kv_empty(s), 1);
     }
-    for (int t = 0; t < 2; ++t) {
-      mbar_init(bar_s_full(t), 1);
-      mbar_init(bar_p_full(t), kBM);
-      mbar_init(bar_o_full(t), 1);
-      mbar_init(bar_epi(t), kBM);
-    }
-    mbar_init(bar_done, 1);
+    mbar_init(bar_o_final, 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     fence_proxy_async_smem();
   }
-  if (warp == kLoaderWarp && lane == 0) {
+  if (warp == kSWarp && lane == 0) {
     tma_prefetch_desc(&tm_q);
     tma_prefetch_desc(&tm_k);
     tma_prefetch_desc(&tm_v);
-    tma_prefetch_desc(&tm_o);
   }
   __syncthreads();
   tc_fence_after();
@@ -176,174 +223,218 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == kLoaderWarp) {
     // =========================================================== loader
     if (lane == 0) {
-      int issued = 0;  // loads issued into the ring
+      int issued = 0;  // ring loads issued
+      int q_issued = 0;
       bool ok = true;
-      mbar_arrive_expect_tx(bar_q, ntiles * L::kTileBytes);
-      for (int t = 0; t < ntiles; ++t)
+      // Two cursors over this CTA's (tile, block) sequence, as in the issuer:
+      // K runs two blocks ahead of V.  A tile's Q is loaded just before its K_0.
+      int k_idx = blockIdx.x, k_tc = 0, k_j = 0, gK = 0;
+      Tile k_T = tile_info<CAUSAL>(k_idx, p);
+      int v_idx = blockIdx.x, v_j = 0, gV = 0;
+      Tile v_T = k_T;
+      auto ring_load = [&](const CUtensorMap* m, const Tile& T, int j) -> bool {
+        const int slot = issued % L::kStages;
+        if (!wait_bar(bar_kv_empty(slot), ((issued / L::kStages) & 1) ^ 1u, wc)) return false;
+        mbar_arrive_expect_tx(bar_kv_full(slot), L::kTileBytes);
         for (int s = 0; s < L::kSlabs; ++s)
-          tma_load_4d(sQ + t * L::kTileBytes + s * L::kSlabBytes, &tm_q, 64 * s, h, q0 + t * kBM, b, bar_q);
-      if (p.test_flags & 1u) {
-        // Test mode: no K/V copy is issued, so the MMA issuer's first wait
-        // expires.  Only the Q copy is in flight; let it land and stop.
-        const uint64_t t0 = globaltimer_ns();
-        while (!mbar_try_wait(bar_q, 0))
-          if (globaltimer_ns() - t0 > p.timeout_ns) break;
-      }
-      for (int j = 0; j < nmax && ok && !(p.test_flags & 1u); ++j) {
-        for (int kv = 0; kv < 2; ++kv) {
-          const int slot = issued % L::kStages;
-          const uint32_t ph = (issued / L::kStages) & 1u;
-          if (!wait_bar(bar_kv_empty(slot), ph ^ 1u, wc)) {
-            ok = false;
-            break;
-          }
-          mbar_arrive_expect_tx(bar_kv_full(slot), L::kTileBytes);
-          const CUtensorMap* m = kv ? &tm_v : &tm_k;
+          tma_load_4d(sRing + slot * L::kTileBytes + s * L::kSlabBytes, m, 64 * s, T.h, j * kBN, T.b,
+                      bar_kv_full(slot));
+        ++issued;
+        return true;
+      };
+      auto load_k = [&]() -> bool {
+        if (k_j == 0) {
+          const int qb = k_tc & 1;
+          if (!wait_bar(bar_q_empty(qb), ((k_tc >> 1) & 1) ^ 1u, wc)) return false;
+          mbar_arrive_expect_tx(bar_q_full(qb), L::kTileBytes);
           for (int s = 0; s < L::kSlabs; ++s)
-            tma_load_4d(sRing + slot * L::kTileBytes + s * L::kSlabBytes, m, 64 * s, h, j * kBN, b,
-                        bar_kv_full(slot));
-          ++issued;
+            tma_load_4d(sQ + qb * L::kTileBytes + s * L::kSlabBytes, &tm_q, 64 * s, k_T.h, k_T.q0, k_T.b,
+                        bar_q_full(qb));
+          ++q_issued;
+          if (p.test_flags & 1u) return false;  // test mode: no K/V copy, the MMA wait must expire
         }
+        if (!ring_load(&tm_k, k_T, k_j)) return false;
+        ++gK;
+        if (++k_j == k_T.nb) {
+          k_j = 0;
+          ++k_tc;
+          k_idx += stride;
+          if (k_idx < p.n_tiles) k_T = tile_info<CAUSAL>(k_idx, p);
+        }
+        return true;
+      };
+      while (ok && k_idx < p.n_tiles && gK < gV + 2) ok = load_k();
+      while (ok && v_idx < p.n_tiles) {
+        if (!ring_load(&tm_v, v_T, v_j)) { ok = false; break; }
+        ++gV;
+        if (++v_j == v_T.nb) {
+          v_j = 0;
+          v_idx += stride;
+          if (v_idx < p.n_tiles) v_T = tile_info<CAUSAL>(v_idx, p);
+        }
+        while (ok && k_idx < p.n_tiles && gK < gV + 2) ok = load_k();
       }
-      if (!ok) {
-        // Let the copies already in flight land before the CTA exits.
-        const uint64_t t0 = globaltimer_ns();
-        for (int n = (issued > L::kStages ? issued - L::kStages : 0); n < issued; ++n) {
-          while (!mbar_try_wait(bar_kv_full(n % L::kStages), (n / L::kStages) & 1u))
-            if (globaltimer_ns() - t0 > p.timeout_ns) break;
-        }
-        while (!mbar_try_wait(bar_q, 0))
+      // Let every copy still in flight land before the CTA can exit (the
+      // newest load of each slot and of each Q buffer; older ones completed
+      // before their slot was refilled).
+      const uint64_t t0 = globaltimer_ns();
+      for (int n = (issued > L::kStages ? issued - L::kStages : 0); n < issued; ++n)
+        while (!mbar_try_wait(bar_kv_full(n % L::kStages), (n / L::kStages) & 1u))
           if (globaltimer_ns() - t0 > p.timeout_ns) break;
-      }
+      for (int n = (q_issued > 2 ? q_issued - 2 : 0); n < q_issued; ++n)
+        while (!mbar_try_wait(bar_q_full(n & 1), (n >> 1) & 1u))
+          if (globaltimer_ns() - t0 > p.timeout_ns) break;
     }
-  } else if (warp == kMmaWarp) {
-    // ======================================================= MMA issuer
+  } else if (warp == kSWarp || warp == kPvWarp) {
+    // ====================================================== MMA issuers
+    // Ring positions follow the loader's order K_0, K_1, V_0, K_2, V_1, …,
+    // K_{G−1}, V_{G−2}, V_{G−1} over the CTA's G blocks: K_0 → 0, K_g → 2g−1,
+    // V_g → 2g+2, except the last V_{G−1} → 2G−1.
     if (lane == 0) {
-      constexpr uint32_t idS = idesc_bf16(kBM, kBN, false);
-      constexpr uint32_t idPV = idesc_bf16(kBM, D, true);
-      // Descriptor bases, computed once.  Every operand of the loop is a base
-      // plus a constant (start address in 16-byte units; all shared-memory
-      // offsets stay below 256 KB, so the 14-bit field never carries).
-      const uint64_t dQ = sdesc_kmajor_sw128(sQ);
-      const uint64_t dK = sdesc_kmajor_sw128(sRing);
-      const uint64_t dV = sdesc_mnmajor_sw128(sRing, L::kSlabBytes);
-      int consumed = 0;  // ring loads seen, in the loader's order K0, V0, K1, V1, …
-      int v_prev_slot = 0;
-      bool ok = wait_bar(bar_q, 0, wc);
-      tc_fence_after();
-      for (int j = 0; j <= nmax && ok; ++j) {
-        int k_slot = -1;
-        for (int t = 0; t < ntiles && ok; ++t) {
-          const uint32_t tSt = tmem + L::col_s(t), tOt = tmem + L::col_o(t);
-          if (j >= 1 && j <= nblk(t)) {
-            // O_t (+)= P_t(j−1) · V_{j−1}
-            if (!wait_bar(bar_p_full(t), (j - 1) & 1, wc)) { ok = false; break; }
+      bool ok = true;
+      if (warp == kSWarp) {
+        // ------------------------------------------------------ S issuer
+        constexpr uint32_t idS = idesc_bf16(kBM, kBN, false);
+        // Descriptor bases, computed once; each operand is a base plus a
+        // constant (start address in 16-byte units; shared-memory offsets
+        // stay below 256 KB, so the 14-bit field never carries).
+        const uint64_t dQ = sdesc_kmajor_sw128(sQ);
+        const uint64_t dK = sdesc_kmajor_sw128(sRing);
+        int g = 0, tc = 0;
+        for (int idx = blockIdx.x; idx < p.n_tiles && ok; idx += stride, ++tc) {
+          const Tile T = tile_info<CAUSAL>(idx, p);
+          const int qb = tc & 1;
+          for (int j = 0; j < T.nb; ++j, ++g) {
+            const int buf = g & 1;
+            // S(g) reuses the buffer of P(g−2): that P·V must have completed.
+            if (g >= 2 && !wait_bar(bar_pv_done(buf), ((g - 2) >> 1) & 1, wc)) { ok = false; break; }
+            if (j == 0 && !wait_bar(bar_q_full(qb), (tc >> 1) & 1, wc)) { ok = false; break; }
+            const int n = (g == 0) ? 0 : 2 * g - 1, slot = n % L::kStages;
+            if (!wait_bar(bar_kv_full(slot), (n / L::kStages) & 1, wc)) { ok = false; break; }
             tc_fence_after();
-            const uint64_t dv = dV + ((v_prev_slot * L::kTileBytes) >> 4);
-#pragma unroll
-            for (int kk = 0; kk < kBN / 16; ++kk)
-              mma_ts(tOt, tSt + kk * 8, dv + ((kk * 2048) >> 4), idPV, (j > 1 || kk > 0) ? 1u : 0u);
-            if (j == nblk(t)) mma_commit(bar_o_full(t));
-          }
-          if (j < nblk(t)) {
-            if (k_slot < 0) {
-              k_slot = consumed % L::kStages;
-              if (!wait_bar(bar_kv_full(k_slot), (consumed / L::kStages) & 1, wc)) { ok = false; break; }
-              ++consumed;
-              tc_fence_after();
-            }
-            // S_t = Q_t · K_jᵀ
-            const uint64_t dq = dQ + ((t * L::kTileBytes) >> 4);
-            const uint64_t dk = dK + ((k_slot * L::kTileBytes) >> 4);
+            const uint64_t dq = dQ + ((qb * L::kTileBytes) >> 4);
+            const uint64_t dk = dK + ((slot * L::kTileBytes) >> 4);
+            const uint32_t tS = tmem + L::col_s(buf);
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk) {
               const uint32_t off = ((kk / 4) * L::kSlabBytes + (kk % 4) * 32) >> 4;
-              mma_ss(tSt, dq + off, dk + off, idS, kk > 0 ? 1u : 0u);
+              mma_ss(tS, dq + off, dk + off, idS, kk > 0 ? 1u : 0u);
             }
-            mma_commit(bar_s_full(t));
+            mma_commit(bar_s_full(buf));
+            mma_commit(bar_kv_empty(slot));                     // K_j no longer read
+            if (j == T.nb - 1) mma_commit(bar_q_empty(qb));     // this tile's Q no longer read
           }
         }
-        if (!ok) break;
-        if (j >= 1) mma_commit(bar_kv_empty(v_prev_slot));  // V_{j−1} no longer read
-        if (j < nmax) {
-          mma_commit(bar_kv_empty(k_slot));  // K_j no longer read
-          const int vs = consumed % L::kStages;
-          if (!wait_bar(bar_kv_full(vs), (consumed / L::kStages) & 1, wc)) { ok = false; break; }
-          ++consumed;
-          tc_fence_after();
-          v_prev_slot = vs;
+      } else {
+        // ---------------------------------------------------- P·V issuer
+        constexpr uint32_t idPV = idesc_bf16(kBM, D, true);
+        const uint64_t dV = sdesc_mnmajor_sw128(sRing, L::kSlabBytes);
+        int G = 0;  // blocks of this CTA
+        for (int idx = blockIdx.x; idx < p.n_tiles; idx += stride) G += tile_info<CAUSAL>(idx, p).nb;
+        int g = 0;
+        for (int idx = blockIdx.x; idx < p.n_tiles && ok; idx += stride) {
+          const Tile T = tile_info<CAUSAL>(idx, p);
+          for (int j = 0; j < T.nb; ++j, ++g) {
+            const int buf = g & 1;
+            if (!wait_bar(bar_p_full(buf), (g >> 1) & 1, wc)) { ok = false; break; }
+            const int n = (g == G - 1) ? 2 * G - 1 : 2 * g + 2, slot = n % L::kStages;
+            if (!wait_bar(bar_kv_full(slot), (n / L::kStages) & 1, wc)) { ok = false; break; }
+            tc_fence_after();
+            // O_h (+)= P_h(g) · V_j[64h : 64h+64]
+            const uint64_t dv = dV + ((slot * L::kTileBytes) >> 4);
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              const uint32_t tP = tmem + L::col_s(buf) + 64 * h;
+              const uint32_t tOh = tmem + L::col_o(h);
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk)
+                mma_ts(tOh, tP + kk * 8, dv + (((4 * h + kk) * 2048) >> 4), idPV, (j > 0 || kk > 0) ? 1u : 0u);
+            }
+            mma_commit(bar_pv_done(buf));
+            if (j == T.nb - 1) mma_commit(bar_o_final);  // the tile's O_0, O_1 are complete
+            mma_commit(bar_kv_empty(slot));                // V_j no longer read
+          }
         }
       }
-      // Every MMA issued above must finish before TMEM is released.
-      mma_commit(bar_done);
+      // Every MMA this thread issued must finish before TMEM is released.
+      const int me = warp - kPvWarp;
+      mma_commit(bar_done(me));
       const uint64_t t0 = globaltimer_ns();
-      while (!mbar_try_wait(bar_done, 0))
+      while (!mbar_try_wait(bar_done(me), 0))
         if (globaltimer_ns() - t0 > p.timeout_ns) break;
     }
   } else {
     // ========================================================== softmax
-    const int t = warp >> 2;              // tile handled by this warpgroup
-    const int r = threadIdx.x & 127;      // row within the tile = TMEM lane
-    if (t < ntiles) {
-      const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
-      const uint32_t tS = tmem + L::col_s(t) + lane_off;
-      const uint32_t tO = tmem + L::col_o(t) + lane_off;
-      const int q_tile = q0 + t * kBM;
-      const int q_row = q_tile + r;
-      const float sc = p.scale_log2;
-      float m_run = -INFINITY;  // running reference maximum (log2 domain)
-      float l_run = 0.f;        // running row sum (fp32, unrounded p)
-      bool ok = true;
-      const int nb = nblk(t);
-      for (int j = 0; j < nb; ++j) {
-        const bool got = wait_bar(bar_s_full(t), j & 1, wc);
+    const int h = warp >> 2;         // key half owned by this warpgroup
+    const int r = threadIdx.x & 127;  // row within the tile = TMEM lane
+    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t tOh = tmem + L::col_o(h) + lane_off;
+    const float sc = p.scale_log2;
+    const uint64_t sc2 = pack2(sc, sc);
+    constexpr int kHalf = kBN / 2;  // keys per half
+    bool ok = true;
+    int g = 0;   // global block counter of this CTA
+    int tc = 0;  // tiles finished by this CTA
+    for (int idx = blockIdx.x; idx < p.n_tiles && ok; idx += stride, ++tc) {
+      const Tile T = tile_info<CAUSAL>(idx, p);
+      const int q_row = T.q0 + r;
+      float m_run = -INFINITY;  // running reference maximum of this half (log2 domain)
+      float l_run = 0.f;        // running row sum of this half (fp32, unrounded p)
+      for (int j = 0; j < T.nb; ++j, ++g) {
+        const int buf = g & 1;
+        const uint32_t tS = tmem + L::col_s(buf) + kHalf * h + lane_off;
+        const bool got = wait_bar(bar_s_full(buf), (g >> 1) & 1, wc);
         if (__any_sync(0xffffffffu, !got)) { ok = false; break; }
         tc_fence_after();
-        // Whole S row (128 fp32) in registers: four loads, one wait.
-        uint32_t u[kBN];
-#pragma unroll
-        for (int c = 0; c < 4; ++c) tmem_ld32(tS + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(&u[32 * c]));
+        // This half of the S row (64 fp32) in registers: two loads, one wait.
+        uint32_t u[kHalf];
+        tmem_ld32(tS, *reinterpret_cast<uint32_t(*)[32]>(&u[0]));
+        tmem_ld32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&u[32]));
         tmem_wait_ld();
-#pragma unroll
-        for (int c = 0; c < 4; ++c) reg_fence32(*reinterpret_cast<uint32_t(*)[32]>(&u[32 * c]));
+        reg_fence32(*reinterpret_cast<uint32_t(*)[32]>(&u[0]));
+        reg_fence32(*reinterpret_cast<uint32_t(*)[32]>(&u[32]));
         float* const s = reinterpret_cast<float*>(u);
-        const int k0 = j * kBN;
-        if (k0 + kBN > p.Sk || (CAUSAL && k0 + kBN - 1 > q_tile)) {
+        const int k0 = j * kBN + kHalf * h;
+        if (k0 + kHalf > p.Sk || (CAUSAL && k0 + kHalf - 1 > T.q0)) {
 #pragma unroll
-          for (int c = 0; c < kBN; ++c) {
+          for (int c = 0; c < kHalf; ++c) {
             const int key = k0 + c;
             if (key >= p.Sk || (CAUSAL && key > q_row)) s[c] = -INFINITY;
           }
         }
-        // Row maximum as a tree of eight independent 16-wide chains.
-        float m8[8];
+        // Row maximum of this half: four independent 16-wide chains.
+        float m4[4];
 #pragma unroll
-        for (int g = 0; g < 8; ++g) {
-          const float* x = s + 16 * g;
+        for (int gg = 0; gg < 4; ++gg) {
+          const float* x = s + 16 * gg;
           float a = fmax3(x[0], x[1], x[2]);
           float b2 = fmax3(x[3], x[4], x[5]);
           a = fmax3(a, x[6], x[7]);
           b2 = fmax3(b2, x[8], x[9]);
           a = fmax3(a, x[10], x[11]);
           b2 = fmax3(b2, x[12], x[13]);
-          m8[g] = fmax3(a, b2, fmaxf(x[14], x[15]));
+          m4[gg] = fmax3(a, b2, fmaxf(x[14], x[15]));
         }
-        float mx = fmax3(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7]));
+        float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
         mx *= sc;
         const bool need = mx > m_run + p.tau;
         if (__any_sync(0xffffffffu, need)) {
           const float m_new = need ? mx : m_run;
           const float alpha = need ? ex2_mufu(m_run - m_new) : 1.f;
-          if (j > 0) {  // O_t holds blocks < j: scale it (block j−1's P·V has completed)
+          if (j > 0) {
+            // O_h holds the tile's blocks < j; wait for the last P_h·V to land.
+            const bool landed = wait_bar(bar_pv_done((g - 1) & 1), ((g - 1) >> 1) & 1, wc);
+            if (__any_sync(0xffffffffu, !landed)) { ok = false; break; }
+            tc_fence_after();
 #pragma unroll 1
             for (int c = 0; c < D / 32; ++c) {
               uint32_t o[32];
-              tmem_ld32(tO + 32 * c, o);
+              tmem_ld32(tOh + 32 * c, o);
               tmem_wait_ld();
               reg_fence32(o);
 #pragma unroll
               for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-              tmem_st32(tO + 32 * c, o);
+              tmem_st32(tOh + 32 * c, o);
             }
           }
           l_run *= alpha;
@@ -353,17 +444,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (lane == 0) atomicAdd(p.counters, static_cast<unsigned long long>(nres));
           }
         }
-        if (p.counters != nullptr && lane == 0) atomicAdd(p.counters + 1, 32ull);
+        if (p.counters != nullptr && lane == 0 && h == 0) atomicAdd(p.counters + 1, 32ull);
         __syncwarp();
         const float negm = (m_run == -INFINITY) ? 0.f : -m_run;
-        const uint64_t sc2 = pack2(sc, sc);
         const uint64_t nm2 = pack2(negm, negm);
         uint64_t acc[4] = {0, 0, 0, 0};  // four packed partial sums (+0.0f pairs)
+        uint32_t pk[kHalf / 2];
 #pragma unroll
-        for (int ch = 0; ch < kBN / 16; ++ch) {
-          uint32_t pk[8];
+        for (int ch = 0; ch < kHalf / 16; ++ch) {
           constexpr uint32_t kPoly = POLY;
-          const bool use_poly = (kPoly >> ch) & 1u;  // folded after unrolling
+          const bool use_poly = (kPoly >> (4 * h + ch)) & 1u;  // folded after unrolling
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
             const int c = ch * 16 + 2 * i;
@@ -376,62 +466,80 @@ __global__ void __launch_bounds__(kThreads, 1)
               x1 = ex2_mufu(x1);
             }
             acc[i & 3] = fadd2(acc[i & 3], pack2(x0, x1));
-            pk[i] = pack_bf16x2(x0, x1);
+            pk[ch * 8 + i] = pack_bf16x2(x0, x1);
           }
-          tmem_st8(tS + ch * 8, pk);
         }
+        tmem_st32(tS, pk);  // P_h over the first 32 columns of this half
         float a0, a1, b0, b1;
         unpack2(fadd2(acc[0], acc[1]), a0, a1);
         unpack2(fadd2(acc[2], acc[3]), b0, b1);
         l_run += (a0 + a1) + (b0 + b1);
         tmem_wait_st();
         tc_fence_before();
-        mbar_arrive(bar_p_full(t));
+        mbar_arrive(bar_p_full(buf));
       }
-      // ------------------------------------------------------ epilogue
-      if (ok) {
-        const bool got = wait_bar(bar_o_full(t), 0, wc);
-        ok = !__any_sync(0xffffffffu, !got);
+      if (!ok) break;
+      // ---------------------------------------------------- epilogue
+      // Exchange (max, sum) with the other half's thread of the same row.
+      const int par = tc & 1;
+      {
+        const bool free_ = wait_bar(bar_exch_empty(par), ((tc >> 1) & 1) ^ 1u, wc);
+        if (__any_sync(0xffffffffu, !free_)) { ok = false; break; }
       }
-      if (ok) {
-        tc_fence_after();
-        const float inv_l = (l_run > 0.f) ? 1.f / l_run : 0.f;
-        // Stage O_t in its (now idle) Q_t buffer with the 128-byte swizzle
-        // the TMA store expects: 16-byte chunk c of row r sits at c ^ (r % 8).
-        uint8_t* const stage = smem + L::kQOff + t * L::kTileBytes;
+      stats[(par * 2 + h) * kBM + r] = make_float2(m_run, l_run);
+      mbar_arrive(bar_exch_full(par));
+      {
+        const bool in = wait_bar(bar_exch_full(par), (tc >> 1) & 1, wc);
+        if (__any_sync(0xffffffffu, !in)) { ok = false; break; }
+      }
+      const float2 other = stats[(par * 2 + (h ^ 1)) * kBM + r];
+      mbar_arrive(bar_exch_empty(par));
+      // Merge the halves: m = max, a_i = 2^(m_i − m), L = Σ a_i l_i.
+      const float m0 = h ? other.x : m_run, l0 = h ? other.y : l_run;
+      const float m1 = h ? m_run : other.x, l1 = h ? l_run : other.y;
+      const float m = fmaxf(m0, m1);
+      const float a0 = (m0 == -INFINITY) ? 0.f : ex2_mufu(m0 - m);
+      const float a1 = (m1 == -INFINITY) ? 0.f : ex2_mufu(m1 - m);
+      const float Lsum = a0 * l0 + a1 * l1;
+      const float inv = (Lsum > 0.f) ? 1.f / Lsum : 0.f;
+      const float w0 = a0 * inv, w1 = a1 * inv;
+      // The tile's last P·V completes phase tc of o_final.
+      const bool landed = wait_bar(bar_o_final, tc & 1, wc);
+      if (__any_sync(0xffffffffu, !landed)) { ok = false; break; }
+      tc_fence_after();
+      // Warpgroup h writes output columns [h·D/2, (h+1)·D/2).
+      const uint32_t t0 = tmem + L::col_o(0) + lane_off + h * (D / 2);
+      const uint32_t t1 = tmem + L::col_o(1) + lane_off + h * (D / 2);
+      uint4* const orow = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.o) +
+                                                   ((static_cast<size_t>(T.b) * p.Sq + q_row) * p.H + T.h) * D +
+                                                   h * (D / 2));
 #pragma unroll 1
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t o[32];
-          tmem_ld32(tO + 32 * c, o);
-          tmem_wait_ld();
-          reg_fence32(o);
-          const int slab = c / 2;
+      for (int c = 0; c < D / 64; ++c) {
+        uint32_t x0[32], x1[32];
+        tmem_ld32(t0 + 32 * c, x0);
+        tmem_ld32(t1 + 32 * c, x1);
+        tmem_wait_ld();
+        reg_fence32(x0);
+        reg_fence32(x1);
+        if (q_row < p.Sq) {
 #pragma unroll
           for (int q16 = 0; q16 < 4; ++q16) {  // four 16-byte chunks of 8 values
-            uint4 w;
-            w.x = pack_bf16x2(__uint_as_float(o[8 * q16 + 0]) * inv_l, __uint_as_float(o[8 * q16 + 1]) * inv_l);
-            w.y = pack_bf16x2(__uint_as_float(o[8 * q16 + 2]) * inv_l, __uint_as_float(o[8 * q16 + 3]) * inv_l);
-            w.z = pack_bf16x2(__uint_as_float(o[8 * q16 + 4]) * inv_l, __uint_as_float(o[8 * q16 + 5]) * inv_l);
-            w.w = pack_bf16x2(__uint_as_float(o[8 * q16 + 6]) * inv_l, __uint_as_float(o[8 * q16 + 7]) * inv_l);
-            const int chunk = (c % 2) * 4 + q16;
-            *reinterpret_cast<uint4*>(stage + slab * L::kSlabBytes + r * 128 + ((chunk ^ (r & 7)) * 16)) = w;
+            float v[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+              v[e] = w0 * __uint_as_float(x0[8 * q16 + e]) + w1 * __uint_as_float(x1[8 * q16 + e]);
+            uint4 wv;
+            wv.x = pack_bf16x2(v[0], v[1]);
+            wv.y = pack_bf16x2(v[2], v[3]);
+            wv.z = pack_bf16x2(v[4], v[5]);
+            wv.w = pack_bf16x2(v[6], v[7]);
+            orow[4 * c + q16] = wv;
           }
         }
-        fence_proxy_async_smem();
-        mbar_arrive(bar_epi(t));
-        if (q_row < p.Sq) {
-          const float lse = (l_run > 0.f) ? (m_run + __log2f(l_run)) * 0.69314718055994531f : -INFINITY;
-          p.lse[(static_cast<size_t>(b) * p.H + h) * p.Sq + q_row] = lse;
-        }
-        if (r == 0) {
-          if (wait_bar(bar_epi(t), 0, wc)) {
-            const uint32_t src = smem_u32(stage);
-            for (int s = 0; s < L::kSlabs; ++s)
-              tma_store_4d(&tm_o, src + s * L::kSlabBytes, 64 * s, h, q_tile, b);
-            tma_store_commit();
-            tma_store_wait_read0();  // smem may be released; the global writes complete on their own
-          }
-        }
+      }
+      if (h == 0 && q_row < p.Sq) {
+        const float lse = (Lsum > 0.f) ? (m + __log2f(Lsum)) * 0.69314718055994531f : -INFINITY;
+        p.lse[(static_cast<size_t>(T.b) * p.H + T.h) * p.Sq + q_row] = lse;
       }
     }
   }
@@ -439,7 +547,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // ---- tear-down: every role arrives here; all TMEM reads/writes are done
   tc_fence_before();
   __syncthreads();
-  if (warp == kMmaWarp) {
+  if (warp == kLoaderWarp) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
