@@ -212,6 +212,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of oracle time for cpu_baseline")
     ap.add_argument("--poly-mask", type=lambda x: int(x, 0), default=0, help="override the exp2 split (tuning)")
+    ap.add_argument("--tau", type=float, default=0.0, help="override the rescale threshold (tuning; 0 = default)")
+    ap.add_argument("--diag", action="store_true", help="report the rescale rate of one extra launch")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -250,7 +252,8 @@ def main():
     od = torch.empty_like(qd)
     ld = torch.empty((w.B, w.H, w.Sq), dtype=torch.float32, device=dev)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
-    opts = attn.make_options(poly_exp2_mask=args.poly_mask) if args.poly_mask else None
+    opts = (attn.make_options(poly_exp2_mask=args.poly_mask, rescale_threshold=args.tau)
+            if (args.poly_mask or args.tau) else None)
     stream = torch.cuda.current_stream()
 
     def step():
@@ -305,6 +308,16 @@ def main():
                "h2d_bytes_per_step": int(3 * q.numel() * 2 * world),
                "d2h_bytes_per_step": int((q.numel() * 2 + w.B * w.H * w.Sq * 4) * world)}
 
+    diag = None
+    if args.diag:
+        cnt = torch.zeros(2, dtype=torch.int64, device=dev)
+        attn.attn_fwd(qd, kd, vd, causal=w.causal, scale=w.scale, out=od, lse=ld,
+                      options=attn.make_options(poly_exp2_mask=args.poly_mask, rescale_threshold=args.tau,
+                                                counters=cnt))
+        torch.cuda.synchronize()
+        c = cnt.cpu().tolist()
+        diag = {"rescales_per_row_half_block": c[0] / max(1, 2 * c[1]), "row_block_updates": c[1]}
+
     if rank != 0:
         if world > 1:
             dist.destroy_process_group()
@@ -343,6 +356,8 @@ def main():
         "gpu_launches": args.steps,
         "clocks": clk.summary(),
     }
+    if diag is not None:
+        line["diag"] = diag
     print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()

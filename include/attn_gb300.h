@@ -94,8 +94,8 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
  *   Inteligente"): a row's running maximum (log2 domain) is only replaced when
  *   a new block's maximum exceeds it by more than τ; otherwise probabilities
  *   up to 2^τ are accumulated against the stale maximum.  The result does not
- *   depend on τ beyond rounding.  Range [0, 32]; a negative value selects
- *   τ = 0 (rescale on every increase); 0 selects the default 8.
+ *   depend on τ beyond rounding.  Range [0, 64]; a negative value selects
+ *   τ = 0 (rescale on every increase); 0 selects the default 32.
  * poly_exp2_mask — which 16-column chunks of each 128-key block compute exp2
  *   with the FMA-pipe cubic polynomial instead of the MUFU unit ("…", section
  *   "Exponenciais de Software via Núcleos CUDA").  Bit c (0..7) selects chunk

@@ -73,10 +73,10 @@ OPT_CASES = [inputs.custom(1, 4, 1024, 1024, 64, False, sigma_qk=3.0, seed=41),
 
 @pytest.mark.parametrize("w", OPT_CASES, ids=lambda w: w.name)
 @pytest.mark.parametrize("poly", [0x100, 0xFF, 0x55, 0x11, 0x01, 0])
-@pytest.mark.parametrize("tau", [-1.0, 8.0, 32.0])
+@pytest.mark.parametrize("tau", [-1.0, 8.0, 32.0, 64.0])
 def test_exp2_paths_and_rescale_threshold(w, poly, tau):
     """Parity holds with every exp2 split (all MUFU, all polynomial, mixed) and
-    rescale thresholds τ = 0, 8 (default) and 32."""
+    rescale thresholds τ = 0, 8, 32 (default) and 64."""
     need_gpu()
     q, k, v = inputs.make_inputs(w)
     o, lse = run(w, q, k, v, options=attn.make_options(rescale_threshold=tau, poly_exp2_mask=poly))
@@ -85,7 +85,7 @@ def test_exp2_paths_and_rescale_threshold(w, poly, tau):
 
 
 def test_rescale_threshold_invariance_and_counts():
-    """τ changes only rounding; a larger τ rescales less often."""
+    """τ changes only rounding; a larger τ rescales less often (τ = 0 vs 8)."""
     need_gpu()
     w = inputs.custom(2, 4, 2048, 2048, 64, False, sigma_qk=3.0, seed=43)
     q, k, v = inputs.make_inputs(w)
