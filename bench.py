@@ -50,13 +50,28 @@ def load_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
+KERNEL_SOURCES = ["exact_attention_63_gb300/csrc/attn_fwd_kernel.cuh", "exact_attention_63_gb300/csrc/attn_device.cuh"]
+
+
+def kernel_source_hash():
+    import hashlib
+
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
 def load_profile_traffic(workload_name):
     """Per-launch DRAM bytes from the committed ncu summary, if it covers this
-    workload and the current kernel build (else None)."""
+    workload and was taken on the current kernel sources (else None)."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
             data = json.load(f)
+        if data.get("kernel_source_sha256_16") != kernel_source_hash():
+            return None
         return data.get(workload_name)
     except (OSError, ValueError):
         return None
