@@ -188,6 +188,7 @@ int attn_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse
   if ((rc = encode_bshd(&a.q, q, B, Sq, H, d)) != ATTN_OK) return rc;
   if ((rc = encode_bshd(&a.k, k, B, Sk, H, d)) != ATTN_OK) return rc;
   if ((rc = encode_bshd(&a.v, v, B, Sk, H, d)) != ATTN_OK) return rc;
+  if ((rc = encode_bshd(&a.o, o, B, Sq, H, d)) != ATTN_OK) return rc;
   const int n_qt = (Sq + 127) / 128;
   a.p.o = o;
   a.p.lse = lse;

@@ -41,6 +41,10 @@
 // current tile finishes, and the issuer starts the next tile's Q·Kᵀ while the
 // softmax warps write the current tile's output.
 //
+// The epilogue stages the tile's bf16 output in the tile's own Q buffer (idle
+// once the tile's last S has completed) and writes it with one TMA store; that
+// buffer is handed back to the loader only after the store has read it.
+//
 // TMEM columns (512 allocated): S buffers [0,128) and [128,256), O_0 [256,
 // 256+D), O_1 [256+D, 256+2D).  P_h (bf16, two per 32-bit column) overwrites
 // columns [64h, 64h+32) of its S buffer, inside the half that warpgroup h has
@@ -106,8 +110,8 @@ struct Layout {
   static constexpr uint32_t kStatsOff = kRingOff + kStages * kTileBytes;
   static constexpr uint32_t kBarOff = kStatsOff + 2 * 2 * kBM * 8;
   // barriers: q_full[2], q_empty[2], kv_full[S], kv_empty[S], s_full[2], p_full[2], pv_done[2],
-  //           o_final, exch_full[2], exch_empty[2], done[2]
-  static constexpr int kNumBars = 2 + 2 + 2 * kStages + 2 + 2 + 2 + 1 + 2 + 2 + 2;
+  //           o_final, exch_full[2], exch_empty[2], done[2], stage_full
+  static constexpr int kNumBars = 2 + 2 + 2 * kStages + 2 + 2 + 2 + 1 + 2 + 2 + 2 + 1;
   static constexpr uint32_t kMiscOff = kBarOff + 8 * kNumBars;  // tmem base (4 B) + abort flag (4 B)
   static constexpr uint32_t kSmemBytes = kMiscOff + 16 + 1024;  // + slack to align the base to 1024
   __device__ static constexpr uint32_t col_s(int buf) { return 128u * buf; }
@@ -154,7 +158,8 @@ __device__ __forceinline__ Tile tile_info(int idx, const FwdParams& p) {
 template <int D, bool CAUSAL, uint32_t POLY>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                    const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
+                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
+                    const FwdParams p) {
   using L = Layout<D>;
   extern __shared__ uint8_t smem_raw[];
   // 128-byte swizzled tiles need a 1024-byte aligned base.
@@ -176,6 +181,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto bar_exch_full = [&](int i) { return bars + 8u * (11 + 2 * L::kStages + i); };
   auto bar_exch_empty = [&](int i) { return bars + 8u * (13 + 2 * L::kStages + i); };
   auto bar_done = [&](int i) { return bars + 8u * (15 + 2 * L::kStages + i); };
+  const uint32_t bar_stage_full = bars + 8u * (17 + 2 * L::kStages);
   float2* const stats = reinterpret_cast<float2*>(smem + L::kStatsOff);
   uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMiscOff);
   volatile uint32_t* const abort_flag = reinterpret_cast<volatile uint32_t*>(smem + L::kMiscOff + 4);
@@ -207,6 +213,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar_kv_empty(s), 1);
     }
     mbar_init(bar_o_final, 1);
+    mbar_init(bar_stage_full, 2 * kBM);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     fence_proxy_async_smem();
   }
@@ -214,6 +221,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_desc(&tm_q);
     tma_prefetch_desc(&tm_k);
     tma_prefetch_desc(&tm_v);
+    tma_prefetch_desc(&tm_o);
   }
   __syncthreads();
   tc_fence_after();
@@ -322,7 +330,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             mma_commit(bar_s_full(buf));
             mma_commit(bar_kv_empty(slot));                     // K_j no longer read
-            if (j == T.nb - 1) mma_commit(bar_q_empty(qb));     // this tile's Q no longer read
+            // (The tile's Q buffer is released by the epilogue, which reuses it.)
           }
         }
       } else {
@@ -507,12 +515,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool landed = wait_bar(bar_o_final, tc & 1, wc);
       if (__any_sync(0xffffffffu, !landed)) { ok = false; break; }
       tc_fence_after();
-      // Warpgroup h writes output columns [h·D/2, (h+1)·D/2).
+      // Warpgroup h produces output columns [h·D/2, (h+1)·D/2), staged in the
+      // tile's Q buffer with the 128-byte swizzle the TMA store expects (16-byte
+      // chunk c of row r at c ^ (r % 8): conflict-free for 8 consecutive rows).
       const uint32_t t0 = tmem + L::col_o(0) + lane_off + h * (D / 2);
       const uint32_t t1 = tmem + L::col_o(1) + lane_off + h * (D / 2);
-      uint4* const orow = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.o) +
-                                                   ((static_cast<size_t>(T.b) * p.Sq + q_row) * p.H + T.h) * D +
-                                                   h * (D / 2));
+      const int qb = tc & 1;
+      uint8_t* const stage = smem + L::kQOff + qb * L::kTileBytes;
 #pragma unroll 1
       for (int c = 0; c < D / 64; ++c) {
         uint32_t x0[32], x1[32];
@@ -521,21 +530,33 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_wait_ld();
         reg_fence32(x0);
         reg_fence32(x1);
-        if (q_row < p.Sq) {
 #pragma unroll
-          for (int q16 = 0; q16 < 4; ++q16) {  // four 16-byte chunks of 8 values
-            float v[8];
+        for (int q16 = 0; q16 < 4; ++q16) {  // four 16-byte chunks of 8 values
+          float v[8];
 #pragma unroll
-            for (int e = 0; e < 8; ++e)
-              v[e] = w0 * __uint_as_float(x0[8 * q16 + e]) + w1 * __uint_as_float(x1[8 * q16 + e]);
-            uint4 wv;
-            wv.x = pack_bf16x2(v[0], v[1]);
-            wv.y = pack_bf16x2(v[2], v[3]);
-            wv.z = pack_bf16x2(v[4], v[5]);
-            wv.w = pack_bf16x2(v[6], v[7]);
-            orow[4 * c + q16] = wv;
-          }
+          for (int e = 0; e < 8; ++e)
+            v[e] = w0 * __uint_as_float(x0[8 * q16 + e]) + w1 * __uint_as_float(x1[8 * q16 + e]);
+          uint4 wv;
+          wv.x = pack_bf16x2(v[0], v[1]);
+          wv.y = pack_bf16x2(v[2], v[3]);
+          wv.z = pack_bf16x2(v[4], v[5]);
+          wv.w = pack_bf16x2(v[6], v[7]);
+          const int col = h * (D / 2) + 32 * c + 8 * q16;
+          const int chunk = (col & 63) >> 3;
+          *reinterpret_cast<uint4*>(stage + (col >> 6) * L::kSlabBytes + r * 128 + ((chunk ^ (r & 7)) << 4)) = wv;
         }
+      }
+      fence_proxy_async_smem();
+      mbar_arrive(bar_stage_full);
+      if (threadIdx.x == 0) {
+        // All 256 threads have staged their columns: one TMA store of the tile
+        // (rows beyond Sq are clipped), then release the Q buffer once read.
+        if (!wait_bar(bar_stage_full, tc & 1, wc)) { ok = false; break; }
+        for (int sl = 0; sl < L::kSlabs; ++sl)
+          tma_store_4d(&tm_o, smem_u32(stage) + sl * L::kSlabBytes, 64 * sl, T.h, T.q0, T.b);
+        tma_store_commit();
+        tma_store_wait_read0();
+        mbar_arrive(bar_q_empty(qb));
       }
       if (h == 0 && q_row < p.Sq) {
         const float lse = (Lsum > 0.f) ? (m + __log2f(Lsum)) * 0.69314718055994531f : -INFINITY;

@@ -12,7 +12,7 @@
 namespace attn {
 
 struct LaunchArgs {
-  CUtensorMap q, k, v;  // 4-D tiled maps, box (64, 1, 128, 1), 128-byte swizzle
+  CUtensorMap q, k, v, o;  // 4-D tiled maps, box (64, 1, 128, 1), 128-byte swizzle
   FwdParams p;
   int grid;             // persistent: min(tiles, SMs)
   uint32_t poly;           // exp2 chunk mask; one of kPolyMasks
@@ -48,7 +48,7 @@ cudaError_t launch_one(const LaunchArgs& a) {
     if (e != cudaSuccess) return e;
     configured[a.device] = true;
   }
-  attn_fwd_kernel<D, CAUSAL, POLY><<<a.grid, kThreads, smem, a.stream>>>(a.q, a.k, a.v, a.p);
+  attn_fwd_kernel<D, CAUSAL, POLY><<<a.grid, kThreads, smem, a.stream>>>(a.q, a.k, a.v, a.o, a.p);
   return cudaGetLastError();
 }
 
