@@ -18,8 +18,9 @@
 //   warp  8    loader — TMA loads of each tile's Q into one of two Q buffers,
 //              and of K and V tiles into a ring of shared-memory slots guarded
 //              by full/empty mbarriers, in the order the MMA issuer consumes
-//              them (K_0, K_1, then V_g, K_{g+2} for every block g, across tile
-//              boundaries), so slots free up in the order they are refilled;
+//              them (K_0 … K_{NB−1}, then V_g, K_{g+NB} for every block g,
+//              across tile boundaries), so slots free up in the order they are
+//              refilled;
 //              allocates and frees tensor memory
 //   warp  9    P·V issuer (one thread) — tcgen05.mma O_h += P_h V_j[64h:64h+64]
 //   warp 10    S issuer (one thread) — tcgen05.mma S = Q K_jᵀ
@@ -34,9 +35,10 @@
 // Online Mais Inteligente"), which after the first blocks is rare.
 //
 // The schedule is built around the tensor core, which runs a 128×128×16 bf16
-// MMA in 64 cycles: S is double-buffered in TMEM, so the issuer computes
-// S(j+1) and S(j+2) while the softmax still works on S(j); the softmax never
-// waits for a Q·Kᵀ, and the tensor core waits only for P.  Q is
+// MMA in 64 cycles: S has NB buffers in TMEM (two at d = 128, three at
+// d = 64), so the S issuer computes S(j+1) … S(j+NB) while the softmax still
+// works on S(j); the softmax seldom waits for a Q·Kᵀ, and the tensor core
+// waits only for P.  Q is
 // double-buffered in shared memory, so the next tile's Q arrives while the
 // current tile finishes, and the issuer starts the next tile's Q·Kᵀ while the
 // softmax warps write the current tile's output.
@@ -45,15 +47,15 @@
 // once the tile's last S has completed) and writes it with one TMA store; that
 // buffer is handed back to the loader only after the store has read it.
 //
-// TMEM columns (512 allocated): S buffers [0,128) and [128,256), O_0 [256,
-// 256+D), O_1 [256+D, 256+2D).  P_h (bf16, two per 32-bit column) overwrites
+// TMEM columns (512 allocated): S buffers [128·i, 128·i+128) for i < NB,
+// then O_0 [128·NB, 128·NB+D) and O_1 [128·NB+D, 128·NB+2D).  P_h (bf16, two per 32-bit column) overwrites
 // columns [64h, 64h+32) of its S buffer, inside the half that warpgroup h has
 // already read.
 //
 // Ordering rules the protocol relies on:
 //  * tcgen05.commit arrives only after all earlier MMAs of the committing
 //    thread complete; MMAs of different threads are not ordered.  So the S
-//    issuer waits for pv_done(g) — P(g)·V has completed — before S(g+2)
+//    issuer waits for pv_done(g) — P(g)·V has completed — before S(g+NB)
 //    reuses P(g)'s buffer.
 //  * O_h is written by P_h(g)·V only after p_full(g), i.e. after both
 //    warpgroups have finished block g (including any rescale of O_h), and a
@@ -63,7 +65,7 @@
 //    the phase waited for.  Every wait here has that property: the next
 //    phase needs work the waiting role has not released yet, and the
 //    previous one is implied by a barrier the role already passed (when the
-//    softmax sees S(g), P(g−2)·V has completed, because S(g) was issued after
+//    softmax sees S(g), P(g−NB)·V has completed, because S(g) was issued after
 //    waiting for it).  The epilogue waits on o_final, completed once per tile
 //    after its last P·V.
 #pragma once
@@ -104,6 +106,9 @@ struct Layout {
   static constexpr uint32_t kSlabBytes = kBM * 128;     // one 128-row slab: 16 KB
   static constexpr uint32_t kTileBytes = kSlabBytes * kSlabs;
   static constexpr int kStages = (D == 128) ? 4 : 10;   // K/V ring slots (each holds one K or V tile)
+  // S buffers in TMEM: the S issuer runs this many blocks ahead of the
+  // softmax.  Three fit at d = 64 (3·128 + 2·64 = 512 columns), two at d = 128.
+  static constexpr int kSBufs = (D == 64) ? 3 : 2;
   static constexpr uint32_t kQOff = 0;                  // two Q buffers
   static constexpr uint32_t kRingOff = 2 * kTileBytes;
   // per-row (max, sum) of each half, exchanged once per tile: [tile parity][half][row] float2
@@ -111,11 +116,13 @@ struct Layout {
   static constexpr uint32_t kBarOff = kStatsOff + 2 * 2 * kBM * 8;
   // barriers: q_full[2], q_empty[2], kv_full[S], kv_empty[S], s_full[2], p_full[2], pv_done[2],
   //           o_final, exch_full[2], exch_empty[2], done[2], stage_full
-  static constexpr int kNumBars = 2 + 2 + 2 * kStages + 2 + 2 + 2 + 1 + 2 + 2 + 2 + 1;
+  static constexpr int kNumBars = 2 + 2 + 2 * kStages + 3 * kSBufs + 1 + 2 + 2 + 2 + 1;
   static constexpr uint32_t kMiscOff = kBarOff + 8 * kNumBars;  // tmem base (4 B) + abort flag (4 B)
   static constexpr uint32_t kSmemBytes = kMiscOff + 16 + 1024;  // + slack to align the base to 1024
   __device__ static constexpr uint32_t col_s(int buf) { return 128u * buf; }
-  __device__ static constexpr uint32_t col_o(int half) { return 256u + static_cast<uint32_t>(D) * half; }
+  __device__ static constexpr uint32_t col_o(int half) {
+    return 128u * kSBufs + static_cast<uint32_t>(D) * half;
+  }
 };
 
 __device__ __forceinline__ void reg_fence32(uint32_t (&r)[32]) {
@@ -174,14 +181,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto bar_q_empty = [&](int i) { return bars + 8u * (2 + i); };
   auto bar_kv_full = [&](int s) { return bars + 8u * (4 + s); };
   auto bar_kv_empty = [&](int s) { return bars + 8u * (4 + L::kStages + s); };
-  auto bar_s_full = [&](int i) { return bars + 8u * (4 + 2 * L::kStages + i); };
-  auto bar_p_full = [&](int i) { return bars + 8u * (6 + 2 * L::kStages + i); };
-  auto bar_pv_done = [&](int i) { return bars + 8u * (8 + 2 * L::kStages + i); };
-  const uint32_t bar_o_final = bars + 8u * (10 + 2 * L::kStages);
-  auto bar_exch_full = [&](int i) { return bars + 8u * (11 + 2 * L::kStages + i); };
-  auto bar_exch_empty = [&](int i) { return bars + 8u * (13 + 2 * L::kStages + i); };
-  auto bar_done = [&](int i) { return bars + 8u * (15 + 2 * L::kStages + i); };
-  const uint32_t bar_stage_full = bars + 8u * (17 + 2 * L::kStages);
+  constexpr int NB = L::kSBufs;
+  constexpr uint32_t kB0 = 4 + 2 * L::kStages;  // first per-S-buffer barrier
+  auto bar_s_full = [&](int i) { return bars + 8u * (kB0 + i); };
+  auto bar_p_full = [&](int i) { return bars + 8u * (kB0 + NB + i); };
+  auto bar_pv_done = [&](int i) { return bars + 8u * (kB0 + 2 * NB + i); };
+  const uint32_t bar_o_final = bars + 8u * (kB0 + 3 * NB);
+  auto bar_exch_full = [&](int i) { return bars + 8u * (kB0 + 3 * NB + 1 + i); };
+  auto bar_exch_empty = [&](int i) { return bars + 8u * (kB0 + 3 * NB + 3 + i); };
+  auto bar_done = [&](int i) { return bars + 8u * (kB0 + 3 * NB + 5 + i); };
+  const uint32_t bar_stage_full = bars + 8u * (kB0 + 3 * NB + 7);
   float2* const stats = reinterpret_cast<float2*>(smem + L::kStatsOff);
   uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMiscOff);
   volatile uint32_t* const abort_flag = reinterpret_cast<volatile uint32_t*>(smem + L::kMiscOff + 4);
@@ -201,9 +210,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar_q_full(i), 1);
       mbar_init(bar_q_empty(i), 1);
+    }
+    for (int i = 0; i < NB; ++i) {
       mbar_init(bar_s_full(i), 1);
       mbar_init(bar_p_full(i), 2 * kBM);  // both warpgroups
       mbar_init(bar_pv_done(i), 1);
+    }
+    for (int i = 0; i < 2; ++i) {
       mbar_init(bar_done(i), 1);
       mbar_init(bar_exch_full(i), 2 * kBM);
       mbar_init(bar_exch_empty(i), 2 * kBM);
@@ -271,7 +284,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         return true;
       };
-      while (ok && k_idx < p.n_tiles && gK < gV + 2) ok = load_k();
+      while (ok && k_idx < p.n_tiles && gK < gV + NB) ok = load_k();
       while (ok && v_idx < p.n_tiles) {
         if (!ring_load(&tm_v, v_T, v_j)) { ok = false; break; }
         ++gV;
@@ -280,7 +293,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           v_idx += stride;
           if (v_idx < p.n_tiles) v_T = tile_info<CAUSAL>(v_idx, p);
         }
-        while (ok && k_idx < p.n_tiles && gK < gV + 2) ok = load_k();
+        while (ok && k_idx < p.n_tiles && gK < gV + NB) ok = load_k();
       }
       // Let every copy still in flight land before the CTA can exit (the
       // newest load of each slot and of each Q buffer; older ones completed
@@ -295,9 +308,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == kSWarp || warp == kPvWarp) {
     // ====================================================== MMA issuers
-    // Ring positions follow the loader's order K_0, K_1, V_0, K_2, V_1, …,
-    // K_{G−1}, V_{G−2}, V_{G−1} over the CTA's G blocks: K_0 → 0, K_g → 2g−1,
-    // V_g → 2g+2, except the last V_{G−1} → 2G−1.
+    // Ring positions follow the loader's order K_0 … K_{NB−1}, then V_g,
+    // K_{g+NB} per block g, then the remaining V's, over the CTA's G blocks:
+    // K_j → j for j < NB, else 2j − NB + 1; V_g → min(2g + NB, G + g).
     if (lane == 0) {
       bool ok = true;
       if (warp == kSWarp) {
@@ -313,11 +326,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           const Tile T = tile_info<CAUSAL>(idx, p);
           const int qb = tc & 1;
           for (int j = 0; j < T.nb; ++j, ++g) {
-            const int buf = g & 1;
-            // S(g) reuses the buffer of P(g−2): that P·V must have completed.
-            if (g >= 2 && !wait_bar(bar_pv_done(buf), ((g - 2) >> 1) & 1, wc)) { ok = false; break; }
+            const int buf = g % NB;
+            // S(g) reuses the buffer of P(g−NB): that P·V must have completed.
+            if (g >= NB && !wait_bar(bar_pv_done(buf), ((g - NB) / NB) & 1, wc)) { ok = false; break; }
             if (j == 0 && !wait_bar(bar_q_full(qb), (tc >> 1) & 1, wc)) { ok = false; break; }
-            const int n = (g == 0) ? 0 : 2 * g - 1, slot = n % L::kStages;
+            const int n = (g < NB) ? g : 2 * g - NB + 1, slot = n % L::kStages;
             if (!wait_bar(bar_kv_full(slot), (n / L::kStages) & 1, wc)) { ok = false; break; }
             tc_fence_after();
             const uint64_t dq = dQ + ((qb * L::kTileBytes) >> 4);
@@ -343,9 +356,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int idx = blockIdx.x; idx < p.n_tiles && ok; idx += stride) {
           const Tile T = tile_info<CAUSAL>(idx, p);
           for (int j = 0; j < T.nb; ++j, ++g) {
-            const int buf = g & 1;
-            if (!wait_bar(bar_p_full(buf), (g >> 1) & 1, wc)) { ok = false; break; }
-            const int n = (g == G - 1) ? 2 * G - 1 : 2 * g + 2, slot = n % L::kStages;
+            const int buf = g % NB;
+            if (!wait_bar(bar_p_full(buf), (g / NB) & 1, wc)) { ok = false; break; }
+            const int n = min(2 * g + NB, G + g), slot = n % L::kStages;
             if (!wait_bar(bar_kv_full(slot), (n / L::kStages) & 1, wc)) { ok = false; break; }
             tc_fence_after();
             // O_h (+)= P_h(g) · V_j[64h : 64h+64]
@@ -389,9 +402,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       float m_run = -INFINITY;  // running reference maximum of this half (log2 domain)
       float l_run = 0.f;        // running row sum of this half (fp32, unrounded p)
       for (int j = 0; j < T.nb; ++j, ++g) {
-        const int buf = g & 1;
+        const int buf = g % NB;
         const uint32_t tS = tmem + L::col_s(buf) + kHalf * h + lane_off;
-        const bool got = wait_bar(bar_s_full(buf), (g >> 1) & 1, wc);
+        const bool got = wait_bar(bar_s_full(buf), (g / NB) & 1, wc);
         if (__any_sync(0xffffffffu, !got)) { ok = false; break; }
         tc_fence_after();
         // This half of the S row (64 fp32) in registers: two loads, one wait.
@@ -431,7 +444,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const float alpha = need ? ex2_mufu(m_run - m_new) : 1.f;
           if (j > 0) {
             // O_h holds the tile's blocks < j; wait for the last P_h·V to land.
-            const bool landed = wait_bar(bar_pv_done((g - 1) & 1), ((g - 1) >> 1) & 1, wc);
+            const bool landed = wait_bar(bar_pv_done((g - 1) % NB), ((g - 1) / NB) & 1, wc);
             if (__any_sync(0xffffffffu, !landed)) { ok = false; break; }
             tc_fence_after();
 #pragma unroll 1
