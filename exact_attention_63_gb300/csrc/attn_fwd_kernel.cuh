@@ -6,7 +6,7 @@
 // ("FlashAttention 4: Atenção Mais Rápida …", section "Novidades no
 // FlashAttention 4": blocks of Q, K, V streamed through on-chip memory).
 //
-// Warp roles (320 threads):
+// Warp roles (384 threads):
 //   warps 0-7  softmax, two warpgroups: warpgroup h owns keys [64h, 64h+64)
 //              of every 128-key block, one thread per query row (= TMEM
 //              lane).  Each half is an independent online softmax with its
@@ -24,6 +24,7 @@
 //              allocates and frees tensor memory
 //   warp  9    P·V issuer (one thread) — tcgen05.mma O_h += P_h V_j[64h:64h+64]
 //   warp 10    S issuer (one thread) — tcgen05.mma S = Q K_jᵀ
+//   warp 11    output store (one thread) — TMA store of each finished tile
 //              Accumulators live in tensor memory.  An MMA issue stalls while
 //              the tensor core's queue is full, so a single issuer leaves the
 //              tensor core idle during each of its barrier waits; with two,
@@ -44,8 +45,9 @@
 // softmax warps write the current tile's output.
 //
 // The epilogue stages the tile's bf16 output in the tile's own Q buffer (idle
-// once the tile's last S has completed) and writes it with one TMA store; that
-// buffer is handed back to the loader only after the store has read it.
+// once the tile's last S has completed); the store warp writes it with one TMA
+// store and hands the buffer back to the loader only after the store has read
+// it.
 //
 // TMEM columns (512 allocated): S buffers [128·i, 128·i+128) for i < NB,
 // then O_0 [128·NB, 128·NB+D) and O_1 [128·NB+D, 128·NB+2D).  P_h (bf16, two per 32-bit column) overwrites
@@ -67,7 +69,10 @@
 //    previous one is implied by a barrier the role already passed (when the
 //    softmax sees S(g), P(g−NB)·V has completed, because S(g) was issued after
 //    waiting for it).  The epilogue waits on o_final, completed once per tile
-//    after its last P·V.
+//    after its last P·V.  stage_full(b) serves the tiles staged in Q buffer
+//    b; it cannot run two phases ahead of the store warp, because staging
+//    tile t+2 in buffer b needs that tile's Q, which the loader brings only
+//    after the store of tile t has released the buffer.
 #pragma once
 
 #include <cstdint>
@@ -79,10 +84,12 @@ namespace attn {
 
 constexpr int kBM = 128;       // query rows per tile (= TMEM lanes)
 constexpr int kBN = 128;       // keys per block
-constexpr int kThreads = 352;  // 8 softmax warps + loader + 2 MMA issuers
+constexpr int kThreads = 384;  // 8 softmax warps + loader + 2 MMA issuers + output store
 constexpr int kLoaderWarp = 8;
 constexpr int kPvWarp = 9;
 constexpr int kSWarp = 10;
+constexpr int kStoreWarp = 11;
+constexpr int kSoftmaxWarps = 8;
 constexpr uint32_t kTmemCols = 512;
 
 struct FwdParams {
@@ -114,9 +121,9 @@ struct Layout {
   // per-row (max, sum) of each half, exchanged once per tile: [tile parity][half][row] float2
   static constexpr uint32_t kStatsOff = kRingOff + kStages * kTileBytes;
   static constexpr uint32_t kBarOff = kStatsOff + 2 * 2 * kBM * 8;
-  // barriers: q_full[2], q_empty[2], kv_full[S], kv_empty[S], s_full[2], p_full[2], pv_done[2],
-  //           o_final, exch_full[2], exch_empty[2], done[2], stage_full
-  static constexpr int kNumBars = 2 + 2 + 2 * kStages + 3 * kSBufs + 1 + 2 + 2 + 2 + 1;
+  // barriers: q_full[2], q_empty[2], kv_full[S], kv_empty[S], s_full[NB], p_full[NB], pv_done[NB],
+  //           o_final, exch_full[2], exch_empty[2], done[2], stage_full[2]
+  static constexpr int kNumBars = 2 + 2 + 2 * kStages + 3 * kSBufs + 1 + 2 + 2 + 2 + 2;
   static constexpr uint32_t kMiscOff = kBarOff + 8 * kNumBars;  // tmem base (4 B) + abort flag (4 B)
   static constexpr uint32_t kSmemBytes = kMiscOff + 16 + 1024;  // + slack to align the base to 1024
   __device__ static constexpr uint32_t col_s(int buf) { return 128u * buf; }
@@ -130,6 +137,15 @@ __device__ __forceinline__ void reg_fence32(uint32_t (&r)[32]) {
   for (int i = 0; i < 32; i += 8)
     asm volatile("" : "+r"(r[i]), "+r"(r[i + 1]), "+r"(r[i + 2]), "+r"(r[i + 3]), "+r"(r[i + 4]),
                  "+r"(r[i + 5]), "+r"(r[i + 6]), "+r"(r[i + 7]));
+}
+
+// One arrival for the whole warp: the lanes' earlier shared-memory writes (and,
+// after tcgen05.wait + fence::before_thread_sync, their tensor-memory stores)
+// are ordered before lane 0's release by the warp barrier.  The softmax
+// barriers then take 8 arrivals a block instead of 256.
+__device__ __forceinline__ void warp_arrive(uint32_t bar, int lane) {
+  __syncwarp();
+  if (lane == 0) mbar_arrive(bar);
 }
 
 // One work tile: 128 query rows of one (batch, head).
@@ -190,7 +206,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto bar_exch_full = [&](int i) { return bars + 8u * (kB0 + 3 * NB + 1 + i); };
   auto bar_exch_empty = [&](int i) { return bars + 8u * (kB0 + 3 * NB + 3 + i); };
   auto bar_done = [&](int i) { return bars + 8u * (kB0 + 3 * NB + 5 + i); };
-  const uint32_t bar_stage_full = bars + 8u * (kB0 + 3 * NB + 7);
+  auto bar_stage_full = [&](int i) { return bars + 8u * (kB0 + 3 * NB + 7 + i); };
   float2* const stats = reinterpret_cast<float2*>(smem + L::kStatsOff);
   uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMiscOff);
   volatile uint32_t* const abort_flag = reinterpret_cast<volatile uint32_t*>(smem + L::kMiscOff + 4);
@@ -213,20 +229,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int i = 0; i < NB; ++i) {
       mbar_init(bar_s_full(i), 1);
-      mbar_init(bar_p_full(i), 2 * kBM);  // both warpgroups
+      mbar_init(bar_p_full(i), kSoftmaxWarps);  // one arrival per softmax warp
       mbar_init(bar_pv_done(i), 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar_done(i), 1);
-      mbar_init(bar_exch_full(i), 2 * kBM);
-      mbar_init(bar_exch_empty(i), 2 * kBM);
+      mbar_init(bar_exch_full(i), kSoftmaxWarps);
+      mbar_init(bar_exch_empty(i), kSoftmaxWarps);
     }
     for (int s = 0; s < L::kStages; ++s) {
       mbar_init(bar_kv_full(s), 1);
       mbar_init(bar_kv_empty(s), 1);
     }
     mbar_init(bar_o_final, 1);
-    mbar_init(bar_stage_full, 2 * kBM);
+    for (int i = 0; i < 2; ++i) mbar_init(bar_stage_full(i), kSoftmaxWarps);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     fence_proxy_async_smem();
   }
@@ -305,6 +321,25 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int n = (q_issued > 2 ? q_issued - 2 : 0); n < q_issued; ++n)
         while (!mbar_try_wait(bar_q_full(n & 1), (n >> 1) & 1u))
           if (globaltimer_ns() - t0 > p.timeout_ns) break;
+    }
+  } else if (warp == kStoreWarp) {
+    // ===================================================== output store
+    // The softmax warps stage each tile's bf16 output in the tile's Q buffer;
+    // one TMA store writes it (rows beyond Sq are clipped), and the buffer
+    // goes back to the loader once the store has read it.  Doing this here
+    // keeps the store's latency off the softmax warps.
+    if (lane == 0) {
+      int tc = 0;
+      for (int idx = blockIdx.x; idx < p.n_tiles; idx += stride, ++tc) {
+        const Tile T = tile_info<CAUSAL>(idx, p);
+        const int qb = tc & 1;
+        if (!wait_bar(bar_stage_full(qb), (tc >> 1) & 1, wc)) break;
+        for (int sl = 0; sl < L::kSlabs; ++sl)
+          tma_store_4d(&tm_o, sQ + qb * L::kTileBytes + sl * L::kSlabBytes, 64 * sl, T.h, T.q0, T.b);
+        tma_store_commit();
+        tma_store_wait_read0();
+        mbar_arrive(bar_q_empty(qb));
+      }
     }
   } else if (warp == kSWarp || warp == kPvWarp) {
     // ====================================================== MMA issuers
@@ -497,7 +532,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         l_run += (a0 + a1) + (b0 + b1);
         tmem_wait_st();
         tc_fence_before();
-        mbar_arrive(bar_p_full(buf));
+        warp_arrive(bar_p_full(buf), lane);
       }
       if (!ok) break;
       // ---------------------------------------------------- epilogue
@@ -508,13 +543,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (__any_sync(0xffffffffu, !free_)) { ok = false; break; }
       }
       stats[(par * 2 + h) * kBM + r] = make_float2(m_run, l_run);
-      mbar_arrive(bar_exch_full(par));
+      warp_arrive(bar_exch_full(par), lane);
       {
         const bool in = wait_bar(bar_exch_full(par), (tc >> 1) & 1, wc);
         if (__any_sync(0xffffffffu, !in)) { ok = false; break; }
       }
       const float2 other = stats[(par * 2 + (h ^ 1)) * kBM + r];
-      mbar_arrive(bar_exch_empty(par));
+      warp_arrive(bar_exch_empty(par), lane);
       // Merge the halves: m = max, a_i = 2^(m_i − m), L = Σ a_i l_i.
       const float m0 = h ? other.x : m_run, l0 = h ? other.y : l_run;
       const float m1 = h ? m_run : other.x, l1 = h ? l_run : other.y;
@@ -560,17 +595,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       fence_proxy_async_smem();
-      mbar_arrive(bar_stage_full);
-      if (threadIdx.x == 0) {
-        // All 256 threads have staged their columns: one TMA store of the tile
-        // (rows beyond Sq are clipped), then release the Q buffer once read.
-        if (!wait_bar(bar_stage_full, tc & 1, wc)) { ok = false; break; }
-        for (int sl = 0; sl < L::kSlabs; ++sl)
-          tma_store_4d(&tm_o, smem_u32(stage) + sl * L::kSlabBytes, 64 * sl, T.h, T.q0, T.b);
-        tma_store_commit();
-        tma_store_wait_read0();
-        mbar_arrive(bar_q_empty(qb));
-      }
+      warp_arrive(bar_stage_full(qb), lane);  // the store warp writes the tile out
       if (h == 0 && q_row < p.Sq) {
         const float lse = (Lsum > 0.f) ? (m + __log2f(Lsum)) * 0.69314718055994531f : -INFINITY;
         p.lse[(static_cast<size_t>(T.b) * p.H + T.h) * p.Sq + q_row] = lse;
