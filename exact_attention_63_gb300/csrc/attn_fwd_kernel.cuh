@@ -76,6 +76,8 @@
 #pragma once
 
 #include <cstdint>
+#include <type_traits>
+
 #include <cuda.h>
 
 #include "attn_device.cuh"
@@ -148,6 +150,41 @@ __device__ __forceinline__ void warp_arrive(uint32_t bar, int lane) {
   if (lane == 0) mbar_arrive(bar);
 }
 
+// The rescale of O_h after a row's running maximum moved at a block j > 0:
+// wait until the previous P_h·V has landed in O_h, then O_h[row, :] *= alpha
+// for this thread's row.  Rare after a tile's first blocks, so it is kept out
+// of line: the per-block softmax code then carries neither this wait loop nor
+// the scaling (inlined, they slowed the common path by several percent).
+// Returns false when the wait ran out of time.
+template <int D>
+__device__ __noinline__ bool rescale_o(uint32_t bar_pv, uint32_t parity, WaitCtx wc, uint32_t t_o, float alpha) {
+  const bool landed = wait_bar(bar_pv, parity, wc);
+  if (__any_sync(0xffffffffu, !landed)) return false;
+  tc_fence_after();
+#pragma unroll 1
+  for (int c = 0; c < D / 32; ++c) {
+    uint32_t o[32];
+    tmem_ld32(t_o + 32 * c, o);
+    tmem_wait_ld();
+    reg_fence32(o);
+#pragma unroll
+    for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+    tmem_st32(t_o + 32 * c, o);
+  }
+  return true;
+}
+
+// wait_bar with only the first test inline; the retry loop is a call, which
+// keeps the per-block softmax code short where the barrier has usually
+// completed already.
+static __device__ __noinline__ bool wait_bar_retry(uint32_t bar, uint32_t parity, WaitCtx c) {
+  return wait_bar(bar, parity, c);
+}
+__device__ __forceinline__ bool wait_bar_cold(uint32_t bar, uint32_t parity, const WaitCtx& c) {
+  if (mbar_try_wait(bar, parity)) return true;
+  return wait_bar_retry(bar, parity, c);
+}
+
 // One work tile: 128 query rows of one (batch, head).
 struct Tile {
   int b, h, q0, nb;  // nb = key blocks visible to the tile
@@ -178,7 +215,8 @@ __device__ __forceinline__ Tile tile_info(int idx, const FwdParams& p) {
 
 // POLY: bit c selects the FMA-pipe polynomial exp2 for 16-column chunk c of
 // every 128-key block (compile time, so the exp loop is one basic block).
-template <int D, bool CAUSAL, uint32_t POLY>
+// COUNT: compile the diagnostic counters (only launched when requested).
+template <int D, bool CAUSAL, uint32_t POLY, bool COUNT>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
@@ -436,33 +474,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int q_row = T.q0 + r;
       float m_run = -INFINITY;  // running reference maximum of this half (log2 domain)
       float l_run = 0.f;        // running row sum of this half (fp32, unrounded p)
-      for (int j = 0; j < T.nb; ++j, ++g) {
-        const int buf = g % NB;
-        const uint32_t tS = tmem + L::col_s(buf) + kHalf * h + lane_off;
-        const bool got = wait_bar(bar_s_full(buf), (g / NB) & 1, wc);
-        if (__any_sync(0xffffffffu, !got)) { ok = false; break; }
-        tc_fence_after();
-        // This half of the S row (64 fp32) in registers: two loads, one wait.
-        uint32_t u[kHalf];
-        tmem_ld32(tS, *reinterpret_cast<uint32_t(*)[32]>(&u[0]));
-        tmem_ld32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&u[32]));
-        tmem_wait_ld();
-        reg_fence32(*reinterpret_cast<uint32_t(*)[32]>(&u[0]));
-        reg_fence32(*reinterpret_cast<uint32_t(*)[32]>(&u[32]));
-        float* const s = reinterpret_cast<float*>(u);
-        const int k0 = j * kBN + kHalf * h;
-        if (k0 + kHalf > p.Sk || (CAUSAL && k0 + kHalf - 1 > T.q0)) {
-#pragma unroll
-          for (int c = 0; c < kHalf; ++c) {
-            const int key = k0 + c;
-            if (key >= p.Sk || (CAUSAL && key > q_row)) s[c] = -INFINITY;
-          }
-        }
-        // Row maximum of this half: four independent 16-wide chains.
+      // Row maximum of this half (log2 domain): four independent 16-wide chains.
+      auto row_max = [&](const float* x0) -> float {
         float m4[4];
 #pragma unroll
         for (int gg = 0; gg < 4; ++gg) {
-          const float* x = s + 16 * gg;
+          const float* x = x0 + 16 * gg;
           float a = fmax3(x[0], x[1], x[2]);
           float b2 = fmax3(x[3], x[4], x[5]);
           a = fmax3(a, x[6], x[7]);
@@ -471,41 +488,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           b2 = fmax3(b2, x[12], x[13]);
           m4[gg] = fmax3(a, b2, fmaxf(x[14], x[15]));
         }
-        float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
-        mx *= sc;
-        const bool need = mx > m_run + p.tau;
-        if (__any_sync(0xffffffffu, need)) {
-          const float m_new = need ? mx : m_run;
-          const float alpha = need ? ex2_mufu(m_run - m_new) : 1.f;
-          if (j > 0) {
-            // O_h holds the tile's blocks < j; wait for the last P_h·V to land.
-            const bool landed = wait_bar(bar_pv_done((g - 1) % NB), ((g - 1) / NB) & 1, wc);
-            if (__any_sync(0xffffffffu, !landed)) { ok = false; break; }
-            tc_fence_after();
-#pragma unroll 1
-            for (int c = 0; c < D / 32; ++c) {
-              uint32_t o[32];
-              tmem_ld32(tOh + 32 * c, o);
-              tmem_wait_ld();
-              reg_fence32(o);
-#pragma unroll
-              for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-              tmem_st32(tOh + 32 * c, o);
-            }
-          }
-          l_run *= alpha;
-          m_run = m_new;
-          if (p.counters != nullptr) {
-            const unsigned int nres = __popc(__ballot_sync(0xffffffffu, need));
-            if (lane == 0) atomicAdd(p.counters, static_cast<unsigned long long>(nres));
-          }
-        }
-        if (p.counters != nullptr && lane == 0 && h == 0) atomicAdd(p.counters + 1, 32ull);
-        __syncwarp();
+        return fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * sc;
+      };
+      // p = 2^(s·scale·log2 e − m_run) for this half's 64 keys: bf16 pairs in
+      // pk, the fp32 sum of the unrounded values returned.
+      auto exps = [&](const float* s, uint32_t (&pk)[kHalf / 2]) -> float {
         const float negm = (m_run == -INFINITY) ? 0.f : -m_run;
         const uint64_t nm2 = pack2(negm, negm);
         uint64_t acc[4] = {0, 0, 0, 0};  // four packed partial sums (+0.0f pairs)
-        uint32_t pk[kHalf / 2];
 #pragma unroll
         for (int ch = 0; ch < kHalf / 16; ++ch) {
           constexpr uint32_t kPoly = POLY;
@@ -525,15 +515,73 @@ __global__ void __launch_bounds__(kThreads, 1)
             pk[ch * 8 + i] = pack_bf16x2(x0, x1);
           }
         }
-        tmem_st32(tS, pk);  // P_h over the first 32 columns of this half
         float a0, a1, b0, b1;
         unpack2(fadd2(acc[0], acc[1]), a0, a1);
         unpack2(fadd2(acc[2], acc[3]), b0, b1);
-        l_run += (a0 + a1) + (b0 + b1);
+        return (a0 + a1) + (b0 + b1);
+      };
+      // One key block.  MASK selects the copy that masks keys beyond Sk and,
+      // when causal, keys after the row; only the tile's last blocks need it,
+      // so the loop over the other blocks runs a copy without that code.
+      auto block = [&](int j, auto mask_tag) -> bool {
+        constexpr bool MASK = decltype(mask_tag)::value;
+        const int buf = g % NB;
+        const uint32_t tS = tmem + L::col_s(buf) + kHalf * h + lane_off;
+        const bool got = wait_bar_cold(bar_s_full(buf), (g / NB) & 1, wc);
+        if (__any_sync(0xffffffffu, !got)) return false;
+        tc_fence_after();
+        // This half of the S row (64 fp32) in registers: two loads, one wait.
+        uint32_t u[kHalf];
+        tmem_ld32(tS, *reinterpret_cast<uint32_t(*)[32]>(&u[0]));
+        tmem_ld32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&u[32]));
+        tmem_wait_ld();
+        reg_fence32(*reinterpret_cast<uint32_t(*)[32]>(&u[0]));
+        reg_fence32(*reinterpret_cast<uint32_t(*)[32]>(&u[32]));
+        float* const s = reinterpret_cast<float*>(u);
+        if constexpr (MASK) {
+          const int k0 = j * kBN + kHalf * h;
+#pragma unroll
+          for (int c = 0; c < kHalf; ++c) {
+            const int key = k0 + c;
+            if (key >= p.Sk || (CAUSAL && key > q_row)) s[c] = -INFINITY;
+          }
+        }
+        const float mx = row_max(s);
+        const bool need = mx > m_run + p.tau;
+        if (__any_sync(0xffffffffu, need)) {
+          const float m_new = need ? mx : m_run;
+          const float alpha = need ? ex2_mufu(m_run - m_new) : 1.f;
+          // O_h holds the tile's blocks < j once the last P_h·V has landed.
+          if (j > 0 && !rescale_o<D>(bar_pv_done((g - 1) % NB), ((g - 1) / NB) & 1, wc, tOh, alpha))
+            return false;
+          l_run *= alpha;
+          m_run = m_new;
+          if constexpr (COUNT) {
+            const unsigned int nres = __popc(__ballot_sync(0xffffffffu, need));
+            if (lane == 0) atomicAdd(p.counters, static_cast<unsigned long long>(nres));
+          }
+        }
+        __syncwarp();
+        uint32_t pk[kHalf / 2];
+        const float lsum = exps(s, pk);
+        if constexpr (COUNT) {
+          if (lane == 0 && h == 0) atomicAdd(p.counters + 1, 32ull);
+        }
+        tmem_st32(tS, pk);  // P_h over the first 32 columns of this half
+        l_run += lsum;
         tmem_wait_st();
         tc_fence_before();
         warp_arrive(bar_p_full(buf), lane);
-      }
+        return true;
+      };
+      // Block j needs no mask for this half when all its keys lie below lim
+      // (Sk, and when causal also the tile's first row + 1):
+      // 128j + 64h + 64 ≤ lim, i.e. j < (lim − 64h + 64) / 128.
+      const int lim = CAUSAL ? min(p.Sk, T.q0 + 1) : p.Sk;
+      const int n_full = min(T.nb, max(0, (lim - kHalf * h + kHalf) / kBN));
+      int j = 0;
+      for (; j < n_full && ok; ++j, ++g) ok = block(j, std::false_type{});
+      for (; j < T.nb && ok; ++j, ++g) ok = block(j, std::true_type{});
       if (!ok) break;
       // ---------------------------------------------------- epilogue
       // Exchange (max, sum) with the other half's thread of the same row.

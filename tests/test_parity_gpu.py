@@ -30,6 +30,12 @@ SMALL = [
     inputs.custom(3, 1, 384, 1000, 64, False, seed=32),
     inputs.custom(1, 2, 257, 383, 128, False, sigma_qk=3.0, seed=33),
     inputs.custom(1, 1, 1000, 17, 128, True, seed=34),
+    # key counts at the 64-key half boundaries of a block: the last block's
+    # second half empty (192), holding one key (65), first half one short (63)
+    inputs.custom(1, 2, 192, 192, 64, False, seed=35),
+    inputs.custom(1, 2, 320, 192, 128, True, seed=36),
+    inputs.custom(2, 1, 150, 65, 64, True, seed=37),
+    inputs.custom(1, 3, 130, 63, 128, False, seed=38),
 ]
 
 
