@@ -400,11 +400,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int qb = tc & 1;
           for (int j = 0; j < T.nb; ++j, ++g) {
             const int buf = g % NB;
-            // S(g) reuses the buffer of P(g−NB): that P·V must have completed.
-            if (g >= NB && !wait_bar(bar_pv_done(buf), ((g - NB) / NB) & 1, wc)) { ok = false; break; }
+            // Operands first: Q and K_j arrive well ahead, so these waits stay
+            // off the softmax → P·V → S chain.  (K_j's ring slot was freed by
+            // an S this thread has already issued, so waiting here first
+            // cannot block that chain.)
             if (j == 0 && !wait_bar(bar_q_full(qb), (tc >> 1) & 1, wc)) { ok = false; break; }
             const int n = (g < NB) ? g : 2 * g - NB + 1, slot = n % L::kStages;
             if (!wait_bar(bar_kv_full(slot), (n / L::kStages) & 1, wc)) { ok = false; break; }
+            // S(g) reuses the buffer of P(g−NB): that P·V must have completed.
+            if (g >= NB && !wait_bar(bar_pv_done(buf), ((g - NB) / NB) & 1, wc)) { ok = false; break; }
             tc_fence_after();
             const uint64_t dq = dQ + ((qb * L::kTileBytes) >> 4);
             const uint64_t dk = dK + ((slot * L::kTileBytes) >> 4);
@@ -430,9 +434,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           const Tile T = tile_info<CAUSAL>(idx, p);
           for (int j = 0; j < T.nb; ++j, ++g) {
             const int buf = g % NB;
-            if (!wait_bar(bar_p_full(buf), (g / NB) & 1, wc)) { ok = false; break; }
+            // V_j first (loaded well ahead; its slot was freed by a P·V this
+            // thread already issued), then the softmax's P(g).
             const int n = min(2 * g + NB, G + g), slot = n % L::kStages;
             if (!wait_bar(bar_kv_full(slot), (n / L::kStages) & 1, wc)) { ok = false; break; }
+            if (!wait_bar(bar_p_full(buf), (g / NB) & 1, wc)) { ok = false; break; }
             tc_fence_after();
             // O_h (+)= P_h(g) · V_j[64h : 64h+64]
             const uint64_t dv = dV + ((slot * L::kTileBytes) >> 4);
