@@ -17,6 +17,7 @@ from .attention import (  # noqa: F401
     attention_rows,
     head_probabilities,
     head_scores,
+    kv_head,
     visible_mask,
     combine_partials,
     to_f64,

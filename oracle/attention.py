@@ -25,7 +25,15 @@ Readings where the pages are silent (each also listed in the design notes):
   * layout: Q, K, V, O are (batch, seq, heads, head_dim), the only layout the
     pages show ("FlashAttention-3: Pipeline Assíncrono …", section
     "Implementando FlashAttention-3 em produção"); LSE is (batch, heads, Sq).
-  * causal: key j is visible to query i iff j ≤ i (top-left alignment).
+  * causal: key j is visible to query i iff j ≤ i (top-left alignment).  The
+    pages give no rule for Sq ≠ Sk; the other common one, bottom-right
+    alignment (j ≤ i + Sk − Sq: the last query row sees every key), is the
+    ``causal_offset = Sk − Sq`` case below.
+  * grouped-query attention: "FlashAttention 4: Atenção Mais Rápida …",
+    section "Compatibilidade e status atual", describes GQA as several query
+    heads sharing one key/value projection.  With H query heads and H_kv key/
+    value heads (H a multiple of H_kv), query head h reads key/value head
+    h // (H / H_kv): consecutive query heads share one, H_kv = 1 being MQA.
   * a row with no visible key has O = 0 and LSE = −inf.
   * the scale is an argument; the pages pass 1/√head_dim.
 
@@ -56,16 +64,17 @@ def to_f64(x) -> np.ndarray:
     return np.asarray(x, dtype=np.float64)
 
 
-def visible_mask(rows: np.ndarray, Sk: int, causal: bool) -> np.ndarray:
+def visible_mask(rows: np.ndarray, Sk: int, causal: bool, causal_offset: int = 0) -> np.ndarray:
     """Boolean [len(rows), Sk]: True where key j is visible to query row i.
 
-    Visible set: 0 ≤ j < Sk, and j ≤ i when causal (top-left alignment).
+    Visible set: 0 ≤ j < Sk, and j ≤ i + causal_offset when causal (offset 0 =
+    top-left alignment, Sk − Sq = bottom-right).
     """
     rows = np.asarray(rows, dtype=np.int64)
     keys = np.arange(Sk, dtype=np.int64)
     if not causal:
         return np.ones((rows.shape[0], Sk), dtype=bool)
-    return keys[None, :] <= rows[:, None]
+    return keys[None, :] <= rows[:, None] + causal_offset
 
 
 def head_scores(q: np.ndarray, k: np.ndarray, scale: float) -> np.ndarray:
@@ -91,11 +100,12 @@ def head_probabilities(s: np.ndarray, mask: np.ndarray):
     return P, M, L
 
 
-def attention_head(q, k, v, scale: float, causal: bool, rows=None):
+def attention_head(q, k, v, scale: float, causal: bool, rows=None, causal_offset: int = 0):
     """Exact attention for one head, float64.
 
     q: [Sq, d], k: [Sk, d], v: [Sk, d].  ``rows`` selects query rows (default
-    all).  Returns (O [n, d], LSE [n]) for the selected rows.
+    all); causal masks see keys j ≤ i + causal_offset.  Returns (O [n, d],
+    LSE [n]) for the selected rows.
     """
     q = np.asarray(q, dtype=np.float64)
     k = np.asarray(k, dtype=np.float64)
@@ -106,43 +116,57 @@ def attention_head(q, k, v, scale: float, causal: bool, rows=None):
     LSE = np.full((rows.shape[0],), -np.inf, dtype=np.float64)
     for c0 in range(0, rows.shape[0], ROW_CHUNK):
         r = rows[c0:c0 + ROW_CHUNK]
-        # Causal rows never see keys beyond their own index: only the needed
-        # key prefix is multiplied (same result, less work).
-        kmax = Sk if not causal else int(min(Sk, r.max() + 1))
+        # Causal rows never see keys beyond their own index (+ offset): only
+        # the needed key prefix is multiplied (same result, less work).
+        kmax = Sk if not causal else int(min(Sk, r.max() + 1 + causal_offset))
+        if kmax <= 0:
+            continue  # no row of the chunk sees a key: O = 0, LSE = −inf
         s = head_scores(q[r], k[:kmax], scale)
-        P, M, L = head_probabilities(s, visible_mask(r, kmax, causal))
+        P, M, L = head_probabilities(s, visible_mask(r, kmax, causal, causal_offset))
         O[c0:c0 + r.shape[0]] = P @ v[:kmax]
         with np.errstate(divide="ignore"):
             LSE[c0:c0 + r.shape[0]] = np.where(np.isfinite(M), M + np.log(np.where(L > 0, L, 1.0)), -np.inf)
     return O, LSE
 
 
-def attention_forward(q, k, v, scale: float, causal: bool):
+def kv_head(h: int, H: int, H_kv: int) -> int:
+    """Key/value head read by query head h (grouped-query attention)."""
+    if H_kv < 1 or H % H_kv != 0:
+        raise ValueError(f"H = {H} is not a multiple of H_kv = {H_kv}")
+    return h // (H // H_kv)
+
+
+def attention_forward(q, k, v, scale: float, causal: bool, causal_offset: int = 0):
     """Exact attention over all batches and heads.
 
-    q: [B, Sq, H, d]; k, v: [B, Sk, H, d] (torch tensors or arrays).
+    q: [B, Sq, H, d]; k, v: [B, Sk, H_kv, d] (torch tensors or arrays), H a
+    multiple of H_kv.  Causal masks see keys j ≤ i + causal_offset.
     Returns O [B, Sq, H, d] float64 and LSE [B, H, Sq] float64.
     """
     q, k, v = to_f64(q), to_f64(k), to_f64(v)
     B, Sq, H, d = q.shape
+    H_kv = k.shape[2]
     O = np.zeros((B, Sq, H, v.shape[3]), dtype=np.float64)
     LSE = np.zeros((B, H, Sq), dtype=np.float64)
     for b in range(B):
         for h in range(H):
-            O[b, :, h, :], LSE[b, h, :] = attention_head(q[b, :, h, :], k[b, :, h, :], v[b, :, h, :], scale, causal)
+            g = kv_head(h, H, H_kv)
+            O[b, :, h, :], LSE[b, h, :] = attention_head(q[b, :, h, :], k[b, :, g, :], v[b, :, g, :], scale, causal,
+                                                         causal_offset=causal_offset)
     return O, LSE
 
 
-def attention_rows(q, k, v, scale: float, causal: bool, b: int, h: int, rows):
+def attention_rows(q, k, v, scale: float, causal: bool, b: int, h: int, rows, causal_offset: int = 0):
     """Exact attention for selected query rows of one (batch, head).
 
-    Used to check full-size GPU outputs on a sample of rows.
-    Returns (O [n, d], LSE [n]) float64.
+    Used to check full-size GPU outputs on a sample of rows; K/V may have fewer
+    heads than Q (grouped-query attention).  Returns (O [n, d], LSE [n]) float64.
     """
+    g = kv_head(h, q.shape[2], k.shape[2])
     qh = to_f64(q[b, :, h, :]) if not isinstance(q, np.ndarray) else q[b, :, h, :]
-    kh = to_f64(k[b, :, h, :]) if not isinstance(k, np.ndarray) else k[b, :, h, :]
-    vh = to_f64(v[b, :, h, :]) if not isinstance(v, np.ndarray) else v[b, :, h, :]
-    return attention_head(qh, kh, vh, scale, causal, rows=rows)
+    kh = to_f64(k[b, :, g, :]) if not isinstance(k, np.ndarray) else k[b, :, g, :]
+    vh = to_f64(v[b, :, g, :]) if not isinstance(v, np.ndarray) else v[b, :, g, :]
+    return attention_head(qh, kh, vh, scale, causal, rows=rows, causal_offset=causal_offset)
 
 
 def combine_partials(O_parts, LSE_parts):

@@ -53,12 +53,13 @@ def rand_head(seed, Sq, Sk, d, sigma=1.0):
 
 
 # ---------------------------------------------------------------- brute force
-def brute_force_head(q, k, v, scale, causal):
-    """Pure-Python attention for one head (lists of floats, math.fsum)."""
+def brute_force_head(q, k, v, scale, causal, offset=0):
+    """Pure-Python attention for one head (lists of floats, math.fsum); causal
+    rows see keys j ≤ i + offset."""
     Sq, Sk, d = len(q), len(k), len(v[0])
     O, LSE = [], []
     for i in range(Sq):
-        vis = [j for j in range(Sk) if (not causal) or j <= i]
+        vis = [j for j in range(Sk) if (not causal) or j <= i + offset]
         if not vis:
             O.append([0.0] * d)
             LSE.append(-math.inf)
@@ -299,6 +300,71 @@ def brute_force_masked(s, mask, v):
         L[i] = m + math.log(math.fsum(e))
         O[i] = (e @ v[vis]) / math.fsum(e)
     return O, L
+
+
+# ------------------------------------------------ grouped heads, causal offset
+def pin_gqa_brute_force_and_repeat():
+    """Grouped-query attention: query head h reads key/value head h // (H/H_kv).
+    Checked per head against brute force, and against ordinary attention on
+    K/V whose heads are repeated H/H_kv times in place (the usual way a grouped
+    model is run on a kernel without grouping)."""
+    r = _rng(1400)
+    B, S, Sk, H, H_kv, d = 2, 9, 11, 6, 2, 8
+    q = _bf16_like(r.standard_normal((B, S, H, d)))
+    k = _bf16_like(r.standard_normal((B, Sk, H_kv, d)))
+    v = _bf16_like(r.standard_normal((B, Sk, H_kv, d)))
+    for causal in (False, True):
+        O, L = oracle.attention_forward(q, k, v, 0.3, causal)
+        for b in range(B):
+            for h in range(H):
+                g = h // (H // H_kv)
+                Ob, Lb = brute_force_head(q[b, :, h].tolist(), k[b, :, g].tolist(), v[b, :, g].tolist(), 0.3, causal)
+                assert np.max(np.abs(O[b, :, h] - Ob)) <= TOL and np.max(np.abs(L[b, h] - Lb)) <= TOL
+        Or, Lr = oracle.attention_forward(q, np.repeat(k, H // H_kv, axis=2), np.repeat(v, H // H_kv, axis=2), 0.3,
+                                          causal)
+        assert np.max(np.abs(O - Or)) <= TOL and np.max(np.abs(L - Lr)) <= TOL
+    # MQA (one key/value head): every query head reads it.
+    O1, L1 = oracle.attention_forward(q, k[:, :, :1], v[:, :, :1], 0.3, False)
+    for h in range(H):
+        Ob, Lb = brute_force_head(q[0, :, h].tolist(), k[0, :, 0].tolist(), v[0, :, 0].tolist(), 0.3, False)
+        assert np.max(np.abs(O1[0, :, h] - Ob)) <= TOL and np.max(np.abs(L1[0, h] - Lb)) <= TOL
+
+
+def pin_causal_bottom_right():
+    """Bottom-right alignment (key j visible to row i iff j ≤ i + Sk − Sq):
+    brute force on tiny shapes, rows without a visible key (Sq > Sk) give
+    O = 0 and LSE = −inf, and for Sq ≤ Sk the result equals the last Sq rows of
+    the top-left causal result with Q padded in front to Sk rows."""
+    for n, (Sq, Sk) in enumerate([(3, 7), (7, 3), (5, 5), (1, 9), (9, 1)]):
+        q, k, v = rand_head(1500 + n, Sq, Sk, 8, sigma=2.0)
+        off = Sk - Sq
+        O, L = oracle.attention_head(q, k, v, 0.4, True, causal_offset=off)
+        Ob, Lb = brute_force_head(q.tolist(), k.tolist(), v.tolist(), 0.4, True, offset=off)
+        fin = np.isfinite(Lb)
+        assert np.array_equal(fin, np.isfinite(L)), (Sq, Sk)
+        assert np.array_equal(fin, np.arange(Sq) >= Sq - Sk) if Sq > Sk else fin.all()
+        assert np.max(np.abs(O - Ob)) <= TOL and np.max(np.abs(L[fin] - Lb[fin])) <= TOL
+        assert np.all(O[~fin] == 0.0)
+    q, k, v = rand_head(1510, 40, 100, 16)
+    O, L = oracle.attention_head(q, k, v, 0.25, True, causal_offset=60)
+    qp = np.concatenate([np.zeros((60, 16)), q])
+    Op, Lp = oracle.attention_head(qp, k, v, 0.25, True)
+    assert np.max(np.abs(O - Op[60:])) <= TOL and np.max(np.abs(L - Lp[60:])) <= TOL
+
+
+def pin_rows_grouped_offset():
+    """attention_rows agrees with attention_forward on sampled rows, with
+    grouped heads and a causal offset."""
+    r = _rng(1600)
+    B, Sq, Sk, H, H_kv, d = 1, 50, 70, 4, 2, 16
+    q = _bf16_like(r.standard_normal((B, Sq, H, d)))
+    k = _bf16_like(r.standard_normal((B, Sk, H_kv, d)))
+    v = _bf16_like(r.standard_normal((B, Sk, H_kv, d)))
+    O, L = oracle.attention_forward(q, k, v, 0.25, True, causal_offset=Sk - Sq)
+    rows = np.array([0, 7, 31, 49])
+    for h in range(H):
+        Os, Ls = oracle.attention_rows(q, k, v, 0.25, True, 0, h, rows, causal_offset=Sk - Sq)
+        assert np.max(np.abs(O[0, rows, h] - Os)) <= TOL and np.max(np.abs(L[0, h, rows] - Ls)) <= TOL
 
 
 ALL_PINS = [v for k_, v in sorted(globals().items()) if k_.startswith("pin_") and callable(v)]

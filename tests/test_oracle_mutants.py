@@ -29,9 +29,16 @@ MUTANTS = {
     "denominator_counts_masked": ("    L = E.sum(axis=1)", "    L = np.exp(s - shift[:, None]).sum(axis=1)"),
     "unnormalised_p": ("E / np.where(finite, L, 1.0)[:, None]", "E"),
     "double_shift": ("np.exp(masked - shift[:, None])", "np.exp(masked - 2 * shift[:, None])"),
-    "causal_prefix_short": ("int(min(Sk, r.max() + 1))", "int(min(Sk, r.max()))"),
-    "forward_swaps_kv": ("attention_head(q[b, :, h, :], k[b, :, h, :], v[b, :, h, :]",
-                         "attention_head(q[b, :, h, :], v[b, :, h, :], k[b, :, h, :]"),
+    "causal_prefix_short": ("int(min(Sk, r.max() + 1 + causal_offset))", "int(min(Sk, r.max() + causal_offset))"),
+    "forward_swaps_kv": ("attention_head(q[b, :, h, :], k[b, :, g, :], v[b, :, g, :]",
+                         "attention_head(q[b, :, h, :], v[b, :, g, :], k[b, :, g, :]"),
+    "gqa_interleaved_heads": ("return h // (H // H_kv)", "return h % H_kv"),
+    "gqa_ignores_grouping": ("            g = kv_head(h, H, H_kv)\n", "            g = min(h, H_kv - 1)\n"),
+    "offset_ignored": ("keys[None, :] <= rows[:, None] + causal_offset", "keys[None, :] <= rows[:, None]"),
+    "offset_negated": ("keys[None, :] <= rows[:, None] + causal_offset", "keys[None, :] <= rows[:, None] - causal_offset"),
+    "forward_drops_offset": ("                                                         causal_offset=causal_offset)",
+                             "                                                         causal_offset=0)"),
+    "rows_drop_offset": ("rows=rows, causal_offset=causal_offset)", "rows=rows)"),
     "forward_lse_transposed_heads": ("LSE[b, h, :] = attention_head", "LSE[b, (h + 1) % H, :] = attention_head"),
     "combine_plain_mean": ("O = (w[..., None] * Os).sum(axis=0)", "O = Os.mean(axis=0)"),
     "combine_lse_max_only": ("LSE = np.where(finite, shift + np.log(np.where(tot > 0, tot, 1.0)), -np.inf)",
@@ -52,7 +59,7 @@ def _load_mutant(old, new):
 def test_mutant_is_caught(name, monkeypatch):
     mod = _load_mutant(*MUTANTS[name])
     for fn in ("attention_forward", "attention_head", "attention_rows", "head_probabilities",
-               "head_scores", "visible_mask", "combine_partials"):
+               "head_scores", "kv_head", "visible_mask", "combine_partials"):
         monkeypatch.setattr(oracle, fn, getattr(mod, fn))
     caught = []
     for pin in oracle_pins.ALL_PINS:
