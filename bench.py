@@ -229,6 +229,10 @@ def main():
     ap.add_argument("--poly-mask", type=lambda x: int(x, 0), default=0, help="override the exp2 split (tuning)")
     ap.add_argument("--tau", type=float, default=0.0, help="override the rescale threshold (tuning; 0 = default)")
     ap.add_argument("--diag", action="store_true", help="report the rescale rate of one extra launch")
+    ap.add_argument("--kv-heads", type=int, default=0,
+                    help="grouped-query variant of the workload: K/V heads (H must be a multiple); 0 = H")
+    ap.add_argument("--causal-align", choices=["top-left", "bottom-right"], default="top-left",
+                    help="causal alignment when Sq != Sk (only the square workloads ship, where both agree)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -236,6 +240,15 @@ def main():
     from exact_attention_63_gb300 import inputs
 
     w = inputs.WORKLOADS[args.config]
+    if args.kv_heads or args.causal_align != "top-left":
+        import dataclasses
+
+        if args.kv_heads and w.H % args.kv_heads:
+            ap.error(f"H = {w.H} is not a multiple of --kv-heads {args.kv_heads}")
+        tag = (f"_hkv{args.kv_heads}" if args.kv_heads else "") + \
+            ("_br" if args.causal_align == "bottom-right" else "")
+        w = dataclasses.replace(w, name=w.name + tag, H_kv=args.kv_heads, causal_align=args.causal_align)
+        args.no_e2e = True  # the host-buffer entry point takes dense multi-head tensors only
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
@@ -272,7 +285,8 @@ def main():
     stream = torch.cuda.current_stream()
 
     def step():
-        attn.attn_fwd(qd, kd, vd, causal=w.causal, scale=w.scale, out=od, lse=ld, options=opts)
+        attn.attn_fwd(qd, kd, vd, causal=w.causal, scale=w.scale, out=od, lse=ld, options=opts,
+                      causal_align=w.causal_align)
 
     for _ in range(args.warmup):
         flush.zero_()
@@ -358,8 +372,8 @@ def main():
         "vs_baseline": None,
         "dtype": "bf16",
         "data": "synthetic",
-        "config": {"workload": w.name, "B": w.B, "H": w.H, "Sq": w.Sq, "Sk": w.Sk, "d": w.d,
-                   "causal": w.causal, "sigma_qk": w.sigma_qk, "seed": w.seed,
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "H_kv": w.kv_heads, "Sq": w.Sq, "Sk": w.Sk, "d": w.d,
+                   "causal": w.causal, "causal_align": w.causal_align, "sigma_qk": w.sigma_qk, "seed": w.seed,
                    "l2": "flushed between timed steps (256 MiB write)",
                    "parallelism": f"replicas{world}" if world > 1 else "single"},
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",

@@ -21,12 +21,14 @@ ATTN_OK = 0
 ERRORS = {
     -1: "ATTN_ERR_NULL", -2: "ATTN_ERR_SHAPE", -3: "ATTN_ERR_HEAD_DIM", -4: "ATTN_ERR_SCALE",
     -5: "ATTN_ERR_ALIGN", -6: "ATTN_ERR_ARCH", -7: "ATTN_ERR_LAUNCH", -8: "ATTN_ERR_TIMEOUT",
-    -9: "ATTN_ERR_OPTION", -10: "ATTN_ERR_WORKSPACE", -11: "ATTN_ERR_STATIC_LIMIT",
+    -9: "ATTN_ERR_OPTION", -10: "ATTN_ERR_WORKSPACE", -11: "ATTN_ERR_STATIC_LIMIT", -12: "ATTN_ERR_LAYOUT",
 }
 
 # Every symbol the header declares (checked by the CPU test-suite).
 EXPORTS = ["attn_fwd", "attn_fwd_ex", "attn_fwd_host", "attn_fwd_host_workspace_size", "attn_get_status",
-           "attn_strerror", "attn_last_cuda_error", "attn_version", "attn_fwd_host_static"]
+           "attn_strerror", "attn_last_cuda_error", "attn_version", "attn_fwd_host_static", "attn_fwd_layout"]
+
+CAUSAL_ALIGN = {"top-left": 0, "bottom-right": 1}
 
 # Size of the library's fixed device staging area used by attn_fwd_host_static.
 STATIC_WORKSPACE_BYTES = 32 << 20
@@ -45,6 +47,25 @@ class Options(ctypes.Structure):
                 ("test_flags", ctypes.c_uint)]
 
 
+class Layout(ctypes.Structure):
+    """Mirror of ``attn_layout``."""
+    _fields_ = [("struct_size", ctypes.c_size_t), ("num_kv_heads", ctypes.c_int), ("causal_align", ctypes.c_int),
+                ("q_strides", ctypes.c_longlong * 3), ("k_strides", ctypes.c_longlong * 3),
+                ("v_strides", ctypes.c_longlong * 3), ("o_strides", ctypes.c_longlong * 3)]
+
+
+def make_layout(num_kv_heads: int = 0, causal_align: int = 0, q_strides=(0, 0, 0), k_strides=(0, 0, 0),
+                v_strides=(0, 0, 0), o_strides=(0, 0, 0)) -> Layout:
+    lay = Layout()
+    lay.struct_size = ctypes.sizeof(Layout)
+    lay.num_kv_heads = num_kv_heads
+    lay.causal_align = causal_align
+    for name, st in (("q_strides", q_strides), ("k_strides", k_strides), ("v_strides", v_strides),
+                     ("o_strides", o_strides)):
+        getattr(lay, name)[:] = [int(x) for x in st]
+    return lay
+
+
 def lib():
     """Load the shared library (raises if it is missing)."""
     global _lib
@@ -58,6 +79,9 @@ def lib():
     L.attn_fwd.restype = i
     L.attn_fwd_ex.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, ctypes.POINTER(Options), vp]
     L.attn_fwd_ex.restype = i
+    L.attn_fwd_layout.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, ctypes.POINTER(Layout),
+                                  ctypes.POINTER(Options), vp]
+    L.attn_fwd_layout.restype = i
     L.attn_fwd_host.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp, sz, vp]
     L.attn_fwd_host.restype = i
     L.attn_fwd_host_workspace_size.argtypes = [i, i, i, i, i]
@@ -90,40 +114,70 @@ def _stream_handle(stream):
     return ctypes.c_void_p(stream.cuda_stream)
 
 
+def _check_tensor(name, t):
+    if t.dtype != torch.bfloat16 or not t.is_cuda or t.dim() != 4 or t.stride(3) != 1:
+        raise ValueError(f"{name} must be a 4-D bf16 CUDA tensor (batch, seq, heads, head_dim) "
+                         "with a contiguous head_dim")
+
+
 def _check_inputs(q, k, v):
     for name, t in (("q", q), ("k", k), ("v", v)):
-        if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous() or t.dim() != 4:
-            raise ValueError(f"{name} must be a contiguous 4-D bf16 CUDA tensor (batch, seq, heads, head_dim)")
+        _check_tensor(name, t)
     B, Sq, H, d = q.shape
-    if k.shape != v.shape or k.shape[0] != B or k.shape[2] != H or k.shape[3] != d:
-        raise ValueError(f"shape mismatch: q {tuple(q.shape)}, k {tuple(k.shape)}, v {tuple(v.shape)}")
+    if k.shape != v.shape or k.shape[0] != B or k.shape[3] != d or k.shape[2] < 1 or H % k.shape[2] != 0:
+        raise ValueError(f"shape mismatch: q {tuple(q.shape)}, k {tuple(k.shape)}, v {tuple(v.shape)} "
+                         "(k and v: (batch, Sk, H_kv, head_dim) with H a multiple of H_kv)")
     return B, H, Sq, k.shape[1], d
 
 
+def _strides(t):
+    return (t.stride(0), t.stride(1), t.stride(2))
+
+
 def attn_fwd(q, k, v, causal: bool = False, scale: float | None = None, out=None, lse=None, stream=None,
-             options: Options | None = None):
-    """Exact attention forward.  Returns (o [B,Sq,H,d] bf16, lse [B,H,Sq] fp32)."""
+             options: Options | None = None, causal_align: str = "top-left"):
+    """Exact attention forward.  Returns (o [B,Sq,H,d] bf16, lse [B,H,Sq] fp32).
+
+    k and v may have fewer heads than q (grouped-query attention: query head h
+    reads key/value head h // (H / H_kv)); q, k, v and out may be strided views
+    whose head_dim is contiguous (strides are passed to the library, which
+    needs them to be multiples of 8 elements).  ``causal_align`` is
+    "top-left" (key j visible to row i iff j <= i) or "bottom-right"
+    (iff j <= i + Sk - Sq).
+    """
     B, H, Sq, Sk, d = _check_inputs(q, k, v)
+    if causal_align not in CAUSAL_ALIGN:
+        raise ValueError(f"causal_align must be one of {sorted(CAUSAL_ALIGN)}")
     if scale is None:
         scale = 1.0 / math.sqrt(d)
     if out is None:
-        out = torch.empty_like(q)
+        out = torch.empty((B, Sq, H, d), dtype=torch.bfloat16, device=q.device)
     if lse is None:
         lse = torch.empty((B, H, Sq), dtype=torch.float32, device=q.device)
-    if out.shape != q.shape or out.dtype != torch.bfloat16 or not out.is_contiguous():
-        raise ValueError("out must be a contiguous bf16 tensor shaped like q")
+    _check_tensor("out", out)
+    if tuple(out.shape) != (B, Sq, H, d):
+        raise ValueError("out must be shaped like q")
     if lse.shape != (B, H, Sq) or lse.dtype != torch.float32 or not lse.is_contiguous():
         raise ValueError("lse must be a contiguous fp32 tensor of shape (B, H, Sq)")
+    dense = all(t.is_contiguous() for t in (q, k, v, out))
+    plain = dense and k.shape[2] == H and (not causal or causal_align == "top-left")
     L = lib()
     with torch.cuda.device(q.device):
         s = _stream_handle(stream)
-        if options is None:
+        if options is not None:
+            options.struct_size = ctypes.sizeof(Options)
+        if plain and options is None:
             rc = L.attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
                             B, H, Sq, Sk, d, float(scale), int(bool(causal)), s)
-        else:
-            options.struct_size = ctypes.sizeof(Options)
+        elif plain:
             rc = L.attn_fwd_ex(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
                                B, H, Sq, Sk, d, float(scale), int(bool(causal)), ctypes.byref(options), s)
+        else:
+            lay = make_layout(k.shape[2], CAUSAL_ALIGN[causal_align], _strides(q), _strides(k), _strides(v),
+                              _strides(out))
+            rc = L.attn_fwd_layout(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
+                                   B, H, Sq, Sk, d, float(scale), int(bool(causal)), ctypes.byref(lay),
+                                   ctypes.byref(options) if options is not None else None, s)
     _check(rc)
     return out, lse
 
@@ -178,6 +232,13 @@ def attn_fwd_host_static(q_h, k_h, v_h, o_h, lse_h, causal: bool, scale: float, 
 def get_status(stream=None) -> int:
     """Synchronise the stream and return/clear the device status (0 = ok)."""
     return int(lib().attn_get_status(_stream_handle(stream)))
+
+
+def raw_fwd_layout(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, B, H, Sq, Sk, d, scale, causal, layout, stream_ptr=0) -> int:
+    """Direct attn_fwd_layout call with integer pointers; returns the status code (tests)."""
+    return int(lib().attn_fwd_layout(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, B, H, Sq, Sk, d, float(scale), int(causal),
+                                     None if layout is None else ctypes.byref(layout), None,
+                                     ctypes.c_void_p(stream_ptr)))
 
 
 def raw_fwd(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, B, H, Sq, Sk, d, scale, causal, stream_ptr=0) -> int:

@@ -41,9 +41,10 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
   return fn;
 }
 
-// 4-D map over a dense bf16 [B, S, H, d] tensor, dims innermost first
-// (d, H, S, B); box (64, 1, 128, 1) = one 128-row × 128-byte slab.
-int encode_bshd(CUtensorMap* m, const void* ptr, int B, int S, int H, int d) {
+// 4-D map over a bf16 [B, S, H, d] tensor with element strides st = (batch,
+// seq, head) and contiguous d, dims innermost first (d, H, S, B); box
+// (64, 1, 128, 1) = one 128-row × 128-byte slab.
+int encode_bshd(CUtensorMap* m, const void* ptr, int B, int S, int H, int d, const long long st[3]) {
   auto enc = get_encode_fn();
   if (enc == nullptr) {
     std::snprintf(t_last_error, sizeof(t_last_error), "cuTensorMapEncodeTiled unavailable");
@@ -51,8 +52,8 @@ int encode_bshd(CUtensorMap* m, const void* ptr, int B, int S, int H, int d) {
   }
   const cuuint64_t dims[4] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(S),
                               static_cast<cuuint64_t>(B)};
-  const cuuint64_t strides[3] = {static_cast<cuuint64_t>(d) * 2, static_cast<cuuint64_t>(H) * d * 2,
-                                 static_cast<cuuint64_t>(S) * H * d * 2};
+  const cuuint64_t strides[3] = {static_cast<cuuint64_t>(st[2]) * 2, static_cast<cuuint64_t>(st[1]) * 2,
+                                 static_cast<cuuint64_t>(st[0]) * 2};
   const cuuint32_t box[4] = {64, 1, 128, 1};
   const cuuint32_t estr[4] = {1, 1, 1, 1};
   CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(ptr), dims, strides, box, estr,
@@ -105,6 +106,39 @@ int current_device(int* dev_out) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// Rows that see no key (bottom-right causal alignment with Sq > Sk): O = 0,
+// LSE = −inf.  One thread per (batch, head, row); rows are 16-byte aligned
+// (strides are multiples of 8 elements).
+__global__ void fill_unseen_rows(uint16_t* o, long long sb, long long ss, long long sh, float* lse, int lse_pitch,
+                                 int B, int H, int rows, int d) {
+  const long long n = static_cast<long long>(B) * H * rows;
+  for (long long t = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; t < n;
+       t += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const int i = static_cast<int>(t % rows);
+    const int h = static_cast<int>((t / rows) % H);
+    const int b = static_cast<int>(t / (static_cast<long long>(rows) * H));
+    uint4* row = reinterpret_cast<uint4*>(o + b * sb + i * ss + h * sh);
+    for (int c = 0; c < d / 8; ++c) row[c] = make_uint4(0u, 0u, 0u, 0u);
+    lse[(static_cast<long long>(b) * H + h) * lse_pitch + i] = -INFINITY;
+  }
+}
+
+// A layout's strides: all zero → dense; else each a positive multiple of 8
+// elements below 2^38 (TMA: 16-byte multiples, strides below 2^40 bytes).
+bool resolve_strides(const long long in[3], long long dense0, long long dense1, long long dense2, long long out[3]) {
+  if (in[0] == 0 && in[1] == 0 && in[2] == 0) {
+    out[0] = dense0;
+    out[1] = dense1;
+    out[2] = dense2;
+    return true;
+  }
+  for (int i = 0; i < 3; ++i) {
+    if (in[i] <= 0 || (in[i] & 7) != 0 || in[i] >= (1LL << 38)) return false;
+    out[i] = in[i];
+  }
+  return true;
+}
+
 int check_args(const void* q, const void* k, const void* v, const void* o, const void* lse, int B, int H, int Sq,
                int Sk, int d, float scale) {
   if (q == nullptr || k == nullptr || v == nullptr || o == nullptr || lse == nullptr) return ATTN_ERR_NULL;
@@ -150,16 +184,47 @@ const char* attn_strerror(int status) {
     case ATTN_ERR_OPTION: return "an attn_options field is out of range";
     case ATTN_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
     case ATTN_ERR_STATIC_LIMIT: return "problem larger than the static workspace of attn_fwd_host_static";
+    case ATTN_ERR_LAYOUT:
+      return "invalid attn_layout (H not a multiple of num_kv_heads, a stride not a positive multiple of 8, "
+             "or an unknown causal_align)";
     default: return "unknown status";
   }
 }
 
 const char* attn_last_cuda_error(void) { return t_last_error; }
 
-int attn_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Sq, int Sk, int d,
-                float scale, int causal, const attn_options* opts, cudaStream_t stream) {
+int attn_fwd_layout(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Sq, int Sk,
+                    int d, float scale, int causal, const attn_layout* layout, const attn_options* opts,
+                    cudaStream_t stream) {
   int rc = check_args(q, k, v, o, lse, B, H, Sq, Sk, d, scale);
   if (rc != ATTN_OK) return rc;
+  int H_kv = H;
+  bool bottom_right = false;
+  long long qs[3], ks[3], vs[3], os[3];
+  {
+    static const long long zero[3] = {0, 0, 0};
+    const long long* qi = zero;
+    const long long* ki = zero;
+    const long long* vi = zero;
+    const long long* oi = zero;
+    if (layout != nullptr) {
+      if (layout->struct_size < sizeof(attn_layout)) return ATTN_ERR_LAYOUT;
+      if (layout->num_kv_heads < 0) return ATTN_ERR_LAYOUT;
+      if (layout->num_kv_heads > 0) H_kv = layout->num_kv_heads;
+      if (H % H_kv != 0) return ATTN_ERR_LAYOUT;
+      if (layout->causal_align != ATTN_CAUSAL_TOP_LEFT && layout->causal_align != ATTN_CAUSAL_BOTTOM_RIGHT)
+        return ATTN_ERR_LAYOUT;
+      bottom_right = causal && layout->causal_align == ATTN_CAUSAL_BOTTOM_RIGHT;
+      qi = layout->q_strides;
+      ki = layout->k_strides;
+      vi = layout->v_strides;
+      oi = layout->o_strides;
+    }
+    const long long hd = static_cast<long long>(H) * d, kd = static_cast<long long>(H_kv) * d;
+    if (!resolve_strides(qi, Sq * hd, hd, d, qs) || !resolve_strides(ki, Sk * kd, kd, d, ks) ||
+        !resolve_strides(vi, Sk * kd, kd, d, vs) || !resolve_strides(oi, Sq * hd, hd, d, os))
+      return ATTN_ERR_LAYOUT;
+  }
   float tau = kDefaultTau;
   uint32_t poly = (d == 64) ? kDefaultPolyMaskD64 : kDefaultPolyMaskD128;
   unsigned long long* counters = nullptr;
@@ -183,12 +248,34 @@ int attn_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse
   rc = current_device(&dev);
   if (rc != ATTN_OK) return rc;
 
+  // Causal offset: key j is visible to row i iff j ≤ i + coff.  Bottom-right
+  // alignment with Sq > Sk leaves the first Sq − Sk rows without a key: they
+  // are written by fill_unseen_rows, and the kernel runs on the remaining
+  // rows, a problem with Sq = Sk and offset 0 (every tile then sees a key).
+  const int lse_pitch = Sq;
+  int coff = bottom_right ? Sk - Sq : 0;
+  if (coff < 0) {
+    const int unseen = -coff;
+    const long long n = static_cast<long long>(B) * H * unseen;
+    const int threads = 256;
+    const int blocks = static_cast<int>(n / threads + 1 < 4096 ? n / threads + 1 : 4096);
+    fill_unseen_rows<<<blocks, threads, 0, stream>>>(static_cast<uint16_t*>(o), os[0], os[1], os[2], lse, lse_pitch,
+                                                      B, H, unseen, d);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return fail_cuda(e, "row fill launch");
+    q = static_cast<const uint16_t*>(q) + static_cast<long long>(unseen) * qs[1];
+    o = static_cast<uint16_t*>(o) + static_cast<long long>(unseen) * os[1];
+    lse += unseen;
+    Sq = Sk;
+    coff = 0;
+  }
+
   attn::LaunchArgs a;
   std::memset(&a, 0, sizeof(a));
-  if ((rc = encode_bshd(&a.q, q, B, Sq, H, d)) != ATTN_OK) return rc;
-  if ((rc = encode_bshd(&a.k, k, B, Sk, H, d)) != ATTN_OK) return rc;
-  if ((rc = encode_bshd(&a.v, v, B, Sk, H, d)) != ATTN_OK) return rc;
-  if ((rc = encode_bshd(&a.o, o, B, Sq, H, d)) != ATTN_OK) return rc;
+  if ((rc = encode_bshd(&a.q, q, B, Sq, H, d, qs)) != ATTN_OK) return rc;
+  if ((rc = encode_bshd(&a.k, k, B, Sk, H_kv, d, ks)) != ATTN_OK) return rc;
+  if ((rc = encode_bshd(&a.v, v, B, Sk, H_kv, d, vs)) != ATTN_OK) return rc;
+  if ((rc = encode_bshd(&a.o, o, B, Sq, H, d, os)) != ATTN_OK) return rc;
   const int n_qt = (Sq + 127) / 128;
   a.p.o = o;
   a.p.lse = lse;
@@ -198,6 +285,9 @@ int attn_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse
   a.p.H = H;
   a.p.Sq = Sq;
   a.p.Sk = Sk;
+  a.p.group = H / H_kv;
+  a.p.coff = coff;
+  a.p.lse_pitch = lse_pitch;
   a.p.n_qt = n_qt;
   a.p.n_tiles = n_qt * B * H;
   a.p.scale_log2 = scale * 1.4426950408889634f;
@@ -213,6 +303,11 @@ int attn_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse
   else e = causal ? attn::launch_fwd_d128_causal(a) : attn::launch_fwd_d128(a);
   if (e != cudaSuccess) return fail_cuda(e, "attention kernel launch");
   return ATTN_OK;
+}
+
+int attn_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Sq, int Sk, int d,
+                float scale, int causal, const attn_options* opts, cudaStream_t stream) {
+  return attn_fwd_layout(q, k, v, o, lse, B, H, Sq, Sk, d, scale, causal, nullptr, opts, stream);
 }
 
 int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Sq, int Sk, int d,

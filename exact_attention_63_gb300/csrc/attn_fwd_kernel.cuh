@@ -100,6 +100,9 @@ struct FwdParams {
   unsigned int* status;          // device status word
   unsigned long long* counters;  // optional diagnostics (may be null)
   int B, H, Sq, Sk;
+  int group;                     // query heads per key/value head (H / H_kv)
+  int coff;                      // causal: key j visible to row i iff j ≤ i + coff (≥ 0)
+  int lse_pitch;                 // LSE elements between consecutive (batch, head) rows
   int n_qt;                      // ceil(Sq / 128)
   int n_tiles;                   // n_qt · B · H
   float scale_log2;              // scale · log2(e)
@@ -187,7 +190,8 @@ __device__ __forceinline__ bool wait_bar_cold(uint32_t bar, uint32_t parity, con
 
 // One work tile: 128 query rows of one (batch, head).
 struct Tile {
-  int b, h, q0, nb;  // nb = key blocks visible to the tile
+  int b, h, q0, nb;  // nb = key blocks visible to the tile (≥ 1)
+  int kvh;           // key/value head read by query head h
 };
 
 // Tile order.  Causal: heaviest query tiles first (longest-processing-time
@@ -208,8 +212,11 @@ __device__ __forceinline__ Tile tile_info(int idx, const FwdParams& p) {
   t.b = bh / p.H;
   t.h = bh % p.H;
   t.q0 = qt * kBM;
+  t.kvh = t.h / p.group;
   const int nk = (p.Sk + kBN - 1) / kBN;
-  t.nb = CAUSAL ? min(nk, (min(t.q0 + kBM, p.Sq) - 1) / kBN + 1) : nk;
+  // Causal: the tile's last row sees keys up to row + coff (coff ≥ 0, so every
+  // tile sees at least key 0).
+  t.nb = CAUSAL ? min(nk, (min(t.q0 + kBM, p.Sq) - 1 + p.coff) / kBN + 1) : nk;
   return t;
 }
 
@@ -312,7 +319,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!wait_bar(bar_kv_empty(slot), ((issued / L::kStages) & 1) ^ 1u, wc)) return false;
         mbar_arrive_expect_tx(bar_kv_full(slot), L::kTileBytes);
         for (int s = 0; s < L::kSlabs; ++s)
-          tma_load_4d(sRing + slot * L::kTileBytes + s * L::kSlabBytes, m, 64 * s, T.h, j * kBN, T.b,
+          tma_load_4d(sRing + slot * L::kTileBytes + s * L::kSlabBytes, m, 64 * s, T.kvh, j * kBN, T.b,
                       bar_kv_full(slot));
         ++issued;
         return true;
@@ -549,7 +556,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int c = 0; c < kHalf; ++c) {
             const int key = k0 + c;
-            if (key >= p.Sk || (CAUSAL && key > q_row)) s[c] = -INFINITY;
+            if (key >= p.Sk || (CAUSAL && key > q_row + p.coff)) s[c] = -INFINITY;
           }
         }
         const float mx = row_max(s);
@@ -581,9 +588,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         return true;
       };
       // Block j needs no mask for this half when all its keys lie below lim
-      // (Sk, and when causal also the tile's first row + 1):
+      // (Sk, and when causal also the tile's first row + coff + 1):
       // 128j + 64h + 64 ≤ lim, i.e. j < (lim − 64h + 64) / 128.
-      const int lim = CAUSAL ? min(p.Sk, T.q0 + 1) : p.Sk;
+      const int lim = CAUSAL ? min(p.Sk, T.q0 + 1 + p.coff) : p.Sk;
       const int n_full = min(T.nb, max(0, (lim - kHalf * h + kHalf) / kBN));
       int j = 0;
       for (; j < n_full && ok; ++j, ++g) ok = block(j, std::false_type{});
@@ -652,7 +659,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       warp_arrive(bar_stage_full(qb), lane);  // the store warp writes the tile out
       if (h == 0 && q_row < p.Sq) {
         const float lse = (Lsum > 0.f) ? (m + __log2f(Lsum)) * 0.69314718055994531f : -INFINITY;
-        p.lse[(static_cast<size_t>(T.b) * p.H + T.h) * p.Sq + q_row] = lse;
+        p.lse[(static_cast<size_t>(T.b) * p.H + T.h) * p.lse_pitch + q_row] = lse;
       }
     }
   }

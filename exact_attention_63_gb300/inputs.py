@@ -34,6 +34,12 @@ class Workload:
     sigma_qk: float = 1.0
     sigma_v: float = 1.0
     seed: int = 0
+    H_kv: int = 0                  # key/value heads (grouped-query attention); 0 = H
+    causal_align: str = "top-left"  # or "bottom-right" (key j visible to row i iff j <= i + Sk - Sq)
+
+    @property
+    def kv_heads(self) -> int:
+        return self.H_kv or self.H
 
     @property
     def scale(self) -> float:
@@ -48,7 +54,7 @@ class Workload:
     @property
     def io_bytes(self) -> int:
         """Algorithmic HBM bytes: Q, K, V read once, O written once (bf16), LSE (fp32)."""
-        return 2 * self.d * self.B * self.H * (2 * self.Sq + 2 * self.Sk) + 4 * self.B * self.H * self.Sq
+        return 2 * self.d * self.B * (2 * self.H * self.Sq + 2 * self.kv_heads * self.Sk) + 4 * self.B * self.H * self.Sq
 
     def as_dict(self):
         d = asdict(self)
@@ -72,8 +78,8 @@ def make_inputs(w: Workload, seed: int | None = None, device=None):
     g = torch.Generator(device="cpu")
     g.manual_seed(w.seed if seed is None else seed)
     q = torch.randn((w.B, w.Sq, w.H, w.d), generator=g, dtype=torch.float32)
-    k = torch.randn((w.B, w.Sk, w.H, w.d), generator=g, dtype=torch.float32)
-    v = torch.randn((w.B, w.Sk, w.H, w.d), generator=g, dtype=torch.float32)
+    k = torch.randn((w.B, w.Sk, w.kv_heads, w.d), generator=g, dtype=torch.float32)
+    v = torch.randn((w.B, w.Sk, w.kv_heads, w.d), generator=g, dtype=torch.float32)
     if w.sigma_qk != 1.0:
         q.mul_(w.sigma_qk)
         k.mul_(w.sigma_qk)
@@ -85,7 +91,10 @@ def make_inputs(w: Workload, seed: int | None = None, device=None):
     return out
 
 
-def custom(B, H, Sq, Sk, d, causal, sigma_qk=1.0, sigma_v=1.0, seed=0, name=None) -> Workload:
+def custom(B, H, Sq, Sk, d, causal, sigma_qk=1.0, sigma_v=1.0, seed=0, name=None, H_kv=0,
+           causal_align="top-left") -> Workload:
     """A workload with explicit sizes (tests: ragged tails, edge cases)."""
-    return Workload(name or f"attn_b{B}_h{H}_sq{Sq}_sk{Sk}_d{d}{'_causal' if causal else ''}",
-                    B, H, Sq, Sk, d, causal, sigma_qk, sigma_v, seed)
+    tag = (f"_hkv{H_kv}" if H_kv else "") + ("_causal" if causal else "") + \
+        ("_br" if causal and causal_align == "bottom-right" else "")
+    return Workload(name or f"attn_b{B}_h{H}_sq{Sq}_sk{Sk}_d{d}{tag}",
+                    B, H, Sq, Sk, d, causal, sigma_qk, sigma_v, seed, H_kv, causal_align)

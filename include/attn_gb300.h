@@ -65,7 +65,8 @@ enum {
   ATTN_ERR_TIMEOUT = -8,   /* (attn_get_status) a kernel wait exceeded its limit; outputs invalid */
   ATTN_ERR_OPTION = -9,    /* an attn_options field is out of range */
   ATTN_ERR_WORKSPACE = -10, /* workspace missing, misaligned or smaller than required */
-  ATTN_ERR_STATIC_LIMIT = -11 /* problem needs more than ATTN_STATIC_WORKSPACE_BYTES (attn_fwd_host_static) */
+  ATTN_ERR_STATIC_LIMIT = -11, /* problem needs more than ATTN_STATIC_WORKSPACE_BYTES (attn_fwd_host_static) */
+  ATTN_ERR_LAYOUT = -12       /* an attn_layout field is invalid (head grouping, strides, causal alignment) */
 };
 
 /*
@@ -130,6 +131,54 @@ typedef struct attn_options {
 int attn_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse,
                 int B, int H, int Sq, int Sk, int d, float scale, int causal,
                 const attn_options* opts, cudaStream_t stream);
+
+/*
+ * Layout and head grouping for attn_fwd_layout().  Zero-initialise and set
+ * struct_size = sizeof(attn_layout); a zero field keeps attn_fwd's default.
+ *
+ * num_kv_heads — H_kv, the number of key/value heads.  Grouped-query attention
+ *   ("FlashAttention 4: Atenção Mais Rápida …", section "Compatibilidade e
+ *   status atual": several query heads share one key/value projection): H must
+ *   be a multiple of H_kv and query head h reads key/value head h / (H / H_kv);
+ *   k and v are then [B, Sk, H_kv, d].  0 selects H (multi-head attention);
+ *   1 is multi-query attention.
+ * causal_align — used when causal != 0.  ATTN_CAUSAL_TOP_LEFT (0, the
+ *   default and attn_fwd's rule): key j is visible to query i iff j ≤ i.
+ *   ATTN_CAUSAL_BOTTOM_RIGHT (1): iff j ≤ i + Sk − Sq, so the last query row
+ *   sees every key.  Rows that see no key (bottom-right with Sq > Sk: the
+ *   first Sq − Sk rows) get O = 0 and LSE = −inf.  The pages fix no rule for
+ *   Sq ≠ Sk; both common ones are offered.
+ * q_strides, k_strides, v_strides, o_strides — element strides of the batch,
+ *   sequence and head dimensions of each tensor; the d elements of one head
+ *   row stay contiguous.  All three zero selects the dense layout above.
+ *   Otherwise each must be a positive multiple of 8 elements (16 bytes, a TMA
+ *   requirement) below 2^38.  Example: a packed [B, S, 3, H, d] QKV tensor
+ *   gives q, k, v at element offsets 0, H·d, 2·H·d with strides
+ *   (3·S·H·d, 3·H·d, d).  o must not overlap q, k, v or lse.
+ * LSE stays dense [B, H, Sq].
+ */
+#define ATTN_CAUSAL_TOP_LEFT 0
+#define ATTN_CAUSAL_BOTTOM_RIGHT 1
+typedef struct attn_layout {
+  size_t struct_size;
+  int num_kv_heads;
+  int causal_align;
+  long long q_strides[3];
+  long long k_strides[3];
+  long long v_strides[3];
+  long long o_strides[3];
+} attn_layout;
+
+/*
+ * attn_fwd_layout — attn_fwd_ex with a layout (layout may be NULL: dense
+ * multi-head tensors, top-left causal alignment, the same as attn_fwd_ex).
+ * Argument meanings, ownership and asynchrony as attn_fwd; additional errors:
+ * ATTN_ERR_LAYOUT for an invalid layout.  When rows see no key, their O and
+ * LSE are written by a second, small kernel on the same stream.
+ */
+int attn_fwd_layout(const void* q, const void* k, const void* v, void* o, float* lse,
+                    int B, int H, int Sq, int Sk, int d, float scale, int causal,
+                    const attn_layout* layout, const attn_options* opts, cudaStream_t stream);
 
 /*
  * attn_fwd_host — the same operation on HOST buffers, end to end.

@@ -109,3 +109,31 @@ def test_python_binding_rejects_cpu_tensors():
     q = torch.zeros(1, 8, 1, 64, dtype=torch.bfloat16)
     with pytest.raises(ValueError):
         attn.attn_fwd(q, q, q)
+
+
+@pytest.mark.parametrize("lay,expect", [
+    (dict(num_kv_heads=3), -12),                       # H = 4 is not a multiple of 3
+    (dict(num_kv_heads=-1), -12),
+    (dict(num_kv_heads=8), -12),                       # more K/V heads than query heads
+    (dict(causal_align=2), -12),
+    (dict(q_strides=(4096, 512, 60)), -12),            # not a multiple of 8 elements
+    (dict(k_strides=(4096, 0, 64)), -12),              # zero mixed with non-zero strides
+    (dict(v_strides=(-4096, 512, 64)), -12),
+    (dict(o_strides=(1 << 38, 512, 64)), -12),         # beyond the TMA stride range
+])
+def test_bad_layout_rejected(L, lay, expect):
+    layout = attn.make_layout(**lay)
+    assert attn.raw_fwd_layout(A, A, A, A, A, 2, 4, 8, 8, 64, 0.125, 1, layout) == expect
+
+
+def test_layout_struct_size_checked(L):
+    layout = attn.make_layout()
+    layout.struct_size = 8
+    assert attn.raw_fwd_layout(A, A, A, A, A, 1, 1, 8, 8, 64, 0.125, 0, layout) == -12
+
+
+def test_layout_argument_checks_come_first(L):
+    # Plain argument errors are reported as by attn_fwd, layout or not.
+    layout = attn.make_layout(num_kv_heads=3)
+    assert attn.raw_fwd_layout(A, A, A, A, A, 1, 4, 8, 8, 96, 0.125, 0, layout) == -3
+    assert attn.raw_fwd_layout(0, A, A, A, A, 1, 4, 8, 8, 64, 0.125, 0, None) == -1
