@@ -15,6 +15,7 @@ from .attention import (  # noqa: F401
     attention_forward,
     attention_head,
     attention_rows,
+    attention_varlen,
     head_probabilities,
     head_scores,
     kv_head,

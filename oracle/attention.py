@@ -169,6 +169,38 @@ def attention_rows(q, k, v, scale: float, causal: bool, b: int, h: int, rows, ca
     return attention_head(qh, kh, vh, scale, causal, rows=rows, causal_offset=causal_offset)
 
 
+def attention_varlen(q, k, v, cu_q, cu_k, scale: float, causal: bool, bottom_right: bool = False):
+    """Exact attention over a batch of sequences of different lengths packed
+    along the row dimension (the "varlen" layout).
+
+    q: [total_q, H, d]; k, v: [total_k, H_kv, d]; cu_q, cu_k: [n + 1]
+    ascending row offsets (cu[0] = 0): sequence s owns query rows
+    [cu_q[s], cu_q[s+1]) and key rows [cu_k[s], cu_k[s+1]), and attends only to
+    its own keys.  Causal masks align per sequence: top-left (j ≤ i) or, with
+    ``bottom_right``, j ≤ i + len_k − len_q.  Rows that see no key get O = 0,
+    LSE = −inf.  Returns O [total_q, H, d] and LSE [H, total_q] (float64).
+    """
+    q, k, v = to_f64(q), to_f64(k), to_f64(v)
+    cu_q = [int(x) for x in np.asarray(cu_q)]
+    cu_k = [int(x) for x in np.asarray(cu_k)]
+    total_q, H, d = q.shape
+    H_kv = k.shape[1]
+    O = np.zeros((total_q, H, v.shape[2]), dtype=np.float64)
+    LSE = np.full((H, total_q), -np.inf, dtype=np.float64)
+    for s in range(len(cu_q) - 1):
+        q0, q1, k0, k1 = cu_q[s], cu_q[s + 1], cu_k[s], cu_k[s + 1]
+        if q1 <= q0:
+            continue
+        off = (k1 - k0) - (q1 - q0) if (causal and bottom_right) else 0
+        for h in range(H):
+            g = kv_head(h, H, H_kv)
+            if k1 <= k0:
+                continue  # no keys: O = 0, LSE = −inf
+            O[q0:q1, h, :], LSE[h, q0:q1] = attention_head(q[q0:q1, h, :], k[k0:k1, g, :], v[k0:k1, g, :], scale,
+                                                           causal, causal_offset=off)
+    return O, LSE
+
+
 def combine_partials(O_parts, LSE_parts):
     """Merge attention results computed over disjoint key ranges.
 

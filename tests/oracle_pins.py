@@ -367,4 +367,53 @@ def pin_rows_grouped_offset():
         assert np.max(np.abs(O[0, rows, h] - Os)) <= TOL and np.max(np.abs(L[0, h, rows] - Ls)) <= TOL
 
 
+# ------------------------------------------------------ packed sequences
+def pin_varlen_identities():
+    """Packed sequences: each sequence's rows equal the batched forward of that
+    sequence alone (B = 1), equal lengths equal the batched forward of the
+    reshaped tensors, and empty key or query ranges give O = 0, LSE = −inf."""
+    r = _rng(1700)
+    H, H_kv, d = 4, 2, 16
+    lq = [5, 0, 12, 1, 9]
+    lk = [7, 3, 12, 0, 4]
+    cu_q, cu_k = np.concatenate([[0], np.cumsum(lq)]), np.concatenate([[0], np.cumsum(lk)])
+    q = _bf16_like(r.standard_normal((cu_q[-1], H, d)))
+    k = _bf16_like(r.standard_normal((cu_k[-1], H_kv, d)))
+    v = _bf16_like(r.standard_normal((cu_k[-1], H_kv, d)))
+    for causal, br in ((False, False), (True, False), (True, True)):
+        O, L = oracle.attention_varlen(q, k, v, cu_q, cu_k, 0.25, causal, bottom_right=br)
+        for s_ in range(len(lq)):
+            a, b = cu_q[s_], cu_q[s_ + 1]
+            if a == b:
+                continue
+            if lk[s_] == 0:
+                assert np.all(O[a:b] == 0.0) and np.all(np.isneginf(L[:, a:b]))
+                continue
+            ka, kb = cu_k[s_], cu_k[s_ + 1]
+            off = (kb - ka) - (b - a) if (causal and br) else 0
+            Ob, Lb = oracle.attention_forward(q[None, a:b], k[None, ka:kb], v[None, ka:kb], 0.25, causal,
+                                              causal_offset=off)
+            fin = np.isfinite(Lb[0])
+            assert np.array_equal(fin, np.isfinite(L[:, a:b]))
+            assert np.max(np.abs(O[a:b] - Ob[0])) <= TOL and np.max(np.abs(L[:, a:b][fin] - Lb[0][fin])) <= TOL
+            # brute force on one head of this sequence
+            h = 3
+            g = h // (H // H_kv)
+            Oq, Lq = brute_force_head(q[a:b, h].tolist(), k[ka:kb, g].tolist(), v[ka:kb, g].tolist(), 0.25, causal,
+                                      offset=off)
+            fq = np.isfinite(Lq)
+            assert np.max(np.abs(O[a:b, h] - Oq)) <= TOL and np.max(np.abs(L[h, a:b][fq] - Lq[fq])) <= TOL
+    # equal lengths: the batched layout
+    B, S = 3, 10
+    qb = _bf16_like(r.standard_normal((B, S, H, d)))
+    kb_ = _bf16_like(r.standard_normal((B, S, H_kv, d)))
+    vb = _bf16_like(r.standard_normal((B, S, H_kv, d)))
+    cu = np.arange(B + 1) * S
+    O, L = oracle.attention_varlen(qb.reshape(B * S, H, d), kb_.reshape(B * S, H_kv, d), vb.reshape(B * S, H_kv, d),
+                                   cu, cu, 0.25, True)
+    Ob, Lb = oracle.attention_forward(qb, kb_, vb, 0.25, True)
+    assert np.max(np.abs(O - Ob.reshape(B * S, H, d))) <= TOL
+    assert np.max(np.abs(L - np.transpose(Lb, (1, 0, 2)).reshape(H, B * S))) <= TOL
+
+
 ALL_PINS = [v for k_, v in sorted(globals().items()) if k_.startswith("pin_") and callable(v)]

@@ -33,12 +33,19 @@ MUTANTS = {
     "forward_swaps_kv": ("attention_head(q[b, :, h, :], k[b, :, g, :], v[b, :, g, :]",
                          "attention_head(q[b, :, h, :], v[b, :, g, :], k[b, :, g, :]"),
     "gqa_interleaved_heads": ("return h // (H // H_kv)", "return h % H_kv"),
-    "gqa_ignores_grouping": ("            g = kv_head(h, H, H_kv)\n", "            g = min(h, H_kv - 1)\n"),
+    "gqa_ignores_grouping": ("            g = kv_head(h, H, H_kv)\n            O[b, :, h, :]",
+                             "            g = min(h, H_kv - 1)\n            O[b, :, h, :]"),
+    "varlen_ignores_grouping": ("            g = kv_head(h, H, H_kv)\n            if k1 <= k0:",
+                                "            g = min(h, H_kv - 1)\n            if k1 <= k0:"),
     "offset_ignored": ("keys[None, :] <= rows[:, None] + causal_offset", "keys[None, :] <= rows[:, None]"),
     "offset_negated": ("keys[None, :] <= rows[:, None] + causal_offset", "keys[None, :] <= rows[:, None] - causal_offset"),
     "forward_drops_offset": ("                                                         causal_offset=causal_offset)",
                              "                                                         causal_offset=0)"),
     "rows_drop_offset": ("rows=rows, causal_offset=causal_offset)", "rows=rows)"),
+    "varlen_global_offset": ("        off = (k1 - k0) - (q1 - q0) if (causal and bottom_right) else 0",
+                             "        off = (cu_k[-1] - cu_q[-1]) if (causal and bottom_right) else 0"),
+    "varlen_keys_from_start": ("k[k0:k1, g, :], v[k0:k1, g, :], scale", "k[0:k1 - k0, g, :], v[0:k1 - k0, g, :], scale"),
+    "varlen_lse_row_major": ("O[q0:q1, h, :], LSE[h, q0:q1] = attention_head", "O[q0:q1, h, :], LSE[h, 0:q1 - q0] = attention_head"),
     "forward_lse_transposed_heads": ("LSE[b, h, :] = attention_head", "LSE[b, (h + 1) % H, :] = attention_head"),
     "combine_plain_mean": ("O = (w[..., None] * Os).sum(axis=0)", "O = Os.mean(axis=0)"),
     "combine_lse_max_only": ("LSE = np.where(finite, shift + np.log(np.where(tot > 0, tot, 1.0)), -np.inf)",
@@ -58,7 +65,7 @@ def _load_mutant(old, new):
 @pytest.mark.parametrize("name", sorted(MUTANTS))
 def test_mutant_is_caught(name, monkeypatch):
     mod = _load_mutant(*MUTANTS[name])
-    for fn in ("attention_forward", "attention_head", "attention_rows", "head_probabilities",
+    for fn in ("attention_forward", "attention_head", "attention_rows", "attention_varlen", "head_probabilities",
                "head_scores", "kv_head", "visible_mask", "combine_partials"):
         monkeypatch.setattr(oracle, fn, getattr(mod, fn))
     caught = []
