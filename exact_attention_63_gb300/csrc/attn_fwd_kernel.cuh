@@ -15,16 +15,15 @@
 //              (the merge a split over keys needs).  Splitting the columns
 //              halves each thread's serial work and puts two softmax warps on
 //              every scheduler, while no value crosses warpgroups per block.
-//   warp  8    loader — TMA loads of each tile's Q into one of two Q buffers,
-//              and of K and V tiles into a ring of shared-memory slots guarded
-//              by full/empty mbarriers, in the order the MMA issuer consumes
-//              them (K_0 … K_{NB−1}, then V_g, K_{g+NB} for every block g,
-//              across tile boundaries), so slots free up in the order they are
-//              refilled;
-//              allocates and frees tensor memory
+//   warp  8    loader — TMA loads of K and V tiles into a ring of shared-
+//              memory slots guarded by full/empty mbarriers, in the order the
+//              MMA issuers consume them (K_0 … K_{NB−1}, then V_g, K_{g+NB} for
+//              every block g, across tile boundaries), so slots free up in the
+//              order they are refilled; allocates and frees tensor memory
 //   warp  9    P·V issuer (one thread) — tcgen05.mma O_h += P_h V_j[64h:64h+64]
 //   warp 10    S issuer (one thread) — tcgen05.mma S = Q K_jᵀ
-//   warp 11    output store (one thread) — TMA store of each finished tile
+//   warp 11    Q and output (one thread) — TMA loads of each tile's Q into one
+//              of two Q buffers and the TMA store of each finished tile
 //              Accumulators live in tensor memory.  An MMA issue stalls while
 //              the tensor core's queue is full, so a single issuer leaves the
 //              tensor core idle during each of its barrier waits; with two,
@@ -46,8 +45,8 @@
 //
 // The epilogue stages the tile's bf16 output in the tile's own Q buffer (idle
 // once the tile's last S has completed); the store warp writes it with one TMA
-// store and hands the buffer back to the loader only after the store has read
-// it.
+// store and, once the store has read it, loads the Q of the tile two ahead
+// into it.
 //
 // TMEM columns (512 allocated): S buffers [128·i, 128·i+128) for i < NB,
 // then O_0 [128·NB, 128·NB+D) and O_1 [128·NB+D, 128·NB+2D).  P_h (bf16, two per 32-bit column) overwrites
@@ -71,8 +70,11 @@
 //    waiting for it).  The epilogue waits on o_final, completed once per tile
 //    after its last P·V.  stage_full(b) serves the tiles staged in Q buffer
 //    b; it cannot run two phases ahead of the store warp, because staging
-//    tile t+2 in buffer b needs that tile's Q, which the loader brings only
-//    after the store of tile t has released the buffer.
+//    tile t+2 in buffer b needs that tile's Q, which the store warp loads
+//    only after its store of tile t.
+//  * The K/V loader waits only for ring slots, each freed by an MMA of an
+//    earlier block, so its look-ahead of NB blocks can never wait on work
+//    that needs a later load.
 #pragma once
 
 #include <cstdint>
@@ -95,14 +97,21 @@ constexpr int kSoftmaxWarps = 8;
 constexpr uint32_t kTmemCols = 512;
 
 struct FwdParams {
-  void* o;                       // bf16 [B, Sq, H, D]
-  float* lse;                    // [B, H, Sq]
+  void* o;                       // bf16 [B, Sq, H, D] (element strides o_sb, o_ss, o_sh)
+  float* lse;                    // [B, H, Sq] ([H, total_q] for packed sequences)
   unsigned int* status;          // device status word
   unsigned long long* counters;  // optional diagnostics (may be null)
-  int B, H, Sq, Sk;
+  int B, H, Sq, Sk;              // packed sequences: B = sequences, Sq = longest query sequence
   int group;                     // query heads per key/value head (H / H_kv)
   int coff;                      // causal: key j visible to row i iff j ≤ i + coff (≥ 0)
   int lse_pitch;                 // LSE elements between consecutive (batch, head) rows
+  long long o_sb, o_ss, o_sh;    // element strides of O (batch, seq, head)
+  // Packed sequences of different lengths (null when not): sequence s owns the
+  // rows [cu_q[s], cu_q[s+1]) of Q/O and [cu_k[s], cu_k[s+1]) of K/V.
+  const int* cu_q;
+  const int* cu_k;
+  int total_q, total_k;          // rows of the packed tensors (bounds for cu_q, cu_k)
+  int bottom_right;              // packed, causal: per-sequence offset len_k − len_q
   int n_qt;                      // ceil(Sq / 128)
   int n_tiles;                   // n_qt · B · H
   float scale_log2;              // scale · log2(e)
@@ -126,9 +135,9 @@ struct Layout {
   // per-row (max, sum) of each half, exchanged once per tile: [tile parity][half][row] float2
   static constexpr uint32_t kStatsOff = kRingOff + kStages * kTileBytes;
   static constexpr uint32_t kBarOff = kStatsOff + 2 * 2 * kBM * 8;
-  // barriers: q_full[2], q_empty[2], kv_full[S], kv_empty[S], s_full[NB], p_full[NB], pv_done[NB],
+  // barriers: q_full[2], kv_full[S], kv_empty[S], s_full[NB], p_full[NB], pv_done[NB],
   //           o_final, exch_full[2], exch_empty[2], done[2], stage_full[2]
-  static constexpr int kNumBars = 2 + 2 + 2 * kStages + 3 * kSBufs + 1 + 2 + 2 + 2 + 2;
+  static constexpr int kNumBars = 2 + 2 * kStages + 3 * kSBufs + 1 + 2 + 2 + 2 + 2;
   static constexpr uint32_t kMiscOff = kBarOff + 8 * kNumBars;  // tmem base (4 B) + abort flag (4 B)
   static constexpr uint32_t kSmemBytes = kMiscOff + 16 + 1024;  // + slack to align the base to 1024
   __device__ static constexpr uint32_t col_s(int buf) { return 128u * buf; }
@@ -190,14 +199,26 @@ __device__ __forceinline__ bool wait_bar_cold(uint32_t bar, uint32_t parity, con
 
 // One work tile: 128 query rows of one (batch, head).
 struct Tile {
-  int b, h, q0, nb;  // nb = key blocks visible to the tile (≥ 1)
+  int b, h, q0, nb;  // nb = key blocks visible to the tile; < 1: the pipeline skips it
   int kvh;           // key/value head read by query head h
+  int len_q, len_k;  // query rows and keys of the tile's sequence
+  int coff;          // causal offset of the sequence
+  int qrow, krow;    // TMA row coordinate of the tile's first query and of the sequence's first key
+  int bcoord;        // TMA batch coordinate
+  long long lse0;    // LSE index of the tile's first row
 };
+
+// Whether the MMA pipeline processes the tile: it has rows and sees keys
+// (always, unless sequences are packed).
+template <bool VARLEN>
+__device__ __forceinline__ bool runs(const Tile& t) {
+  if constexpr (VARLEN) return t.q0 < t.len_q && t.nb >= 1; else return true;
+}
 
 // Tile order.  Causal: heaviest query tiles first (longest-processing-time
 // order for the static round-robin below).  Otherwise: the tiles of one head
 // are consecutive, so CTAs working side by side share that head's K/V in L2.
-template <bool CAUSAL>
+template <bool CAUSAL, bool VARLEN>
 __device__ __forceinline__ Tile tile_info(int idx, const FwdParams& p) {
   const int BH = p.B * p.H;
   int qt, bh;
@@ -213,17 +234,80 @@ __device__ __forceinline__ Tile tile_info(int idx, const FwdParams& p) {
   t.h = bh % p.H;
   t.q0 = qt * kBM;
   t.kvh = t.h / p.group;
-  const int nk = (p.Sk + kBN - 1) / kBN;
-  // Causal: the tile's last row sees keys up to row + coff (coff ≥ 0, so every
-  // tile sees at least key 0).
-  t.nb = CAUSAL ? min(nk, (min(t.q0 + kBM, p.Sq) - 1 + p.coff) / kBN + 1) : nk;
+  if constexpr (VARLEN) {
+    // Packed sequences; offsets outside the tensors are clamped, so a bad
+    // table cannot make the kernel read or write outside them.
+    const int qa = min(max(p.cu_q[t.b], 0), p.total_q), qz = min(max(p.cu_q[t.b + 1], qa), p.total_q);
+    const int ka = min(max(p.cu_k[t.b], 0), p.total_k), kz = min(max(p.cu_k[t.b + 1], ka), p.total_k);
+    t.len_q = qz - qa;
+    t.len_k = kz - ka;
+    t.coff = (CAUSAL && p.bottom_right) ? t.len_k - t.len_q : 0;
+    t.qrow = qa + t.q0;
+    t.krow = ka;
+    t.bcoord = 0;
+    t.lse0 = static_cast<long long>(t.h) * p.lse_pitch + qa + t.q0;
+    const int nk = (t.len_k + kBN - 1) / kBN;
+    // Causal: the tile's last row sees keys up to row + coff (none when that
+    // is negative).
+    const int last = min(t.q0 + kBM, t.len_q) - 1 + t.coff;
+    t.nb = CAUSAL ? (last < 0 ? 0 : min(nk, last / kBN + 1)) : nk;
+  } else {
+    // One sequence per batch: the sizes are the kernel's parameters (coff ≥ 0,
+    // so every tile sees a key); the per-sequence fields stay unset and the
+    // accessors below read the parameters instead.
+    const int nk = (p.Sk + kBN - 1) / kBN;
+    t.nb = CAUSAL ? min(nk, (min(t.q0 + kBM, p.Sq) - 1 + p.coff) / kBN + 1) : nk;
+  }
   return t;
+}
+
+// Per-tile sizes and coordinates: from the tile for packed sequences, else
+// from the kernel parameters (constant bank, no registers held).
+template <bool VARLEN>
+__device__ __forceinline__ int len_q_of(const Tile& t, const FwdParams& p) {
+  if constexpr (VARLEN) return t.len_q; else return p.Sq;
+}
+template <bool VARLEN>
+__device__ __forceinline__ int len_k_of(const Tile& t, const FwdParams& p) {
+  if constexpr (VARLEN) return t.len_k; else return p.Sk;
+}
+template <bool VARLEN>
+__device__ __forceinline__ int coff_of(const Tile& t, const FwdParams& p) {
+  if constexpr (VARLEN) return t.coff; else return p.coff;
+}
+template <bool VARLEN>
+__device__ __forceinline__ int qrow_of(const Tile& t) {
+  if constexpr (VARLEN) return t.qrow; else return t.q0;
+}
+template <bool VARLEN>
+__device__ __forceinline__ int krow_of(const Tile& t) {
+  if constexpr (VARLEN) return t.krow; else return 0;
+}
+template <bool VARLEN>
+__device__ __forceinline__ int bcoord_of(const Tile& t) {
+  if constexpr (VARLEN) return t.bcoord; else return t.b;
+}
+template <bool VARLEN>
+__device__ __forceinline__ long long lse0_of(const Tile& t, const FwdParams& p) {
+  if constexpr (VARLEN) return t.lse0; else return (static_cast<long long>(t.b) * p.H + t.h) * p.lse_pitch + t.q0;
+}
+
+// The first tile index ≥ idx (stepping by stride) that the pipeline runs, with
+// its description in T; p.n_tiles or more when there is none.
+template <bool CAUSAL, bool VARLEN>
+__device__ __forceinline__ int next_running(int idx, int stride, const FwdParams& p, Tile& T) {
+  for (; idx < p.n_tiles; idx += stride) {
+    T = tile_info<CAUSAL, VARLEN>(idx, p);
+    if (runs<VARLEN>(T)) break;
+  }
+  return idx;
 }
 
 // POLY: bit c selects the FMA-pipe polynomial exp2 for 16-column chunk c of
 // every 128-key block (compile time, so the exp loop is one basic block).
 // COUNT: compile the diagnostic counters (only launched when requested).
-template <int D, bool CAUSAL, uint32_t POLY, bool COUNT>
+// VARLEN: sequences of different lengths packed along the rows.
+template <int D, bool CAUSAL, uint32_t POLY, bool COUNT, bool VARLEN>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
@@ -239,11 +323,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t sRing = base + L::kRingOff;
   const uint32_t bars = base + L::kBarOff;
   auto bar_q_full = [&](int i) { return bars + 8u * i; };
-  auto bar_q_empty = [&](int i) { return bars + 8u * (2 + i); };
-  auto bar_kv_full = [&](int s) { return bars + 8u * (4 + s); };
-  auto bar_kv_empty = [&](int s) { return bars + 8u * (4 + L::kStages + s); };
+  auto bar_kv_full = [&](int s) { return bars + 8u * (2 + s); };
+  auto bar_kv_empty = [&](int s) { return bars + 8u * (2 + L::kStages + s); };
   constexpr int NB = L::kSBufs;
-  constexpr uint32_t kB0 = 4 + 2 * L::kStages;  // first per-S-buffer barrier
+  constexpr uint32_t kB0 = 2 + 2 * L::kStages;  // first per-S-buffer barrier
   auto bar_s_full = [&](int i) { return bars + 8u * (kB0 + i); };
   auto bar_p_full = [&](int i) { return bars + 8u * (kB0 + NB + i); };
   auto bar_pv_done = [&](int i) { return bars + 8u * (kB0 + 2 * NB + i); };
@@ -270,7 +353,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     *abort_flag = 0u;
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar_q_full(i), 1);
-      mbar_init(bar_q_empty(i), 1);
     }
     for (int i = 0; i < NB; ++i) {
       mbar_init(bar_s_full(i), 1);
@@ -306,42 +388,32 @@ __global__ void __launch_bounds__(kThreads, 1)
     // =========================================================== loader
     if (lane == 0) {
       int issued = 0;  // ring loads issued
-      int q_issued = 0;
       bool ok = true;
-      // Two cursors over this CTA's (tile, block) sequence, as in the issuer:
-      // K runs two blocks ahead of V.  A tile's Q is loaded just before its K_0.
-      int k_idx = blockIdx.x, k_tc = 0, k_j = 0, gK = 0;
-      Tile k_T = tile_info<CAUSAL>(k_idx, p);
-      int v_idx = blockIdx.x, v_j = 0, gV = 0;
-      Tile v_T = k_T;
+      // Two cursors over this CTA's (tile, block) sequence, as in the issuers:
+      // K runs NB blocks ahead of V.  (Q is loaded by the store warp, so this
+      // thread never waits for a Q buffer: with one-block tiles, the K look-
+      // ahead would otherwise wait for a store that needs a V not yet loaded.)
+      Tile k_T, v_T;
+      int k_idx = next_running<CAUSAL, VARLEN>(blockIdx.x, stride, p, k_T), k_j = 0, gK = 0;
+      int v_idx = k_idx, v_j = 0, gV = 0;
+      v_T = k_T;
       auto ring_load = [&](const CUtensorMap* m, const Tile& T, int j) -> bool {
         const int slot = issued % L::kStages;
         if (!wait_bar(bar_kv_empty(slot), ((issued / L::kStages) & 1) ^ 1u, wc)) return false;
         mbar_arrive_expect_tx(bar_kv_full(slot), L::kTileBytes);
         for (int s = 0; s < L::kSlabs; ++s)
-          tma_load_4d(sRing + slot * L::kTileBytes + s * L::kSlabBytes, m, 64 * s, T.kvh, j * kBN, T.b,
-                      bar_kv_full(slot));
+          tma_load_4d(sRing + slot * L::kTileBytes + s * L::kSlabBytes, m, 64 * s, T.kvh,
+                      krow_of<VARLEN>(T) + j * kBN, bcoord_of<VARLEN>(T), bar_kv_full(slot));
         ++issued;
         return true;
       };
       auto load_k = [&]() -> bool {
-        if (k_j == 0) {
-          const int qb = k_tc & 1;
-          if (!wait_bar(bar_q_empty(qb), ((k_tc >> 1) & 1) ^ 1u, wc)) return false;
-          mbar_arrive_expect_tx(bar_q_full(qb), L::kTileBytes);
-          for (int s = 0; s < L::kSlabs; ++s)
-            tma_load_4d(sQ + qb * L::kTileBytes + s * L::kSlabBytes, &tm_q, 64 * s, k_T.h, k_T.q0, k_T.b,
-                        bar_q_full(qb));
-          ++q_issued;
-          if (p.test_flags & 1u) return false;  // test mode: no K/V copy, the MMA wait must expire
-        }
+        if (p.test_flags & 1u) return false;  // test mode: no K/V copy, the MMA wait must expire
         if (!ring_load(&tm_k, k_T, k_j)) return false;
         ++gK;
         if (++k_j == k_T.nb) {
           k_j = 0;
-          ++k_tc;
-          k_idx += stride;
-          if (k_idx < p.n_tiles) k_T = tile_info<CAUSAL>(k_idx, p);
+          k_idx = next_running<CAUSAL, VARLEN>(k_idx + stride, stride, p, k_T);
         }
         return true;
       };
@@ -351,40 +423,61 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++gV;
         if (++v_j == v_T.nb) {
           v_j = 0;
-          v_idx += stride;
-          if (v_idx < p.n_tiles) v_T = tile_info<CAUSAL>(v_idx, p);
+          v_idx = next_running<CAUSAL, VARLEN>(v_idx + stride, stride, p, v_T);
         }
         while (ok && k_idx < p.n_tiles && gK < gV + NB) ok = load_k();
       }
       // Let every copy still in flight land before the CTA can exit (the
-      // newest load of each slot and of each Q buffer; older ones completed
-      // before their slot was refilled).
+      // newest load of each slot; older ones completed before their slot was
+      // refilled).
       const uint64_t t0 = globaltimer_ns();
       for (int n = (issued > L::kStages ? issued - L::kStages : 0); n < issued; ++n)
         while (!mbar_try_wait(bar_kv_full(n % L::kStages), (n / L::kStages) & 1u))
-          if (globaltimer_ns() - t0 > p.timeout_ns) break;
-      for (int n = (q_issued > 2 ? q_issued - 2 : 0); n < q_issued; ++n)
-        while (!mbar_try_wait(bar_q_full(n & 1), (n >> 1) & 1u))
           if (globaltimer_ns() - t0 > p.timeout_ns) break;
     }
   } else if (warp == kStoreWarp) {
     // ===================================================== output store
     // The softmax warps stage each tile's bf16 output in the tile's Q buffer;
-    // one TMA store writes it (rows beyond Sq are clipped), and the buffer
-    // goes back to the loader once the store has read it.  Doing this here
-    // keeps the store's latency off the softmax warps.
+    // one TMA store writes it (rows beyond Sq are clipped).  The same thread
+    // loads the Q tiles: the CTA's first two at the start, then tile t+2's
+    // into tile t's buffer as soon as the store of tile t has read it.
+    // Doing this here keeps the store's latency off the softmax warps and the
+    // Q buffers' turnover off the K/V loader.
     if (lane == 0) {
+      Tile Tq;
+      int q_idx = next_running<CAUSAL, VARLEN>(blockIdx.x, stride, p, Tq), q_issued = 0;
+      auto load_q = [&]() {
+        const int qb = q_issued & 1;
+        mbar_arrive_expect_tx(bar_q_full(qb), L::kTileBytes);
+        for (int sl = 0; sl < L::kSlabs; ++sl)
+          tma_load_4d(sQ + qb * L::kTileBytes + sl * L::kSlabBytes, &tm_q, 64 * sl, Tq.h, qrow_of<VARLEN>(Tq),
+                      bcoord_of<VARLEN>(Tq), bar_q_full(qb));
+        ++q_issued;
+        q_idx = next_running<CAUSAL, VARLEN>(q_idx + stride, stride, p, Tq);
+      };
+      for (int n = 0; n < 2 && q_idx < p.n_tiles; ++n) load_q();
       int tc = 0;
-      for (int idx = blockIdx.x; idx < p.n_tiles; idx += stride, ++tc) {
-        const Tile T = tile_info<CAUSAL>(idx, p);
+      Tile T;
+      for (int idx = next_running<CAUSAL, VARLEN>(blockIdx.x, stride, p, T); idx < p.n_tiles;
+           idx = next_running<CAUSAL, VARLEN>(idx + stride, stride, p, T), ++tc) {
         const int qb = tc & 1;
         if (!wait_bar(bar_stage_full(qb), (tc >> 1) & 1, wc)) break;
-        for (int sl = 0; sl < L::kSlabs; ++sl)
-          tma_store_4d(&tm_o, sQ + qb * L::kTileBytes + sl * L::kSlabBytes, 64 * sl, T.h, T.q0, T.b);
-        tma_store_commit();
-        tma_store_wait_read0();
-        mbar_arrive(bar_q_empty(qb));
+        // A packed sequence's last tile is written by the softmax threads
+        // (its rows beyond the sequence belong to the next one).
+        if (!VARLEN || T.q0 + kBM <= len_q_of<VARLEN>(T, p)) {
+          for (int sl = 0; sl < L::kSlabs; ++sl)
+            tma_store_4d(&tm_o, sQ + qb * L::kTileBytes + sl * L::kSlabBytes, 64 * sl, T.h, qrow_of<VARLEN>(T),
+                         bcoord_of<VARLEN>(T));
+          tma_store_commit();
+          tma_store_wait_read0();
+        }
+        if (q_idx < p.n_tiles) load_q();  // tile tc + 2, into buffer qb
       }
+      // Let the Q copies still in flight land before the CTA can exit.
+      const uint64_t t0 = globaltimer_ns();
+      for (int n = (q_issued > 2 ? q_issued - 2 : 0); n < q_issued; ++n)
+        while (!mbar_try_wait(bar_q_full(n & 1), (n >> 1) & 1u))
+          if (globaltimer_ns() - t0 > p.timeout_ns) break;
     }
   } else if (warp == kSWarp || warp == kPvWarp) {
     // ====================================================== MMA issuers
@@ -402,8 +495,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint64_t dQ = sdesc_kmajor_sw128(sQ);
         const uint64_t dK = sdesc_kmajor_sw128(sRing);
         int g = 0, tc = 0;
-        for (int idx = blockIdx.x; idx < p.n_tiles && ok; idx += stride, ++tc) {
-          const Tile T = tile_info<CAUSAL>(idx, p);
+        Tile T;
+        for (int idx = next_running<CAUSAL, VARLEN>(blockIdx.x, stride, p, T); idx < p.n_tiles && ok;
+             idx = next_running<CAUSAL, VARLEN>(idx + stride, stride, p, T), ++tc) {
           const int qb = tc & 1;
           for (int j = 0; j < T.nb; ++j, ++g) {
             const int buf = g % NB;
@@ -434,11 +528,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ---------------------------------------------------- P·V issuer
         constexpr uint32_t idPV = idesc_bf16(kBM, D, true);
         const uint64_t dV = sdesc_mnmajor_sw128(sRing, L::kSlabBytes);
+        Tile T;
         int G = 0;  // blocks of this CTA
-        for (int idx = blockIdx.x; idx < p.n_tiles; idx += stride) G += tile_info<CAUSAL>(idx, p).nb;
+        for (int idx = next_running<CAUSAL, VARLEN>(blockIdx.x, stride, p, T); idx < p.n_tiles;
+             idx = next_running<CAUSAL, VARLEN>(idx + stride, stride, p, T))
+          G += T.nb;
         int g = 0;
-        for (int idx = blockIdx.x; idx < p.n_tiles && ok; idx += stride) {
-          const Tile T = tile_info<CAUSAL>(idx, p);
+        for (int idx = next_running<CAUSAL, VARLEN>(blockIdx.x, stride, p, T); idx < p.n_tiles && ok;
+             idx = next_running<CAUSAL, VARLEN>(idx + stride, stride, p, T)) {
           for (int j = 0; j < T.nb; ++j, ++g) {
             const int buf = g % NB;
             // V_j first (loaded well ahead; its slot was freed by a P·V this
@@ -481,10 +578,29 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr int kHalf = kBN / 2;  // keys per half
     bool ok = true;
     int g = 0;   // global block counter of this CTA
-    int tc = 0;  // tiles finished by this CTA
-    for (int idx = blockIdx.x; idx < p.n_tiles && ok; idx += stride, ++tc) {
-      const Tile T = tile_info<CAUSAL>(idx, p);
+    int tc = 0;  // tiles of this CTA the pipeline has run
+    // O row of this thread in tile T (element offset), for the tiles the
+    // softmax threads write directly.
+    auto o_row = [&](const Tile& T) -> uint16_t* {
+      return static_cast<uint16_t*>(p.o) + bcoord_of<VARLEN>(T) * p.o_sb +
+             static_cast<long long>(qrow_of<VARLEN>(T) + r) * p.o_ss + T.h * p.o_sh;
+    };
+    for (int idx = blockIdx.x; idx < p.n_tiles && ok; idx += stride) {
+      const Tile T = tile_info<CAUSAL, VARLEN>(idx, p);
       const int q_row = T.q0 + r;
+      if constexpr (VARLEN) {
+        if (!runs<VARLEN>(T)) {
+          // A tile beyond its sequence has nothing to write; rows of a tile
+          // that sees no key get O = 0 and LSE = −inf.
+          if (T.q0 < T.len_q && q_row < T.len_q) {
+            uint4* const dst = reinterpret_cast<uint4*>(o_row(T) + h * (D / 2));
+#pragma unroll
+            for (int c = 0; c < D / 16; ++c) dst[c] = make_uint4(0u, 0u, 0u, 0u);
+            if (h == 0) p.lse[T.lse0 + r] = -INFINITY;
+          }
+          continue;
+        }
+      }
       float m_run = -INFINITY;  // running reference maximum of this half (log2 domain)
       float l_run = 0.f;        // running row sum of this half (fp32, unrounded p)
       // Row maximum of this half (log2 domain): four independent 16-wide chains.
@@ -556,7 +672,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int c = 0; c < kHalf; ++c) {
             const int key = k0 + c;
-            if (key >= p.Sk || (CAUSAL && key > q_row + p.coff)) s[c] = -INFINITY;
+            if (key >= len_k_of<VARLEN>(T, p) || (CAUSAL && key > q_row + coff_of<VARLEN>(T, p))) s[c] = -INFINITY;
           }
         }
         const float mx = row_max(s);
@@ -590,7 +706,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       // Block j needs no mask for this half when all its keys lie below lim
       // (Sk, and when causal also the tile's first row + coff + 1):
       // 128j + 64h + 64 ≤ lim, i.e. j < (lim − 64h + 64) / 128.
-      const int lim = CAUSAL ? min(p.Sk, T.q0 + 1 + p.coff) : p.Sk;
+      const int lk = len_k_of<VARLEN>(T, p);
+      const int lim = CAUSAL ? min(lk, T.q0 + 1 + coff_of<VARLEN>(T, p)) : lk;
       const int n_full = min(T.nb, max(0, (lim - kHalf * h + kHalf) / kBN));
       int j = 0;
       for (; j < n_full && ok; ++j, ++g) ok = block(j, std::false_type{});
@@ -631,6 +748,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t t1 = tmem + L::col_o(1) + lane_off + h * (D / 2);
       const int qb = tc & 1;
       uint8_t* const stage = smem + L::kQOff + qb * L::kTileBytes;
+      // A packed sequence's last tile: each thread writes its own row (rows
+      // beyond the sequence belong to the next one); else staged for the TMA
+      // store.
+      const bool direct = VARLEN && T.q0 + kBM > len_q_of<VARLEN>(T, p);
+      uint16_t* const orow = o_row(T);
 #pragma unroll 1
       for (int c = 0; c < D / 64; ++c) {
         uint32_t x0[32], x1[32];
@@ -652,15 +774,19 @@ __global__ void __launch_bounds__(kThreads, 1)
           wv.w = pack_bf16x2(v[6], v[7]);
           const int col = h * (D / 2) + 32 * c + 8 * q16;
           const int chunk = (col & 63) >> 3;
-          *reinterpret_cast<uint4*>(stage + (col >> 6) * L::kSlabBytes + r * 128 + ((chunk ^ (r & 7)) << 4)) = wv;
+          if (!direct)
+            *reinterpret_cast<uint4*>(stage + (col >> 6) * L::kSlabBytes + r * 128 + ((chunk ^ (r & 7)) << 4)) = wv;
+          else if (q_row < len_q_of<VARLEN>(T, p))
+            *reinterpret_cast<uint4*>(orow + col) = wv;
         }
       }
       fence_proxy_async_smem();
       warp_arrive(bar_stage_full(qb), lane);  // the store warp writes the tile out
-      if (h == 0 && q_row < p.Sq) {
+      if (h == 0 && q_row < len_q_of<VARLEN>(T, p)) {
         const float lse = (Lsum > 0.f) ? (m + __log2f(Lsum)) * 0.69314718055994531f : -INFINITY;
-        p.lse[(static_cast<size_t>(T.b) * p.H + T.h) * p.lse_pitch + q_row] = lse;
+        p.lse[lse0_of<VARLEN>(T, p) + r] = lse;
       }
+      ++tc;
     }
   }
 

@@ -36,6 +36,11 @@ SMALL = [
     inputs.custom(1, 2, 320, 192, 128, True, seed=36),
     inputs.custom(2, 1, 150, 65, 64, True, seed=37),
     inputs.custom(1, 3, 130, 63, 128, False, seed=38),
+    # many tiles of a single key block per CTA (several in a row on each SM),
+    # with the K/V look-ahead running several tiles ahead of the output
+    inputs.custom(2, 160, 256, 100, 64, False, seed=39),
+    inputs.custom(1, 320, 256, 256, 64, True, seed=40),
+    inputs.custom(2, 160, 256, 100, 128, False, seed=41),
 ]
 
 
