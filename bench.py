@@ -231,6 +231,9 @@ def main():
     ap.add_argument("--diag", action="store_true", help="report the rescale rate of one extra launch")
     ap.add_argument("--kv-heads", type=int, default=0,
                     help="grouped-query variant of the workload: K/V heads (H must be a multiple); 0 = H")
+    ap.add_argument("--varlen", type=int, default=0,
+                    help="packed-sequence variant: this many sequences with a seeded mix of lengths up to the "
+                         "workload's S (same H, d, mask); FLOPs counted per sequence")
     ap.add_argument("--causal-align", choices=["top-left", "bottom-right"], default="top-left",
                     help="causal alignment when Sq != Sk (only the square workloads ship, where both agree)")
     args = ap.parse_args()
@@ -240,15 +243,15 @@ def main():
     from exact_attention_63_gb300 import inputs
 
     w = inputs.WORKLOADS[args.config]
-    if args.kv_heads or args.causal_align != "top-left":
+    if args.kv_heads or args.causal_align != "top-left" or args.varlen:
         import dataclasses
 
         if args.kv_heads and w.H % args.kv_heads:
             ap.error(f"H = {w.H} is not a multiple of --kv-heads {args.kv_heads}")
         tag = (f"_hkv{args.kv_heads}" if args.kv_heads else "") + \
-            ("_br" if args.causal_align == "bottom-right" else "")
+            ("_br" if args.causal_align == "bottom-right" else "") + (f"_varlen{args.varlen}" if args.varlen else "")
         w = dataclasses.replace(w, name=w.name + tag, H_kv=args.kv_heads, causal_align=args.causal_align)
-        args.no_e2e = True  # the host-buffer entry point takes dense multi-head tensors only
+        args.no_e2e = True  # the host-buffer entry point takes dense, unpacked multi-head tensors only
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
@@ -275,18 +278,34 @@ def main():
         torch.cuda.synchronize()
 
     seed = adist.rank_seed(w.seed, rank)
-    q, k, v = inputs.make_inputs(w, seed=seed)
-    qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
-    od = torch.empty_like(qd)
-    ld = torch.empty((w.B, w.H, w.Sq), dtype=torch.float32, device=dev)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     opts = (attn.make_options(poly_exp2_mask=args.poly_mask, rescale_threshold=args.tau)
             if (args.poly_mask or args.tau) else None)
     stream = torch.cuda.current_stream()
+    lens = None
+    if args.varlen:
+        # Packed sequences: lengths from the seeded mix; FLOPs per sequence.
+        lens = inputs.varlen_lengths(args.varlen, w.Sq, seed)
+        q, kk, vv, cu_q, cu_k = inputs.make_varlen_inputs(lens, lens, w.H, w.kv_heads, w.d, seed,
+                                                          sigma_qk=w.sigma_qk)
+        qd, kd, vd, cqd, ckd = (t_.to(dev) for t_ in (q, kk, vv, cu_q, cu_k))
+        od = torch.empty_like(qd)
+        ld = torch.empty((w.H, qd.shape[0]), dtype=torch.float32, device=dev)
+        per_seq = [4.0 * w.H * w.d * n * n for n in lens]
+        varlen_flops = sum(f / 2 if w.causal else f for f in per_seq)
 
-    def step():
-        attn.attn_fwd(qd, kd, vd, causal=w.causal, scale=w.scale, out=od, lse=ld, options=opts,
-                      causal_align=w.causal_align)
+        def step():
+            attn.attn_fwd_varlen(qd, kd, vd, cqd, ckd, max(lens), causal=w.causal, scale=w.scale, out=od, lse=ld,
+                                 options=opts, causal_align=w.causal_align)
+    else:
+        q, k, v = inputs.make_inputs(w, seed=seed)
+        qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
+        od = torch.empty_like(qd)
+        ld = torch.empty((w.B, w.H, w.Sq), dtype=torch.float32, device=dev)
+
+        def step():
+            attn.attn_fwd(qd, kd, vd, causal=w.causal, scale=w.scale, out=od, lse=ld, options=opts,
+                          causal_align=w.causal_align)
 
     for _ in range(args.warmup):
         flush.zero_()
@@ -310,7 +329,7 @@ def main():
     times_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
     total_ms = adist.max_over_ranks(sum(times_ms), device=dev)
     ms_per_step = total_ms / args.steps
-    flops = w.flops
+    flops = varlen_flops if lens is not None else w.flops
     value = flops * world * args.steps / (total_ms * 1e-3) / 1e12
     achieved = flops / (statistics.mean(times_ms) * 1e-3) / 1e12
 
@@ -338,7 +357,7 @@ def main():
                "d2h_bytes_per_step": int((q.numel() * 2 + w.B * w.H * w.Sq * 4) * world)}
 
     diag = None
-    if args.diag:
+    if args.diag and lens is None:
         cnt = torch.zeros(2, dtype=torch.int64, device=dev)
         attn.attn_fwd(qd, kd, vd, causal=w.causal, scale=w.scale, out=od, lse=ld,
                       options=attn.make_options(poly_exp2_mask=args.poly_mask, rescale_threshold=args.tau,
@@ -374,6 +393,7 @@ def main():
         "data": "synthetic",
         "config": {"workload": w.name, "B": w.B, "H": w.H, "H_kv": w.kv_heads, "Sq": w.Sq, "Sk": w.Sk, "d": w.d,
                    "causal": w.causal, "causal_align": w.causal_align, "sigma_qk": w.sigma_qk, "seed": w.seed,
+                   **({"varlen_lengths": lens} if lens is not None else {}),
                    "l2": "flushed between timed steps (256 MiB write)",
                    "parallelism": f"replicas{world}" if world > 1 else "single"},
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",

@@ -26,7 +26,8 @@ ERRORS = {
 
 # Every symbol the header declares (checked by the CPU test-suite).
 EXPORTS = ["attn_fwd", "attn_fwd_ex", "attn_fwd_host", "attn_fwd_host_workspace_size", "attn_get_status",
-           "attn_strerror", "attn_last_cuda_error", "attn_version", "attn_fwd_host_static", "attn_fwd_layout"]
+           "attn_strerror", "attn_last_cuda_error", "attn_version", "attn_fwd_host_static", "attn_fwd_layout",
+           "attn_fwd_varlen"]
 
 CAUSAL_ALIGN = {"top-left": 0, "bottom-right": 1}
 
@@ -82,6 +83,9 @@ def lib():
     L.attn_fwd_layout.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, ctypes.POINTER(Layout),
                                   ctypes.POINTER(Options), vp]
     L.attn_fwd_layout.restype = i
+    L.attn_fwd_varlen.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f, i, i, ctypes.POINTER(Options),
+                                  vp]
+    L.attn_fwd_varlen.restype = i
     L.attn_fwd_host.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp, sz, vp]
     L.attn_fwd_host.restype = i
     L.attn_fwd_host_workspace_size.argtypes = [i, i, i, i, i]
@@ -182,6 +186,54 @@ def attn_fwd(q, k, v, causal: bool = False, scale: float | None = None, out=None
     return out, lse
 
 
+def attn_fwd_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int, causal: bool = False,
+                    scale: float | None = None, out=None, lse=None, stream=None, options: Options | None = None,
+                    causal_align: str = "top-left"):
+    """Exact attention over sequences of different lengths packed along the rows.
+
+    q [total_q, H, d], k and v [total_k, H_kv, d] (dense bf16, H a multiple of
+    H_kv); cu_seqlens_q / cu_seqlens_k: int32 CUDA tensors of n + 1 ascending
+    row offsets starting at 0 (sequence s owns rows [cu[s], cu[s+1]));
+    max_seqlen_q >= every query length.  Returns (o [total_q, H, d] bf16,
+    lse [H, total_q] fp32).  Causal masks align per sequence.
+    """
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if t.dtype != torch.bfloat16 or not t.is_cuda or t.dim() != 3 or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous 3-D bf16 CUDA tensor (rows, heads, head_dim)")
+    total_q, H, d = q.shape
+    total_k, H_kv = k.shape[0], k.shape[1]
+    if k.shape != v.shape or k.shape[2] != d or H % H_kv != 0:
+        raise ValueError(f"shape mismatch: q {tuple(q.shape)}, k {tuple(k.shape)}, v {tuple(v.shape)}")
+    for name, t in (("cu_seqlens_q", cu_seqlens_q), ("cu_seqlens_k", cu_seqlens_k)):
+        if t.dtype != torch.int32 or not t.is_cuda or t.dim() != 1 or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous 1-D int32 CUDA tensor")
+    n_seq = cu_seqlens_q.numel() - 1
+    if cu_seqlens_k.numel() != n_seq + 1:
+        raise ValueError("cu_seqlens_q and cu_seqlens_k must have the same length")
+    if causal_align not in CAUSAL_ALIGN:
+        raise ValueError(f"causal_align must be one of {sorted(CAUSAL_ALIGN)}")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((H, total_q), dtype=torch.float32, device=q.device)
+    if out.shape != q.shape or out.dtype != torch.bfloat16 or not out.is_contiguous():
+        raise ValueError("out must be a contiguous bf16 tensor shaped like q")
+    if lse.shape != (H, total_q) or lse.dtype != torch.float32 or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous fp32 tensor of shape (H, total_q)")
+    if options is not None:
+        options.struct_size = ctypes.sizeof(Options)
+    with torch.cuda.device(q.device):
+        rc = lib().attn_fwd_varlen(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
+                                   cu_seqlens_q.data_ptr(), cu_seqlens_k.data_ptr(), n_seq, total_q, total_k,
+                                   int(max_seqlen_q), H, H_kv, d, float(scale), int(bool(causal)),
+                                   CAUSAL_ALIGN[causal_align], ctypes.byref(options) if options is not None else None,
+                                   _stream_handle(stream))
+    _check(rc)
+    return out, lse
+
+
 TEST_WITHHOLD_KV = 1
 
 
@@ -232,6 +284,14 @@ def attn_fwd_host_static(q_h, k_h, v_h, o_h, lse_h, causal: bool, scale: float, 
 def get_status(stream=None) -> int:
     """Synchronise the stream and return/clear the device status (0 = ok)."""
     return int(lib().attn_get_status(_stream_handle(stream)))
+
+
+def raw_fwd_varlen(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, cu_q_ptr, cu_k_ptr, n_seq, total_q, total_k, max_q, H, H_kv,
+                   d, scale, causal, causal_align=0, stream_ptr=0) -> int:
+    """Direct attn_fwd_varlen call with integer pointers; returns the status code (tests)."""
+    return int(lib().attn_fwd_varlen(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, cu_q_ptr, cu_k_ptr, n_seq, total_q, total_k,
+                                     max_q, H, H_kv, d, float(scale), int(causal), causal_align, None,
+                                     ctypes.c_void_p(stream_ptr)))
 
 
 def raw_fwd_layout(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, B, H, Sq, Sk, d, scale, causal, layout, stream_ptr=0) -> int:

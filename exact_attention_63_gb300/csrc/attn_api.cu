@@ -164,6 +164,54 @@ constexpr unsigned int kDefaultTimeoutMs = 4000;
 constexpr uint32_t kDefaultPolyMaskD64 = 0x00u;
 constexpr uint32_t kDefaultPolyMaskD128 = 0x00u;
 
+struct Opts {
+  float tau = kDefaultTau;
+  uint32_t poly = 0;
+  unsigned long long* counters = nullptr;
+  unsigned int timeout_ms = kDefaultTimeoutMs;
+  unsigned int test_flags = 0;
+};
+
+int parse_options(const attn_options* opts, int d, Opts* out) {
+  Opts r;
+  r.poly = (d == 64) ? kDefaultPolyMaskD64 : kDefaultPolyMaskD128;
+  if (opts != nullptr) {
+    if (opts->struct_size < sizeof(attn_options)) return ATTN_ERR_OPTION;
+    if (!std::isfinite(opts->rescale_threshold) || opts->rescale_threshold > kMaxTau) return ATTN_ERR_OPTION;
+    if (opts->rescale_threshold < 0.f) r.tau = 0.f;
+    else if (opts->rescale_threshold > 0.f) r.tau = opts->rescale_threshold;
+    if (opts->poly_exp2_mask == 0x100u) r.poly = 0u;
+    else if (opts->poly_exp2_mask != 0u) r.poly = opts->poly_exp2_mask;
+    if (!attn::poly_mask_supported(r.poly)) return ATTN_ERR_OPTION;
+    if (opts->counters != nullptr && (reinterpret_cast<uintptr_t>(opts->counters) & 7u) != 0) return ATTN_ERR_ALIGN;
+    r.counters = opts->counters;
+    if (opts->timeout_ms != 0) r.timeout_ms = opts->timeout_ms;
+    if ((opts->test_flags & ~ATTN_TEST_WITHHOLD_KV) != 0) return ATTN_ERR_OPTION;
+    r.test_flags = opts->test_flags;
+  }
+  *out = r;
+  return ATTN_OK;
+}
+
+// Fill in the launch-wide fields and launch the kernel for (d, causal).
+int launch(attn::LaunchArgs& a, const Opts& op, int dev, int d, int causal, float scale, cudaStream_t stream) {
+  a.p.status = g_dev[dev].status;
+  a.p.counters = op.counters;
+  a.p.scale_log2 = scale * 1.4426950408889634f;
+  a.p.tau = op.tau;
+  a.p.timeout_ns = static_cast<uint64_t>(op.timeout_ms) * 1000000ull;
+  a.p.test_flags = op.test_flags;
+  a.grid = a.p.n_tiles < g_dev[dev].sms ? a.p.n_tiles : g_dev[dev].sms;
+  a.poly = op.poly;
+  a.device = dev;
+  a.stream = stream;
+  cudaError_t e;
+  if (d == 64) e = causal ? attn::launch_fwd_d64_causal(a) : attn::launch_fwd_d64(a);
+  else e = causal ? attn::launch_fwd_d128_causal(a) : attn::launch_fwd_d128(a);
+  if (e != cudaSuccess) return fail_cuda(e, "attention kernel launch");
+  return ATTN_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -225,25 +273,8 @@ int attn_fwd_layout(const void* q, const void* k, const void* v, void* o, float*
         !resolve_strides(vi, Sk * kd, kd, d, vs) || !resolve_strides(oi, Sq * hd, hd, d, os))
       return ATTN_ERR_LAYOUT;
   }
-  float tau = kDefaultTau;
-  uint32_t poly = (d == 64) ? kDefaultPolyMaskD64 : kDefaultPolyMaskD128;
-  unsigned long long* counters = nullptr;
-  unsigned int timeout_ms = kDefaultTimeoutMs;
-  unsigned int test_flags = 0;
-  if (opts != nullptr) {
-    if (opts->struct_size < sizeof(attn_options)) return ATTN_ERR_OPTION;
-    if (!std::isfinite(opts->rescale_threshold) || opts->rescale_threshold > kMaxTau) return ATTN_ERR_OPTION;
-    if (opts->rescale_threshold < 0.f) tau = 0.f;
-    else if (opts->rescale_threshold > 0.f) tau = opts->rescale_threshold;
-    if (opts->poly_exp2_mask == 0x100u) poly = 0u;
-    else if (opts->poly_exp2_mask != 0u) poly = opts->poly_exp2_mask;
-    if (!attn::poly_mask_supported(poly)) return ATTN_ERR_OPTION;
-    if (opts->counters != nullptr && (reinterpret_cast<uintptr_t>(opts->counters) & 7u) != 0) return ATTN_ERR_ALIGN;
-    counters = opts->counters;
-    if (opts->timeout_ms != 0) timeout_ms = opts->timeout_ms;
-    if ((opts->test_flags & ~ATTN_TEST_WITHHOLD_KV) != 0) return ATTN_ERR_OPTION;
-    test_flags = opts->test_flags;
-  }
+  Opts op;
+  if ((rc = parse_options(opts, d, &op)) != ATTN_OK) return rc;
   int dev = -1;
   rc = current_device(&dev);
   if (rc != ATTN_OK) return rc;
@@ -279,8 +310,9 @@ int attn_fwd_layout(const void* q, const void* k, const void* v, void* o, float*
   const int n_qt = (Sq + 127) / 128;
   a.p.o = o;
   a.p.lse = lse;
-  a.p.status = g_dev[dev].status;
-  a.p.counters = counters;
+  a.p.o_sb = os[0];
+  a.p.o_ss = os[1];
+  a.p.o_sh = os[2];
   a.p.B = B;
   a.p.H = H;
   a.p.Sq = Sq;
@@ -290,19 +322,62 @@ int attn_fwd_layout(const void* q, const void* k, const void* v, void* o, float*
   a.p.lse_pitch = lse_pitch;
   a.p.n_qt = n_qt;
   a.p.n_tiles = n_qt * B * H;
-  a.p.scale_log2 = scale * 1.4426950408889634f;
-  a.p.tau = tau;
-  a.p.timeout_ns = static_cast<uint64_t>(timeout_ms) * 1000000ull;
-  a.p.test_flags = test_flags;
-  a.grid = a.p.n_tiles < g_dev[dev].sms ? a.p.n_tiles : g_dev[dev].sms;
-  a.poly = poly;
-  a.device = dev;
-  a.stream = stream;
-  cudaError_t e;
-  if (d == 64) e = causal ? attn::launch_fwd_d64_causal(a) : attn::launch_fwd_d64(a);
-  else e = causal ? attn::launch_fwd_d128_causal(a) : attn::launch_fwd_d128(a);
-  if (e != cudaSuccess) return fail_cuda(e, "attention kernel launch");
-  return ATTN_OK;
+  return launch(a, op, dev, d, causal, scale, stream);
+}
+
+int attn_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse, const int* cu_seqlens_q,
+                    const int* cu_seqlens_k, int n_seq, int total_q, int total_k, int max_seqlen_q, int H, int H_kv,
+                    int d, float scale, int causal, int causal_align, const attn_options* opts, cudaStream_t stream) {
+  if (q == nullptr || k == nullptr || v == nullptr || o == nullptr || lse == nullptr || cu_seqlens_q == nullptr ||
+      cu_seqlens_k == nullptr)
+    return ATTN_ERR_NULL;
+  if (n_seq < 1 || total_q < 1 || total_k < 1 || max_seqlen_q < 1 || H < 1) return ATTN_ERR_SHAPE;
+  const long long n_qt = (static_cast<long long>(max_seqlen_q) + 127) / 128;
+  if (static_cast<long long>(n_seq) * H * n_qt > 0x7FFFFFFFLL) return ATTN_ERR_SHAPE;
+  if (d != 64 && d != 128) return ATTN_ERR_HEAD_DIM;
+  if (!std::isfinite(scale) || !(scale > 0.f)) return ATTN_ERR_SCALE;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) ||
+      (reinterpret_cast<uintptr_t>(cu_seqlens_q) & 3u) != 0 || (reinterpret_cast<uintptr_t>(cu_seqlens_k) & 3u) != 0)
+    return ATTN_ERR_ALIGN;
+  if (H_kv < 1 || H % H_kv != 0) return ATTN_ERR_LAYOUT;
+  if (causal_align != ATTN_CAUSAL_TOP_LEFT && causal_align != ATTN_CAUSAL_BOTTOM_RIGHT) return ATTN_ERR_LAYOUT;
+  Opts op;
+  int rc = parse_options(opts, d, &op);
+  if (rc != ATTN_OK) return rc;
+  if (op.poly != 0u) return ATTN_ERR_OPTION;  // packed sequences: all-MUFU exp2 only
+  int dev = -1;
+  if ((rc = current_device(&dev)) != ATTN_OK) return rc;
+
+  // One "batch" of total rows each; the kernel finds each sequence's rows
+  // through the offset tables.
+  const long long hd = static_cast<long long>(H) * d, kd = static_cast<long long>(H_kv) * d;
+  const long long qs[3] = {total_q * hd, hd, d}, ks[3] = {total_k * kd, kd, d};
+  attn::LaunchArgs a;
+  std::memset(&a, 0, sizeof(a));
+  if ((rc = encode_bshd(&a.q, q, 1, total_q, H, d, qs)) != ATTN_OK) return rc;
+  if ((rc = encode_bshd(&a.k, k, 1, total_k, H_kv, d, ks)) != ATTN_OK) return rc;
+  if ((rc = encode_bshd(&a.v, v, 1, total_k, H_kv, d, ks)) != ATTN_OK) return rc;
+  if ((rc = encode_bshd(&a.o, o, 1, total_q, H, d, qs)) != ATTN_OK) return rc;
+  a.p.o = o;
+  a.p.lse = lse;
+  a.p.o_sb = qs[0];
+  a.p.o_ss = qs[1];
+  a.p.o_sh = qs[2];
+  a.p.B = n_seq;
+  a.p.H = H;
+  a.p.Sq = max_seqlen_q;
+  a.p.Sk = 0;
+  a.p.group = H / H_kv;
+  a.p.coff = 0;
+  a.p.lse_pitch = total_q;
+  a.p.cu_q = cu_seqlens_q;
+  a.p.cu_k = cu_seqlens_k;
+  a.p.total_q = total_q;
+  a.p.total_k = total_k;
+  a.p.bottom_right = (causal && causal_align == ATTN_CAUSAL_BOTTOM_RIGHT) ? 1 : 0;
+  a.p.n_qt = static_cast<int>(n_qt);
+  a.p.n_tiles = static_cast<int>(n_qt * n_seq * H);
+  return launch(a, op, dev, d, causal, scale, stream);
 }
 
 int attn_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Sq, int Sk, int d,

@@ -37,37 +37,44 @@ cudaError_t launch_fwd_d128_causal(const LaunchArgs& a);
 
 // Launch one instantiation, setting its shared-memory opt-in the first time
 // each device uses it.
-template <int D, bool CAUSAL, uint32_t POLY, bool COUNT>
+template <int D, bool CAUSAL, uint32_t POLY, bool COUNT, bool VARLEN>
 cudaError_t launch_one(const LaunchArgs& a) {
   constexpr unsigned int smem = Layout<D>::kSmemBytes;
   static volatile bool configured[64] = {};
   if (a.device < 0 || a.device >= 64) return cudaErrorInvalidDevice;
   if (!configured[a.device]) {
     const cudaError_t e =
-        cudaFuncSetAttribute(attn_fwd_kernel<D, CAUSAL, POLY, COUNT>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        cudaFuncSetAttribute(attn_fwd_kernel<D, CAUSAL, POLY, COUNT, VARLEN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             smem);
     if (e != cudaSuccess) return e;
     configured[a.device] = true;
   }
-  attn_fwd_kernel<D, CAUSAL, POLY, COUNT><<<a.grid, kThreads, smem, a.stream>>>(a.q, a.k, a.v, a.o, a.p);
+  attn_fwd_kernel<D, CAUSAL, POLY, COUNT, VARLEN><<<a.grid, kThreads, smem, a.stream>>>(a.q, a.k, a.v, a.o, a.p);
   return cudaGetLastError();
 }
 
 template <int D, bool CAUSAL, bool COUNT>
 cudaError_t launch_poly(const LaunchArgs& a) {
   switch (a.poly) {
-    case 0x00u: return launch_one<D, CAUSAL, 0x00u, COUNT>(a);
-    case 0x01u: return launch_one<D, CAUSAL, 0x01u, COUNT>(a);
-    case 0x11u: return launch_one<D, CAUSAL, 0x11u, COUNT>(a);
-    case 0x55u: return launch_one<D, CAUSAL, 0x55u, COUNT>(a);
-    case 0xFFu: return launch_one<D, CAUSAL, 0xFFu, COUNT>(a);
+    case 0x00u: return launch_one<D, CAUSAL, 0x00u, COUNT, false>(a);
+    case 0x01u: return launch_one<D, CAUSAL, 0x01u, COUNT, false>(a);
+    case 0x11u: return launch_one<D, CAUSAL, 0x11u, COUNT, false>(a);
+    case 0x55u: return launch_one<D, CAUSAL, 0x55u, COUNT, false>(a);
+    case 0xFFu: return launch_one<D, CAUSAL, 0xFFu, COUNT, false>(a);
     default: return cudaErrorInvalidValue;
   }
 }
 
 // The counting kernels are separate instantiations, so the default ones carry
-// no diagnostic code.
+// no diagnostic code.  Packed sequences (offset tables given) have their own
+// instantiations, compiled with the default exp2 split only.
 template <int D, bool CAUSAL>
 cudaError_t launch_variant(const LaunchArgs& a) {
+  if (a.p.cu_q != nullptr) {
+    if (a.poly != 0x00u) return cudaErrorInvalidValue;
+    return a.p.counters != nullptr ? launch_one<D, CAUSAL, 0x00u, true, true>(a)
+                                   : launch_one<D, CAUSAL, 0x00u, false, true>(a);
+  }
   return a.p.counters != nullptr ? launch_poly<D, CAUSAL, true>(a) : launch_poly<D, CAUSAL, false>(a);
 }
 

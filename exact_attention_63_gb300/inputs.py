@@ -98,3 +98,35 @@ def custom(B, H, Sq, Sk, d, causal, sigma_qk=1.0, sigma_v=1.0, seed=0, name=None
         ("_br" if causal and causal_align == "bottom-right" else "")
     return Workload(name or f"attn_b{B}_h{H}_sq{Sq}_sk{Sk}_d{d}{tag}",
                     B, H, Sq, Sk, d, causal, sigma_qk, sigma_v, seed, H_kv, causal_align)
+
+
+# ------------------------------------------------------- packed sequences
+def varlen_lengths(n: int, max_len: int, seed: int) -> list[int]:
+    """A seeded mix of n sequence lengths in [0, max_len]: mostly uniform,
+    with the edge lengths of a 128-row tile mixed in (1, 127, 128, 129) and the
+    longest one present."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(seed)
+    lens = torch.randint(1, max_len + 1, (n,), generator=g).tolist()
+    edges = [1, 127, 128, 129, max_len]
+    for i, e in enumerate(edges):
+        if i < n and e <= max_len:
+            lens[(i * 7) % n] = e
+    return lens
+
+
+def make_varlen_inputs(lens_q, lens_k, H: int, H_kv: int, d: int, seed: int, sigma_qk: float = 1.0, device=None):
+    """bf16 q [total_q, H, d], k, v [total_k, H_kv, d] and int32 offset tables
+    cu_q, cu_k ([n + 1], starting at 0) for sequences of the given lengths."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(seed)
+    tq, tk = int(sum(lens_q)), int(sum(lens_k))
+    q = torch.randn((tq, H, d), generator=g, dtype=torch.float32) * sigma_qk
+    k = torch.randn((tk, H_kv, d), generator=g, dtype=torch.float32) * sigma_qk
+    v = torch.randn((tk, H_kv, d), generator=g, dtype=torch.float32)
+    cu_q = torch.tensor([0] + list(torch.cumsum(torch.tensor(lens_q), 0).tolist()), dtype=torch.int32)
+    cu_k = torch.tensor([0] + list(torch.cumsum(torch.tensor(lens_k), 0).tolist()), dtype=torch.int32)
+    out = tuple(t.to(torch.bfloat16) for t in (q, k, v)) + (cu_q, cu_k)
+    if device is not None:
+        out = tuple(t.to(device) for t in out)
+    return out

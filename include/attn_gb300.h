@@ -181,6 +181,42 @@ int attn_fwd_layout(const void* q, const void* k, const void* v, void* o, float*
                     const attn_layout* layout, const attn_options* opts, cudaStream_t stream);
 
 /*
+ * attn_fwd_varlen — attention over a batch of sequences of different lengths
+ * packed along the rows ("FlashAttention 4: …", section "Compatibilidade e
+ * status atual", names variable-length batches, processed without padding).
+ *   q, o          : device, bf16 [total_q, H, d] (dense); o is written.
+ *   k, v          : device, bf16 [total_k, H_kv, d] (dense).
+ *   lse           : device, fp32 [H, total_q] (written).
+ *   cu_seqlens_q  : device, int32 [n_seq + 1], ascending, cu_seqlens_q[0] = 0,
+ *                   cu_seqlens_q[n_seq] = total_q: sequence s owns query rows
+ *                   [cu_seqlens_q[s], cu_seqlens_q[s+1]).
+ *   cu_seqlens_k  : the same for key/value rows (total_k); sequence s attends
+ *                   only to its own keys.  Lengths may be 0.
+ *   max_seqlen_q  : host, at least the longest query sequence (it sizes the
+ *                   grid; rows of a longer sequence beyond it are not written).
+ *   H, H_kv, d, scale : as attn_fwd / attn_layout (H a multiple of H_kv).
+ *   causal, causal_align : as attn_fwd / attn_layout, per sequence: with
+ *                   bottom-right alignment key j is visible to row i of a
+ *                   sequence iff j ≤ i + len_k − len_q.  Rows that see no key
+ *                   (also every row of a sequence without keys) get O = 0,
+ *                   LSE = −inf.
+ * The offset tables are read on the device; offsets outside [0, total] are
+ * clamped, so a malformed table gives wrong results but no access outside the
+ * tensors.  Returns ATTN_OK after launching, or a negative code (before any
+ * launch): ATTN_ERR_NULL, ATTN_ERR_SHAPE (n_seq, total_q, total_k,
+ * max_seqlen_q < 1 or the grid does not fit), ATTN_ERR_HEAD_DIM,
+ * ATTN_ERR_SCALE, ATTN_ERR_ALIGN (tensors 16-byte, tables 4-byte aligned),
+ * ATTN_ERR_LAYOUT (H_kv, causal_align), ATTN_ERR_OPTION (also for a
+ * poly_exp2_mask other than the default: this call computes every exp2 on
+ * the MUFU unit).
+ */
+int attn_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse,
+                    const int* cu_seqlens_q, const int* cu_seqlens_k, int n_seq,
+                    int total_q, int total_k, int max_seqlen_q,
+                    int H, int H_kv, int d, float scale, int causal, int causal_align,
+                    const attn_options* opts, cudaStream_t stream);
+
+/*
  * attn_fwd_host — the same operation on HOST buffers, end to end.
  *   q_h, k_h, v_h : host bf16 inputs (layouts above); o_h, lse_h : host outputs.
  *   workspace     : caller-owned DEVICE buffer of at least

@@ -137,3 +137,25 @@ def test_layout_argument_checks_come_first(L):
     layout = attn.make_layout(num_kv_heads=3)
     assert attn.raw_fwd_layout(A, A, A, A, A, 1, 4, 8, 8, 96, 0.125, 0, layout) == -3
     assert attn.raw_fwd_layout(0, A, A, A, A, 1, 4, 8, 8, 64, 0.125, 0, None) == -1
+
+
+@pytest.mark.parametrize("args,expect", [
+    ((0, A, A, A, A, A, A, 2, 100, 100, 64, 4, 2, 64, 0.125, 1), -1),
+    ((A, A, A, A, A, 0, A, 2, 100, 100, 64, 4, 2, 64, 0.125, 1), -1),
+    ((A, A, A, A, A, A, A, 0, 100, 100, 64, 4, 2, 64, 0.125, 1), -2),   # no sequences
+    ((A, A, A, A, A, A, A, 2, 0, 100, 64, 4, 2, 64, 0.125, 1), -2),
+    ((A, A, A, A, A, A, A, 2, 100, 0, 64, 4, 2, 64, 0.125, 1), -2),
+    ((A, A, A, A, A, A, A, 2, 100, 100, 0, 4, 2, 64, 0.125, 1), -2),   # max_seqlen_q
+    ((A, A, A, A, A, A, A, 2, 100, 100, 64, 4, 2, 80, 0.125, 1), -3),
+    ((A, A, A, A, A, A, A, 2, 100, 100, 64, 4, 2, 64, 0.0, 1), -4),
+    ((A, A, A, A, A, A + 2, A, 2, 100, 100, 64, 4, 2, 64, 0.125, 1), -5),  # table not 4-byte aligned
+    ((A + 8, A, A, A, A, A, A, 2, 100, 100, 64, 4, 2, 64, 0.125, 1), -5),
+    ((A, A, A, A, A, A, A, 2, 100, 100, 64, 4, 3, 64, 0.125, 1), -12),  # H not a multiple of H_kv
+    ((A, A, A, A, A, A, A, 2, 100, 100, 64, 4, 0, 64, 0.125, 1), -12),
+])
+def test_varlen_rejected_before_launch(L, args, expect):
+    assert attn.raw_fwd_varlen(*args) == expect
+
+
+def test_varlen_bad_alignment_rejected(L):
+    assert attn.raw_fwd_varlen(A, A, A, A, A, A, A, 2, 100, 100, 64, 4, 2, 64, 0.125, 1, causal_align=5) == -12
