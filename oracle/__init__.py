@@ -12,6 +12,8 @@ library routines and invariants; no function is "parity unpinned".
 """
 
 from .attention import (  # noqa: F401
+    attention_backward,
+    attention_backward_head,
     attention_forward,
     attention_head,
     attention_rows,

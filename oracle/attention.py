@@ -201,6 +201,47 @@ def attention_varlen(q, k, v, cu_q, cu_k, scale: float, causal: bool, bottom_rig
     return O, LSE
 
 
+def attention_backward_head(q, k, v, dO, scale: float, causal: bool, causal_offset: int = 0):
+    """Gradients of one head's attention output with respect to q, k and v.
+
+    The pages give no backward formulas ("FlashAttention-4 no Blackwell B200
+    …", section "Redução de tráfego no backward", only says where FA4 keeps its
+    intermediates), so this is the derivative of the definition above, written
+    out in float64 for a loss whose gradient with respect to O is dO (the LSE
+    output is not differentiated):
+      P = softmax over visible keys of s,  dV = Pᵀ dO,  dP = dO Vᵀ,
+      D_i = Σ_c dO_ic O_ic = Σ_j P_ij dP_ij,  dS = P ∘ (dP − D),
+      dQ = scale · dS K,  dK = scale · dSᵀ Q.
+    Rows without visible keys contribute nothing.  q, dO: [Sq, d]; k, v:
+    [Sk, d].  Returns (dQ [Sq, d], dK [Sk, d], dV [Sk, d], D [Sq]).
+    """
+    q, k, v, dO = (np.asarray(x, dtype=np.float64) for x in (q, k, v, dO))
+    s = head_scores(q, k, scale)
+    P, M, L = head_probabilities(s, visible_mask(np.arange(q.shape[0]), k.shape[0], causal, causal_offset))
+    O = P @ v
+    dV = P.T @ dO
+    dP = dO @ v.T
+    D = (dO * O).sum(axis=1)
+    dS = P * (dP - D[:, None])
+    return scale * (dS @ k), scale * (dS.T @ q), dV, D
+
+
+def attention_backward(q, k, v, dO, scale: float, causal: bool, causal_offset: int = 0):
+    """Gradients over all batches and heads: q, dO [B, Sq, H, d], k, v
+    [B, Sk, H, d] (torch tensors or arrays).  Returns dQ, dK, dV (float64, the
+    shapes of q, k, v)."""
+    q, k, v, dO = to_f64(q), to_f64(k), to_f64(v), to_f64(dO)
+    B, Sq, H, d = q.shape
+    if k.shape[2] != H:
+        raise ValueError("the backward oracle takes one key/value head per query head")
+    dQ, dK, dV = np.zeros_like(q), np.zeros_like(k), np.zeros_like(v)
+    for b in range(B):
+        for h in range(H):
+            dQ[b, :, h], dK[b, :, h], dV[b, :, h], _ = attention_backward_head(
+                q[b, :, h], k[b, :, h], v[b, :, h], dO[b, :, h], scale, causal, causal_offset)
+    return dQ, dK, dV
+
+
 def combine_partials(O_parts, LSE_parts):
     """Merge attention results computed over disjoint key ranges.
 

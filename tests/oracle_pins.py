@@ -416,4 +416,79 @@ def pin_varlen_identities():
     assert np.max(np.abs(L - np.transpose(Lb, (1, 0, 2)).reshape(H, B * S))) <= TOL
 
 
+# ----------------------------------------------------------------- backward
+def _torch_grads(q, k, v, dO, scale, causal, offset=0):
+    """Reference gradients from torch autograd (float64, CPU) of the plain
+    formula softmax(scale·QKᵀ + mask)V: an independent implementation."""
+    import torch
+
+    qt, kt, vt = (torch.tensor(x, dtype=torch.float64, requires_grad=True) for x in (q, k, v))
+    s = scale * qt @ kt.T
+    if causal:
+        i = torch.arange(q.shape[0])[:, None]
+        j = torch.arange(k.shape[0])[None, :]
+        s = s.masked_fill(j > i + offset, float("-inf"))
+    o = torch.softmax(s, dim=1) @ vt
+    (o * torch.tensor(dO, dtype=torch.float64)).sum().backward()
+    return qt.grad.numpy(), kt.grad.numpy(), vt.grad.numpy()
+
+
+def pin_backward_autograd():
+    """Backward against torch autograd (float64) of the plain formula."""
+    for n, (Sq, Sk, d, causal, off) in enumerate([(9, 9, 8, False, 0), (9, 9, 8, True, 0), (7, 13, 16, True, 6),
+                                                  (13, 5, 8, False, 0), (130, 130, 64, True, 0)]):
+        q, k, v = rand_head(1800 + n, Sq, Sk, d, sigma=1.5)
+        dO = _bf16_like(_rng(1850 + n).standard_normal((Sq, d)))
+        dQ, dK, dV, D = oracle.attention_backward_head(q, k, v, dO, 0.3, causal, causal_offset=off)
+        tQ, tK, tV = _torch_grads(q, k, v, dO, 0.3, causal, off)
+        assert np.max(np.abs(dQ - tQ)) <= 1e-10 and np.max(np.abs(dK - tK)) <= 1e-10
+        assert np.max(np.abs(dV - tV)) <= 1e-10
+
+
+def pin_backward_finite_differences():
+    """Central differences of the loss Σ O∘dO on a tiny causal problem."""
+    q, k, v = rand_head(1900, 5, 6, 4, sigma=1.0)
+    dO = _rng(1901).standard_normal((5, 4))
+    dQ, dK, dV, _ = oracle.attention_backward_head(q, k, v, dO, 0.7, True, causal_offset=1)
+
+    def loss(q_, k_, v_):
+        O, _ = oracle.attention_head(q_, k_, v_, 0.7, True, causal_offset=1)
+        return float((O * dO).sum())
+
+    h = 1e-6
+    for (arr, grad) in ((q, dQ), (k, dK), (v, dV)):
+        for idx in [(0, 0), (2, 3), (4, 1)]:
+            if idx[0] >= arr.shape[0]:
+                continue
+            a, b = arr.copy(), arr.copy()
+            a[idx] += h
+            b[idx] -= h
+            args_a = [a if arr is x else x for x in (q, k, v)]
+            args_b = [b if arr is x else x for x in (q, k, v)]
+            fd = (loss(*args_a) - loss(*args_b)) / (2 * h)
+            assert abs(fd - grad[idx]) <= 1e-7, (idx, fd, grad[idx])
+
+
+def pin_backward_identities():
+    """D = rowsum(dO ∘ O); Σ_j dS_ij = 0 makes Σ_j dK-contributions vanish:
+    adding a constant vector to every key changes nothing, so the key
+    gradients sum to zero; the batched call matches the per-head one."""
+    q, k, v = rand_head(1950, 20, 30, 16, sigma=1.5)
+    dO = _rng(1951).standard_normal((20, 16))
+    for causal in (False, True):
+        dQ, dK, dV, D = oracle.attention_backward_head(q, k, v, dO, 0.25, causal)
+        O, _ = oracle.attention_head(q, k, v, 0.25, causal)
+        assert np.max(np.abs(D - (dO * O).sum(axis=1))) <= TOL
+        assert np.max(np.abs(dK.sum(axis=0))) <= 1e-10
+    r = _rng(1952)
+    qb, kb, vb, db = (_bf16_like(r.standard_normal((2, 11, 3, 8))) for _ in range(4))
+    dQ, dK, dV = oracle.attention_backward(qb, kb, vb, db, 0.35, True)
+    for b in range(2):
+        for h in range(3):
+            hq, hk, hv, _ = oracle.attention_backward_head(qb[b, :, h], kb[b, :, h], vb[b, :, h], db[b, :, h], 0.35,
+                                                           True)
+            assert np.array_equal(dQ[b, :, h], hq) and np.array_equal(dK[b, :, h], hk)
+            assert np.array_equal(dV[b, :, h], hv)
+
+
 ALL_PINS = [v for k_, v in sorted(globals().items()) if k_.startswith("pin_") and callable(v)]

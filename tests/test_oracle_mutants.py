@@ -42,6 +42,10 @@ MUTANTS = {
     "forward_drops_offset": ("                                                         causal_offset=causal_offset)",
                              "                                                         causal_offset=0)"),
     "rows_drop_offset": ("rows=rows, causal_offset=causal_offset)", "rows=rows)"),
+    "bwd_dv_untransposed": ("    dV = P.T @ dO", "    dV = P @ dO[:P.shape[1]] if P.shape[0] >= P.shape[1] else P.T @ dO * 0.5"),
+    "bwd_ds_drops_d": ("    dS = P * (dP - D[:, None])", "    dS = P * dP"),
+    "bwd_dk_unscaled": ("scale * (dS.T @ q), dV, D", "(dS.T @ q), dV, D"),
+    "bwd_dq_uses_v": ("return scale * (dS @ k), scale", "return scale * (dS @ v), scale"),
     "varlen_global_offset": ("        off = (k1 - k0) - (q1 - q0) if (causal and bottom_right) else 0",
                              "        off = (cu_k[-1] - cu_q[-1]) if (causal and bottom_right) else 0"),
     "varlen_keys_from_start": ("k[k0:k1, g, :], v[k0:k1, g, :], scale", "k[0:k1 - k0, g, :], v[0:k1 - k0, g, :], scale"),
@@ -65,8 +69,9 @@ def _load_mutant(old, new):
 @pytest.mark.parametrize("name", sorted(MUTANTS))
 def test_mutant_is_caught(name, monkeypatch):
     mod = _load_mutant(*MUTANTS[name])
-    for fn in ("attention_forward", "attention_head", "attention_rows", "attention_varlen", "head_probabilities",
-               "head_scores", "kv_head", "visible_mask", "combine_partials"):
+    for fn in ("attention_forward", "attention_head", "attention_rows", "attention_varlen", "attention_backward",
+               "attention_backward_head", "head_probabilities", "head_scores", "kv_head", "visible_mask",
+               "combine_partials"):
         monkeypatch.setattr(oracle, fn, getattr(mod, fn))
     caught = []
     for pin in oracle_pins.ALL_PINS:
