@@ -27,7 +27,7 @@ ERRORS = {
 # Every symbol the header declares (checked by the CPU test-suite).
 EXPORTS = ["attn_fwd", "attn_fwd_ex", "attn_fwd_host", "attn_fwd_host_workspace_size", "attn_get_status",
            "attn_strerror", "attn_last_cuda_error", "attn_version", "attn_fwd_host_static", "attn_fwd_layout",
-           "attn_fwd_varlen"]
+           "attn_fwd_varlen", "attn_bwd", "attn_bwd_workspace_size"]
 
 CAUSAL_ALIGN = {"top-left": 0, "bottom-right": 1}
 
@@ -86,6 +86,10 @@ def lib():
     L.attn_fwd_varlen.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f, i, i, ctypes.POINTER(Options),
                                   vp]
     L.attn_fwd_varlen.restype = i
+    L.attn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp, sz, vp]
+    L.attn_bwd.restype = i
+    L.attn_bwd_workspace_size.argtypes = [i, i, i]
+    L.attn_bwd_workspace_size.restype = sz
     L.attn_fwd_host.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp, sz, vp]
     L.attn_fwd_host.restype = i
     L.attn_fwd_host_workspace_size.argtypes = [i, i, i, i, i]
@@ -232,6 +236,42 @@ def attn_fwd_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int, caus
                                    _stream_handle(stream))
     _check(rc)
     return out, lse
+
+
+def attn_bwd(q, k, v, o, lse, dout, causal: bool = False, scale: float | None = None, dq=None, dk=None, dv=None,
+             workspace=None, stream=None):
+    """Gradients of attn_fwd's output: returns (dq, dk, dv), bf16, shaped
+    like q, k, v.  o and lse are what attn_fwd returned for the same inputs;
+    dout is the gradient of the loss with respect to o.  Dense (batch, seq,
+    heads, head_dim) tensors, one key/value head per query head, top-left
+    causal alignment."""
+    for name, t in (("q", q), ("k", k), ("v", v), ("o", o), ("dout", dout)):
+        if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous() or t.dim() != 4:
+            raise ValueError(f"{name} must be a contiguous 4-D bf16 CUDA tensor (batch, seq, heads, head_dim)")
+    B, Sq, H, d = q.shape
+    Sk = k.shape[1]
+    if k.shape != (B, Sk, H, d) or v.shape != k.shape or o.shape != q.shape or dout.shape != q.shape:
+        raise ValueError("shape mismatch (the backward takes one key/value head per query head)")
+    if lse.shape != (B, H, Sq) or lse.dtype != torch.float32 or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous fp32 tensor of shape (B, H, Sq)")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    for name, t, ref in (("dq", dq, q), ("dk", dk, k), ("dv", dv, v)):
+        if t.shape != ref.shape or t.dtype != torch.bfloat16 or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous bf16 tensor shaped like its input")
+    L = lib()
+    need = int(L.attn_bwd_workspace_size(B, H, Sq))
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    with torch.cuda.device(q.device):
+        rc = L.attn_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), dout.data_ptr(),
+                        dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, Sq, Sk, d, float(scale), int(bool(causal)),
+                        workspace.data_ptr(), workspace.numel() * workspace.element_size(), _stream_handle(stream))
+    _check(rc)
+    return dq, dk, dv
 
 
 TEST_WITHHOLD_KV = 1

@@ -10,6 +10,7 @@
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
+#include "attn_bwd_launch.h"
 #include "attn_gb300.h"
 #include "attn_launch.h"
 
@@ -388,6 +389,77 @@ int attn_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse
 int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Sq, int Sk, int d,
              float scale, int causal, cudaStream_t stream) {
   return attn_fwd_ex(q, k, v, o, lse, B, H, Sq, Sk, d, scale, causal, nullptr, stream);
+}
+
+size_t attn_bwd_workspace_size(int B, int H, int Sq) {
+  if (B < 1 || H < 1 || Sq < 1) return 0;
+  const size_t pitch = (static_cast<size_t>(Sq) + 127) / 128 * 128;
+  return (2 * static_cast<size_t>(B) * H * pitch * 4 + 255) & ~static_cast<size_t>(255);
+}
+
+int attn_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dout, void* dq,
+             void* dk, void* dv, int B, int H, int Sq, int Sk, int d, float scale, int causal, void* workspace,
+             size_t workspace_bytes, cudaStream_t stream) {
+  int rc = check_args(q, k, v, o, lse, B, H, Sq, Sk, d, scale);
+  if (rc != ATTN_OK) return rc;
+  if (dout == nullptr || dq == nullptr || dk == nullptr || dv == nullptr) return ATTN_ERR_NULL;
+  if (!aligned16(dout) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv)) return ATTN_ERR_ALIGN;
+  const long long n_kt = (static_cast<long long>(Sk) + 127) / 128;
+  if (static_cast<long long>(B) * H * n_kt > 0x7FFFFFFFLL) return ATTN_ERR_SHAPE;
+  if (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 ||
+      workspace_bytes < attn_bwd_workspace_size(B, H, Sq))
+    return ATTN_ERR_WORKSPACE;
+  int dev = -1;
+  if ((rc = current_device(&dev)) != ATTN_OK) return rc;
+
+  const int pitch = (Sq + 127) / 128 * 128;
+  float* lse2 = static_cast<float*>(workspace);
+  float* dvec = lse2 + static_cast<size_t>(B) * H * pitch;
+  cudaError_t e = attn::launch_bwd_prep(o, dout, lse, lse2, dvec, B, H, Sq, pitch, d, stream);
+  if (e != cudaSuccess) return fail_cuda(e, "backward preparation launch");
+
+  const long long hd = static_cast<long long>(H) * d;
+  const long long qs[3] = {Sq * hd, hd, d}, ks[3] = {Sk * hd, hd, d};
+  attn::BwdLaunchArgs a;
+  std::memset(&a, 0, sizeof(a));
+  a.p.lse2 = lse2;
+  a.p.dvec = dvec;
+  a.p.status = g_dev[dev].status;
+  a.p.B = B;
+  a.p.H = H;
+  a.p.Sq = Sq;
+  a.p.Sk = Sk;
+  a.p.pitch = pitch;
+  a.p.coff = 0;
+  a.p.scale_log2 = scale * 1.4426950408889634f;
+  a.p.scale = scale;
+  a.p.timeout_ns = static_cast<uint64_t>(kDefaultTimeoutMs) * 1000000ull;
+  a.causal = causal != 0;
+  a.device = dev;
+  a.stream = stream;
+  // dK, dV: rows are keys; the queries' Q and dO stream past them.
+  if ((rc = encode_bshd(&a.x, k, B, Sk, H, d, ks)) != ATTN_OK) return rc;
+  if ((rc = encode_bshd(&a.x2, v, B, Sk, H, d, ks)) != ATTN_OK) return rc;
+  if ((rc = encode_bshd(&a.a, q, B, Sq, H, d, qs)) != ATTN_OK) return rc;
+  if ((rc = encode_bshd(&a.b, dout, B, Sq, H, d, qs)) != ATTN_OK) return rc;
+  a.p.out0 = dv;
+  a.p.out1 = dk;
+  a.p.n_rt = static_cast<int>(n_kt);
+  a.grid = static_cast<int>(n_kt * B * H);
+  a.mode = 1;
+  if ((e = attn::launch_bwd(a, d)) != cudaSuccess) return fail_cuda(e, "backward dK/dV launch");
+  // dQ: rows are queries; K and V stream past them.
+  if ((rc = encode_bshd(&a.x, q, B, Sq, H, d, qs)) != ATTN_OK) return rc;
+  if ((rc = encode_bshd(&a.x2, dout, B, Sq, H, d, qs)) != ATTN_OK) return rc;
+  if ((rc = encode_bshd(&a.a, k, B, Sk, H, d, ks)) != ATTN_OK) return rc;
+  if ((rc = encode_bshd(&a.b, v, B, Sk, H, d, ks)) != ATTN_OK) return rc;
+  a.p.out0 = dq;
+  a.p.out1 = nullptr;
+  a.p.n_rt = (Sq + 127) / 128;
+  a.grid = a.p.n_rt * B * H;
+  a.mode = 0;
+  if ((e = attn::launch_bwd(a, d)) != cudaSuccess) return fail_cuda(e, "backward dQ launch");
+  return ATTN_OK;
 }
 
 size_t attn_fwd_host_workspace_size(int B, int H, int Sq, int Sk, int d) {

@@ -1,0 +1,54 @@
+// Attention backward kernels: instantiations and launches (both head dims,
+// both masks, both passes) and the preparation kernel.
+#include "attn_bwd_launch.h"
+
+#include "attn_bwd_kernel.cuh"
+
+namespace attn {
+namespace {
+
+template <int D, bool CAUSAL, int MODE>
+cudaError_t launch_bwd_one(const BwdLaunchArgs& a) {
+  constexpr unsigned int smem = BwdLayout<D, MODE>::kSmemBytes;
+  static volatile bool configured[64] = {};
+  if (a.device < 0 || a.device >= 64) return cudaErrorInvalidDevice;
+  if (!configured[a.device]) {
+    const cudaError_t e =
+        cudaFuncSetAttribute(attn_bwd_kernel<D, CAUSAL, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    configured[a.device] = true;
+  }
+  attn_bwd_kernel<D, CAUSAL, MODE><<<a.grid, kBwdThreads, smem, a.stream>>>(a.x, a.x2, a.a, a.b, a.p);
+  return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t launch_bwd_d(const BwdLaunchArgs& a) {
+  if (a.mode == kModeDQ)
+    return a.causal ? launch_bwd_one<D, true, kModeDQ>(a) : launch_bwd_one<D, false, kModeDQ>(a);
+  return a.causal ? launch_bwd_one<D, true, kModeDKV>(a) : launch_bwd_one<D, false, kModeDKV>(a);
+}
+
+}  // namespace
+
+cudaError_t launch_bwd(const BwdLaunchArgs& a, int d) {
+  if (d == 64) return launch_bwd_d<64>(a);
+  if (d == 128) return launch_bwd_d<128>(a);
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_bwd_prep(const void* o, const void* dout, const float* lse, float* lse2, float* dvec, int B, int H,
+                            int Sq, int pitch, int d, cudaStream_t stream) {
+  const long long n = static_cast<long long>(B) * H * pitch;
+  const int threads = 256;
+  const int blocks = static_cast<int>(n / threads + 1 < 8192 ? n / threads + 1 : 8192);
+  const uint16_t* o16 = static_cast<const uint16_t*>(o);
+  const uint16_t* g16 = static_cast<const uint16_t*>(dout);
+  if (d == 64)
+    attn_bwd_prep_kernel<64><<<blocks, threads, 0, stream>>>(o16, g16, lse, lse2, dvec, B, H, Sq, pitch);
+  else
+    attn_bwd_prep_kernel<128><<<blocks, threads, 0, stream>>>(o16, g16, lse, lse2, dvec, B, H, Sq, pitch);
+  return cudaGetLastError();
+}
+
+}  // namespace attn

@@ -1,0 +1,392 @@
+// Exact attention backward kernels for sm_103a (GB300).
+//
+// Gradients of O = softmax(scale·QKᵀ)V for a loss with dL/dO = dO, from the
+// forward's O and LSE: with P = exp(scale·QKᵀ − LSE) over visible keys,
+//   dV = Pᵀ dO,  dP = dO Vᵀ,  D = rowsum(dO ∘ O),  dS = P ∘ (dP − D),
+//   dQ = scale · dS K,  dK = scale · dSᵀ Q.
+// (The pages give no backward formulas; "FlashAttention-4 no Blackwell B200
+// …", section "Redução de tráfego no backward", says FA4 keeps the backward's
+// intermediates in tensor memory.  These kernels do that too: S, dP, P, dS and
+// the accumulators live in TMEM, and P / dS feed the MMAs from there.)
+//
+// One kernel template serves both passes; a CTA owns one tile of 128 rows of
+// one (batch, head) and walks the blocks of 128 columns that the rows see:
+//   DQ  rows = queries (X = Q, X2 = dO), columns = keys  (A = K, B = V):
+//       S = Q Kᵀ, dP = dO Vᵀ, P and dS per (query, key), dQ += dS K.
+//   DKV rows = keys (X = K, X2 = V), columns = queries (A = Q, B = dO):
+//       Sᵀ = K Qᵀ, dPᵀ = V dOᵀ, Pᵀ and dSᵀ per (key, query),
+//       dV += Pᵀ dO, dK += dSᵀ Q.
+// In both, S = X·Aᵀ and dP = X2·Bᵀ are K-major products like the forward's
+// Q·Kᵀ, and every accumulation is TMEM operand × MN-major shared-memory
+// operand like the forward's P·V.  No atomics: dQ and dK/dV are separate
+// passes.
+//
+// Warp roles (320 threads): warps 0-7 turn S, dP into P, dS (warpgroup h owns
+// columns [64h, 64h+64) of each block; one thread per row) and write the
+// tile's outputs; warp 8 loads X, X2 once and streams (A, B) blocks — plus, in
+// DKV, the 128 log2-LSE and D values of the block's queries — through a ring;
+// warp 9 issues the MMAs.  S and dP are single-buffered: the next block's
+// products wait until the accumulations that read P and dS from them are done.
+//
+// TMEM columns: S [0, 128), dP [128, 256), acc0 [256, 256+D) (dQ or dV),
+// acc1 [256+D, 256+2D) (dK).  P (bf16 pairs) overwrites S's columns and dS
+// overwrites dP's, in the packed layout the forward uses for P.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+
+#include "attn_bwd_launch.h"
+#include "attn_device.cuh"
+
+namespace attn {
+
+constexpr int kBwdThreads = 320;
+constexpr int kBwdLoaderWarp = 8;
+constexpr int kBwdMmaWarp = 9;
+constexpr int kModeDQ = 0;
+constexpr int kModeDKV = 1;
+
+
+template <int D, int MODE>
+struct BwdLayout {
+  static_assert(D == 64 || D == 128, "head dim");
+  static constexpr int kSlabs = D / 64;
+  static constexpr uint32_t kSlabBytes = 128 * 128;
+  static constexpr uint32_t kTileBytes = kSlabBytes * kSlabs;
+  static constexpr int kStages = (D == 128) ? 2 : 3;
+  static constexpr uint32_t kVecBytes = (MODE == kModeDKV) ? 2 * 128 * 4 : 0;  // log2-LSE and D of 128 queries
+  static constexpr uint32_t kSlotBytes = 2 * kTileBytes + ((kVecBytes + 1023) / 1024) * 1024;
+  static constexpr uint32_t kXOff = 0;                       // X, X2
+  static constexpr uint32_t kRingOff = 2 * kTileBytes;
+  static constexpr uint32_t kBarOff = kRingOff + kStages * kSlotBytes;
+  // barriers: fix_full, ring_full[S], ring_empty[S], s_full, p_full, acc_done, done
+  static constexpr int kNumBars = 1 + 2 * kStages + 4;
+  static constexpr uint32_t kMiscOff = kBarOff + 8 * kNumBars;
+  static constexpr uint32_t kSmemBytes = kMiscOff + 16 + 1024;
+};
+
+template <int D, bool CAUSAL, int MODE>
+__global__ void __launch_bounds__(kBwdThreads, 1)
+    attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_x2,
+                    const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
+                    const BwdParams p) {
+  using L = BwdLayout<D, MODE>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* const smem = smem_raw + (base - raw);
+  const uint32_t sX = base + L::kXOff;
+  const uint32_t sRing = base + L::kRingOff;
+  const uint32_t bars = base + L::kBarOff;
+  const uint32_t bar_fix = bars;
+  auto bar_ring_full = [&](int s) { return bars + 8u * (1 + s); };
+  auto bar_ring_empty = [&](int s) { return bars + 8u * (1 + L::kStages + s); };
+  const uint32_t bar_s_full = bars + 8u * (1 + 2 * L::kStages);
+  const uint32_t bar_p_full = bar_s_full + 8u;
+  const uint32_t bar_acc_done = bar_s_full + 16u;
+  const uint32_t bar_done = bar_s_full + 24u;
+  uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMiscOff);
+  volatile uint32_t* const abort_flag = reinterpret_cast<volatile uint32_t*>(smem + L::kMiscOff + 4);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  // ---- the tile and the blocks of 128 columns its rows see
+  const int rt = blockIdx.x % p.n_rt;
+  const int bh = blockIdx.x / p.n_rt;
+  const int b = bh / p.H, h = bh % p.H;
+  const int r0 = rt * 128;
+  const int n_q = (p.Sq + 127) / 128, n_k = (p.Sk + 127) / 128;
+  int c_first, c_end;  // column blocks [c_first, c_end)
+  if (MODE == kModeDQ) {
+    c_first = 0;
+    c_end = CAUSAL ? min(n_k, (min(r0 + 128, p.Sq) - 1 + p.coff) / 128 + 1) : n_k;
+  } else {
+    // Queries i see key j iff j ≤ i + coff: the tile's first key r0 is first
+    // seen by query r0 − coff.
+    c_first = CAUSAL ? max(0, (r0 - p.coff) / 128) : 0;
+    if (CAUSAL && r0 - p.coff < 0) c_first = 0;
+    c_end = n_q;
+  }
+  const int nblk = max(0, c_end - c_first);
+
+  if (warp == kBwdLoaderWarp) {
+    tmem_alloc(smem_u32(tmem_slot), 512);
+    tmem_relinquish();
+    tc_fence_before();
+  }
+  if (threadIdx.x == 0) {
+    *abort_flag = 0u;
+    mbar_init(bar_fix, 1);
+    for (int s = 0; s < L::kStages; ++s) {
+      mbar_init(bar_ring_full(s), 1);
+      mbar_init(bar_ring_empty(s), 1);
+    }
+    mbar_init(bar_s_full, 1);
+    mbar_init(bar_p_full, 8);  // one arrival per softmax-gradient warp
+    mbar_init(bar_acc_done, 1);
+    mbar_init(bar_done, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    fence_proxy_async_smem();
+  }
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const WaitCtx wc{abort_flag, p.status, p.timeout_ns};
+  const uint32_t tS = tmem, tdP = tmem + 128, tAcc0 = tmem + 256, tAcc1 = tmem + 256 + D;
+
+  if (warp == kBwdLoaderWarp) {
+    // ============================================================ loader
+    if (lane == 0 && nblk > 0) {
+      mbar_arrive_expect_tx(bar_fix, 2 * L::kTileBytes);
+      for (int s = 0; s < L::kSlabs; ++s) {
+        tma_load_4d(sX + s * L::kSlabBytes, &tm_x, 64 * s, h, r0, b, bar_fix);
+        tma_load_4d(sX + L::kTileBytes + s * L::kSlabBytes, &tm_x2, 64 * s, h, r0, b, bar_fix);
+      }
+      int n = 0;
+      for (; n < nblk; ++n) {
+        const int slot = n % L::kStages;
+        if (!wait_bar(bar_ring_empty(slot), ((n / L::kStages) & 1) ^ 1u, wc)) break;
+        const uint32_t dst = sRing + slot * L::kSlotBytes;
+        const int c0 = (c_first + n) * 128;
+        mbar_arrive_expect_tx(bar_ring_full(slot), 2 * L::kTileBytes + L::kVecBytes);
+        for (int s = 0; s < L::kSlabs; ++s) {
+          tma_load_4d(dst + s * L::kSlabBytes, &tm_a, 64 * s, h, c0, b, bar_ring_full(slot));
+          tma_load_4d(dst + L::kTileBytes + s * L::kSlabBytes, &tm_b, 64 * s, h, c0, b, bar_ring_full(slot));
+        }
+        if (MODE == kModeDKV) {
+          const size_t row = static_cast<size_t>(bh) * p.pitch + c0;
+          bulk_load(dst + 2 * L::kTileBytes, p.lse2 + row, 512, bar_ring_full(slot));
+          bulk_load(dst + 2 * L::kTileBytes + 512, p.dvec + row, 512, bar_ring_full(slot));
+        }
+      }
+      // Let the copies in flight land before the CTA can exit.
+      const uint64_t t0 = globaltimer_ns();
+      while (!mbar_try_wait(bar_fix, 0))
+        if (globaltimer_ns() - t0 > p.timeout_ns) break;
+      for (int m = (n > L::kStages ? n - L::kStages : 0); m < n; ++m)
+        while (!mbar_try_wait(bar_ring_full(m % L::kStages), (m / L::kStages) & 1u))
+          if (globaltimer_ns() - t0 > p.timeout_ns) break;
+    }
+  } else if (warp == kBwdMmaWarp) {
+    // ======================================================== MMA issuer
+    if (lane == 0 && nblk > 0) {
+      constexpr uint32_t idS = idesc_bf16(128, 128, false);
+      constexpr uint32_t idAcc = idesc_bf16(128, D, true);
+      const uint64_t dX = sdesc_kmajor_sw128(sX);
+      const uint64_t dX2 = sdesc_kmajor_sw128(sX + L::kTileBytes);
+      bool ok = wait_bar(bar_fix, 0, wc);
+      for (int n = 0; n < nblk && ok; ++n) {
+        const int slot = n % L::kStages;
+        const uint32_t sA = sRing + slot * L::kSlotBytes, sB = sA + L::kTileBytes;
+        if (!wait_bar(bar_ring_full(slot), (n / L::kStages) & 1, wc)) { ok = false; break; }
+        // S and dP overwrite P and dS of the previous block: its accumulations
+        // must have completed.
+        if (n > 0 && !wait_bar(bar_acc_done, (n - 1) & 1, wc)) { ok = false; break; }
+        tc_fence_after();
+        const uint64_t dA = sdesc_kmajor_sw128(sA), dB = sdesc_kmajor_sw128(sB);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = ((kk / 4) * L::kSlabBytes + (kk % 4) * 32) >> 4;
+          mma_ss(tS, dX + off, dA + off, idS, kk > 0 ? 1u : 0u);
+        }
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = ((kk / 4) * L::kSlabBytes + (kk % 4) * 32) >> 4;
+          mma_ss(tdP, dX2 + off, dB + off, idS, kk > 0 ? 1u : 0u);
+        }
+        mma_commit(bar_s_full);
+        if (!wait_bar(bar_p_full, n & 1, wc)) { ok = false; break; }
+        tc_fence_after();
+        const uint64_t dAm = sdesc_mnmajor_sw128(sA, L::kSlabBytes), dBm = sdesc_mnmajor_sw128(sB, L::kSlabBytes);
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            const uint32_t acc = (n > 0 || hh > 0 || kk > 0) ? 1u : 0u;
+            const uint32_t rows = ((4 * hh + kk) * 2048) >> 4;  // 16 columns of the block per step
+            if (MODE == kModeDQ) {
+              mma_ts(tAcc0, tdP + 64 * hh + 8 * kk, dAm + rows, idAcc, acc);      // dQ += dS K
+            } else {
+              mma_ts(tAcc0, tS + 64 * hh + 8 * kk, dBm + rows, idAcc, acc);       // dV += Pᵀ dO
+              mma_ts(tAcc1, tdP + 64 * hh + 8 * kk, dAm + rows, idAcc, acc);      // dK += dSᵀ Q
+            }
+          }
+        }
+        mma_commit(bar_acc_done);
+        mma_commit(bar_ring_empty(slot));
+      }
+      // Every MMA must finish before the accumulators are read or TMEM freed.
+      mma_commit(bar_done);
+      const uint64_t t0 = globaltimer_ns();
+      while (!mbar_try_wait(bar_done, 0))
+        if (globaltimer_ns() - t0 > p.timeout_ns) break;
+    }
+  } else {
+    // ============================================ softmax gradient, output
+    const int hh = warp >> 2;          // column half
+    const int r = threadIdx.x & 127;   // row of the tile = TMEM lane
+    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const int row = r0 + r;            // DQ: query; DKV: key
+    float lse2_row = 0.f, d_row = 0.f;
+    if (MODE == kModeDQ) {
+      lse2_row = p.lse2[static_cast<size_t>(bh) * p.pitch + row];  // row < n_rt·128 = pitch
+      d_row = p.dvec[static_cast<size_t>(bh) * p.pitch + row];
+    }
+    const float sc = p.scale_log2;
+    bool ok = true;
+    for (int n = 0; n < nblk && ok; ++n) {
+      const bool got = wait_bar(bar_s_full, n & 1, wc);
+      if (__any_sync(0xffffffffu, !got)) { ok = false; break; }
+      tc_fence_after();
+      const int c0 = (c_first + n) * 128;
+      const float* vec = reinterpret_cast<const float*>(smem + L::kRingOff + (n % L::kStages) * L::kSlotBytes +
+                                                        2 * L::kTileBytes);
+      if (MODE == kModeDKV) {
+        // The block's log2-LSE and D arrived with its ring slot (which stays
+        // loaded until this block's P is released).
+        const bool in = wait_bar(bar_ring_full(n % L::kStages), (n / L::kStages) & 1, wc);
+        if (__any_sync(0xffffffffu, !in)) { ok = false; break; }
+      }
+      // Does any element of this thread's half-block need a mask?
+      bool edge;
+      if (MODE == kModeDQ) {
+        edge = c0 + 64 * hh + 64 > p.Sk || (CAUSAL && c0 + 64 * hh + 63 > r0 + p.coff);
+      } else {
+        edge = CAUSAL && r0 + 127 > c0 + 64 * hh + p.coff;
+      }
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        const int col0 = 64 * hh + 32 * c;
+        uint32_t us[32], ud[32];
+        tmem_ld32(tS + col0 + lane_off, us);
+        tmem_ld32(tdP + col0 + lane_off, ud);
+        tmem_wait_ld();
+        reg_fence32(us);
+        reg_fence32(ud);
+        uint32_t pk[16], qk[16];
+#pragma unroll
+        for (int e = 0; e < 32; e += 2) {
+          float lse_a, lse_b, dv_a, dv_b;
+          if (MODE == kModeDQ) {
+            lse_a = lse_b = lse2_row;
+            dv_a = dv_b = d_row;
+          } else {
+            lse_a = vec[col0 + e];
+            lse_b = vec[col0 + e + 1];
+            dv_a = vec[128 + col0 + e];
+            dv_b = vec[128 + col0 + e + 1];
+          }
+          float pa = ex2_mufu(__uint_as_float(us[e]) * sc - lse_a);
+          float pb = ex2_mufu(__uint_as_float(us[e + 1]) * sc - lse_b);
+          if (edge) {
+            const int ca = c0 + col0 + e, cb = ca + 1;  // global column: DQ key, DKV query
+            if (MODE == kModeDQ) {
+              if (ca >= p.Sk || (CAUSAL && ca > row + p.coff)) pa = 0.f;
+              if (cb >= p.Sk || (CAUSAL && cb > row + p.coff)) pb = 0.f;
+            } else {
+              if (CAUSAL && row > ca + p.coff) pa = 0.f;
+              if (CAUSAL && row > cb + p.coff) pb = 0.f;
+            }
+          }
+          const float sa = pa * (__uint_as_float(ud[e]) - dv_a);
+          const float sb = pb * (__uint_as_float(ud[e + 1]) - dv_b);
+          pk[e / 2] = pack_bf16x2(pa, pb);
+          qk[e / 2] = pack_bf16x2(sa, sb);
+        }
+        // Packed bf16 pairs over the columns this thread has already read.
+        tmem_st16(tS + 64 * hh + 16 * c + lane_off, pk);
+        tmem_st16(tdP + 64 * hh + 16 * c + lane_off, qk);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_p_full);
+    }
+    // ------------------------------------------------------------ outputs
+    // Warpgroup hh writes columns [hh·D/2, (hh+1)·D/2) of its rows.
+    bool have = nblk > 0 && ok;
+    if (have) {
+      const bool fin = wait_bar(bar_acc_done, (nblk - 1) & 1, wc);
+      if (__any_sync(0xffffffffu, !fin)) have = false;
+      tc_fence_after();
+    }
+    const int rows_total = (MODE == kModeDQ) ? p.Sq : p.Sk;
+    for (int o = 0; o < (MODE == kModeDQ ? 1 : 2) && (ok || nblk == 0); ++o) {
+      const uint32_t tacc = (o == 0 ? tAcc0 : tAcc1) + lane_off + hh * (D / 2);
+      const float mul = (MODE == kModeDQ || o == 1) ? p.scale : 1.f;
+      uint16_t* const out = static_cast<uint16_t*>(o == 0 ? p.out0 : p.out1) +
+                            ((static_cast<size_t>(b) * rows_total + row) * p.H + h) * D + hh * (D / 2);
+#pragma unroll
+      for (int c = 0; c < D / 64; ++c) {
+        uint32_t x[32];
+        if (have) {
+          tmem_ld32(tacc + 32 * c, x);
+          tmem_wait_ld();
+          reg_fence32(x);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) x[i] = 0u;  // rows that see no column: zero gradient
+        }
+        if (row < rows_total) {
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            uint4 w;
+            w.x = pack_bf16x2(mul * __uint_as_float(x[8 * q]), mul * __uint_as_float(x[8 * q + 1]));
+            w.y = pack_bf16x2(mul * __uint_as_float(x[8 * q + 2]), mul * __uint_as_float(x[8 * q + 3]));
+            w.z = pack_bf16x2(mul * __uint_as_float(x[8 * q + 4]), mul * __uint_as_float(x[8 * q + 5]));
+            w.w = pack_bf16x2(mul * __uint_as_float(x[8 * q + 6]), mul * __uint_as_float(x[8 * q + 7]));
+            *reinterpret_cast<uint4*>(out + 32 * c + 8 * q) = w;
+          }
+        }
+      }
+    }
+  }
+
+  // ---- tear-down
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kBwdLoaderWarp) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// D = rowsum(dO ∘ O) and LSE · log2(e) per query row, in [B·H, pitch] arrays
+// padded to whole 128-row blocks (+inf and 0 beyond Sq, so padded queries get
+// P = 0).  One thread per (batch, head, row).
+template <int D>
+__global__ void attn_bwd_prep_kernel(const uint16_t* o, const uint16_t* dout, const float* lse, float* lse2,
+                                     float* dvec, int B, int H, int Sq, int pitch) {
+  const long long n = static_cast<long long>(B) * H * pitch;
+  for (long long t = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; t < n;
+       t += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const int i = static_cast<int>(t % pitch);
+    const long long bh = t / pitch;
+    const int b = static_cast<int>(bh / H), h = static_cast<int>(bh % H);
+    if (i >= Sq) {
+      lse2[t] = INFINITY;
+      dvec[t] = 0.f;
+      continue;
+    }
+    const size_t off = ((static_cast<size_t>(b) * Sq + i) * H + h) * D;
+    const uint4* a = reinterpret_cast<const uint4*>(o + off);
+    const uint4* g = reinterpret_cast<const uint4*>(dout + off);
+    float acc = 0.f;
+#pragma unroll 4
+    for (int c = 0; c < D / 8; ++c) {
+      const uint4 x = a[c], y = g[c];
+      const uint32_t xs[4] = {x.x, x.y, x.z, x.w}, ys[4] = {y.x, y.y, y.z, y.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        acc = fmaf(__uint_as_float(xs[e] << 16), __uint_as_float(ys[e] << 16), acc);
+        acc = fmaf(__uint_as_float(xs[e] & 0xFFFF0000u), __uint_as_float(ys[e] & 0xFFFF0000u), acc);
+      }
+    }
+    dvec[t] = acc;
+    lse2[t] = lse[(static_cast<size_t>(b) * H + h) * Sq + i] * 1.4426950408889634f;
+  }
+}
+
+}  // namespace attn

@@ -1,0 +1,40 @@
+// Internal interface between the C-ABI host code (attn_api.cu) and the
+// backward kernels' translation unit (attn_bwd.cu).
+#pragma once
+
+#include <cstdint>
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace attn {
+
+struct BwdParams {
+  void* out0;          // dQ pass: dQ [B, Sq, H, D]; dK/dV pass: dV [B, Sk, H, D]   (bf16, dense)
+  void* out1;          // dK/dV pass: dK [B, Sk, H, D]
+  const float* lse2;   // [B·H, pitch]: LSE · log2(e) of each query row; +inf beyond Sq
+  const float* dvec;   // [B·H, pitch]: D = rowsum(dO ∘ O); 0 beyond Sq
+  unsigned int* status;
+  int B, H, Sq, Sk, pitch;
+  int coff;            // causal: key j visible to query i iff j ≤ i + coff (≥ 0)
+  int n_rt;            // row tiles per (batch, head)
+  float scale_log2;    // scale · log2(e)
+  float scale;
+  uint64_t timeout_ns;
+};
+
+struct BwdLaunchArgs {
+  CUtensorMap x, x2, a, b;  // row tiles X, X2 and the streamed A, B (4-D maps as in the forward)
+  BwdParams p;
+  int grid;
+  int mode;                 // 0: dQ pass, 1: dK/dV pass
+  bool causal;
+  int device;
+  cudaStream_t stream;
+};
+
+cudaError_t launch_bwd(const BwdLaunchArgs& a, int d);
+cudaError_t launch_bwd_prep(const void* o, const void* dout, const float* lse, float* lse2, float* dvec, int B, int H,
+                            int Sq, int pitch, int d, cudaStream_t stream);
+
+}  // namespace attn

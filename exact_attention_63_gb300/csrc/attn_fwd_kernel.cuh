@@ -146,12 +146,6 @@ struct Layout {
   }
 };
 
-__device__ __forceinline__ void reg_fence32(uint32_t (&r)[32]) {
-#pragma unroll
-  for (int i = 0; i < 32; i += 8)
-    asm volatile("" : "+r"(r[i]), "+r"(r[i + 1]), "+r"(r[i + 2]), "+r"(r[i + 3]), "+r"(r[i + 4]),
-                 "+r"(r[i + 5]), "+r"(r[i + 6]), "+r"(r[i + 7]));
-}
 
 // One arrival for the whole warp: the lanes' earlier shared-memory writes (and,
 // after tcgen05.wait + fence::before_thread_sync, their tensor-memory stores)

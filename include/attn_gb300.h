@@ -217,6 +217,34 @@ int attn_fwd_varlen(const void* q, const void* k, const void* v, void* o, float*
                     const attn_options* opts, cudaStream_t stream);
 
 /*
+ * attn_bwd — gradients of attn_fwd's O with respect to q, k and v.
+ *   The pages give no backward formulas ("FlashAttention-4 no Blackwell B200
+ *   …", section "Redução de tráfego no backward", only says FA4 keeps the
+ *   backward's intermediates in tensor memory); this is the derivative of the
+ *   definition above for a loss whose gradient with respect to O is dout (the
+ *   LSE output is not differentiated).  With P_ij = exp(s_ij − LSE_i) over
+ *   visible keys:  dV = Pᵀ·dout,  dP = dout·Vᵀ,  D_i = Σ_c dout_ic·o_ic,
+ *   dS = P ∘ (dP − D),  dQ = scale·dS·K,  dK = scale·dSᵀ·Q.
+ *   q, k, v, o, dout : device, bf16, dense, layouts as attn_fwd (o and lse as
+ *                      attn_fwd returned them for the same q, k, v, scale,
+ *                      causal).  Read only.
+ *   dq, dk, dv       : device, bf16, shaped like q, k, v (written).
+ *   B, H, Sq, Sk, d, scale, causal : as attn_fwd (top-left causal alignment;
+ *                      K and V have H heads).
+ *   workspace        : caller-owned DEVICE buffer of at least
+ *                      attn_bwd_workspace_size(B, H, Sq) bytes, 256-byte
+ *                      aligned (holds D and LSE·log2 e per query row).
+ * Arithmetic: bf16 operands, fp32 accumulation in tensor memory, P and dS
+ * rounded to bf16 for the products, outputs rounded once to bf16.
+ * Enqueues three kernels on `stream` (D and LSE·log2 e, then dK/dV, then dQ)
+ * and returns; errors as attn_fwd, plus ATTN_ERR_WORKSPACE.
+ */
+size_t attn_bwd_workspace_size(int B, int H, int Sq);
+int attn_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dout,
+             void* dq, void* dk, void* dv, int B, int H, int Sq, int Sk, int d, float scale, int causal,
+             void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/*
  * attn_fwd_host — the same operation on HOST buffers, end to end.
  *   q_h, k_h, v_h : host bf16 inputs (layouts above); o_h, lse_h : host outputs.
  *   workspace     : caller-owned DEVICE buffer of at least

@@ -1,0 +1,76 @@
+"""Backward pass (attn_bwd): GPU gradients vs the CPU oracle's, element by
+element."""
+
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from exact_attention_63_gb300 import attn, inputs
+from gpu_common import f64, need_gpu
+
+pytestmark = pytest.mark.gpu
+
+# Gradient tolerance (the parity bar of the forward covers O and LSE only):
+# every element within 1e-2 of the tensor's largest |value| plus 1e-2 of its
+# own |value|.  Sources of error: P and dS rounded to bf16 before their
+# products (2^-9 relative per term), D from the bf16 O, outputs rounded once
+# to bf16 (2^-9 relative).
+G_ATOL, G_RTOL = 1e-2, 1e-2
+
+C = inputs.custom
+CASES = [
+    C(1, 2, 256, 256, 64, False, seed=101),
+    C(1, 2, 300, 300, 128, True, seed=102),
+    C(2, 3, 129, 200, 64, False, seed=103),
+    C(1, 2, 64, 500, 128, True, seed=104),
+    C(1, 2, 500, 64, 64, True, seed=105),
+    C(1, 1, 1000, 1000, 128, True, seed=106),
+    C(1, 2, 640, 640, 64, False, sigma_qk=3.0, seed=107),
+]
+
+
+def grads(w, q, k, v, dout):
+    dev = torch.device("cuda:0")
+    qd, kd, vd, gd = (t.to(dev) for t in (q, k, v, dout))
+    o, lse = attn.attn_fwd(qd, kd, vd, causal=w.causal, scale=w.scale)
+    dq, dk, dv = attn.attn_bwd(qd, kd, vd, o, lse, gd, causal=w.causal, scale=w.scale)
+    torch.cuda.synchronize()
+    assert attn.get_status() == 0
+    return dq, dk, dv
+
+
+def check(name, got, ref, what):
+    g = f64(got)
+    assert np.all(np.isfinite(g)), f"{what} {name}: non-finite"
+    bound = G_ATOL * np.abs(ref).max() + G_RTOL * np.abs(ref)
+    excess = np.abs(g - ref) - bound
+    assert (excess <= 0).all(), (f"{what} {name}: {(excess > 0).sum()} elements out of tolerance, "
+                                 f"max |err| {np.abs(g - ref).max():.3e} (max |ref| {np.abs(ref).max():.3e})")
+
+
+@pytest.mark.parametrize("w", CASES, ids=lambda w: w.name)
+def test_backward_matches_oracle(w):
+    need_gpu()
+    q, k, v = inputs.make_inputs(w)
+    g = torch.Generator().manual_seed(w.seed + 1000)
+    dout = torch.randn(q.shape, generator=g).to(torch.bfloat16)
+    dq, dk, dv = grads(w, q, k, v, dout)
+    rq, rk, rv = oracle.attention_backward(q, k, v, dout, w.scale, w.causal)
+    check("dq", dq, rq, w.name)
+    check("dk", dk, rk, w.name)
+    check("dv", dv, rv, w.name)
+
+
+def test_backward_deterministic():
+    need_gpu()
+    w = C(2, 4, 520, 520, 128, True, seed=108)
+    q, k, v = (t.cuda() for t in inputs.make_inputs(w))
+    dout = torch.randn(q.shape, generator=torch.Generator().manual_seed(5)).to(torch.bfloat16).cuda()
+    o, lse = attn.attn_fwd(q, k, v, causal=True)
+    a = attn.attn_bwd(q, k, v, o, lse, dout, causal=True)
+    b_ = attn.attn_bwd(q, k, v, o, lse, dout, causal=True)
+    torch.cuda.synchronize()
+    assert all(torch.equal(x, y) for x, y in zip(a, b_))
