@@ -231,6 +231,9 @@ def main():
     ap.add_argument("--diag", action="store_true", help="report the rescale rate of one extra launch")
     ap.add_argument("--kv-heads", type=int, default=0,
                     help="grouped-query variant of the workload: K/V heads (H must be a multiple); 0 = H")
+    ap.add_argument("--backward", action="store_true",
+                    help="time the backward pass (dQ, dK, dV) instead; FLOPs counted as 2.5x the forward's "
+                         "(the five products S, dP, dV, dK, dQ), halved when causal")
     ap.add_argument("--varlen", type=int, default=0,
                     help="packed-sequence variant: this many sequences with a seeded mix of lengths up to the "
                          "workload's S (same H, d, mask); FLOPs counted per sequence")
@@ -243,6 +246,8 @@ def main():
     from exact_attention_63_gb300 import inputs
 
     w = inputs.WORKLOADS[args.config]
+    if args.backward and (args.kv_heads or args.varlen or args.causal_align != "top-left"):
+        ap.error("--backward takes the plain workloads")
     if args.kv_heads or args.causal_align != "top-left" or args.varlen:
         import dataclasses
 
@@ -307,6 +312,18 @@ def main():
             attn.attn_fwd(qd, kd, vd, causal=w.causal, scale=w.scale, out=od, lse=ld, options=opts,
                           causal_align=w.causal_align)
 
+        if args.backward:
+            step()  # O and LSE for the backward
+            gen = torch.Generator().manual_seed(seed + 7)
+            gd = torch.randn(q.shape, generator=gen).to(torch.bfloat16).to(dev)
+            dqd, dkd, dvd = torch.empty_like(qd), torch.empty_like(kd), torch.empty_like(vd)
+            wsd = torch.empty(attn.lib().attn_bwd_workspace_size(w.B, w.H, w.Sq), dtype=torch.uint8, device=dev)
+
+            def step():
+                attn.attn_bwd(qd, kd, vd, od, ld, gd, causal=w.causal, scale=w.scale, dq=dqd, dk=dkd, dv=dvd,
+                              workspace=wsd)
+            args.no_e2e = True
+
     for _ in range(args.warmup):
         flush.zero_()
         step()
@@ -330,6 +347,8 @@ def main():
     total_ms = adist.max_over_ranks(sum(times_ms), device=dev)
     ms_per_step = total_ms / args.steps
     flops = varlen_flops if lens is not None else w.flops
+    if args.backward:
+        flops *= 2.5
     value = flops * world * args.steps / (total_ms * 1e-3) / 1e12
     achieved = flops / (statistics.mean(times_ms) * 1e-3) / 1e12
 
@@ -391,7 +410,7 @@ def main():
         "vs_baseline": None,
         "dtype": "bf16",
         "data": "synthetic",
-        "config": {"workload": w.name, "B": w.B, "H": w.H, "H_kv": w.kv_heads, "Sq": w.Sq, "Sk": w.Sk, "d": w.d,
+        "config": {"workload": w.name + ("_backward" if args.backward else ""), "B": w.B, "H": w.H, "H_kv": w.kv_heads, "Sq": w.Sq, "Sk": w.Sk, "d": w.d,
                    "causal": w.causal, "causal_align": w.causal_align, "sigma_qk": w.sigma_qk, "seed": w.seed,
                    **({"varlen_lengths": lens} if lens is not None else {}),
                    "l2": "flushed between timed steps (256 MiB write)",
@@ -402,7 +421,7 @@ def main():
                      "frac_of_contract_2250": achieved / CONTRACT_PEAK_TFLOPS},
         "cpu_baseline": cpu,
         "e2e": e2e,
-        "gpu_launches": args.steps,
+        "gpu_launches": args.steps * (3 if args.backward else 1),
         "clocks": clk.summary(),
     }
     if diag is not None:
