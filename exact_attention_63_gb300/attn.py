@@ -27,7 +27,7 @@ ERRORS = {
 # Every symbol the header declares (checked by the CPU test-suite).
 EXPORTS = ["attn_fwd", "attn_fwd_ex", "attn_fwd_host", "attn_fwd_host_workspace_size", "attn_get_status",
            "attn_strerror", "attn_last_cuda_error", "attn_version", "attn_fwd_host_static", "attn_fwd_layout",
-           "attn_fwd_varlen", "attn_bwd", "attn_bwd_workspace_size"]
+           "attn_fwd_varlen", "attn_bwd", "attn_bwd_workspace_size", "attn_bwd_layout"]
 
 CAUSAL_ALIGN = {"top-left": 0, "bottom-right": 1}
 
@@ -88,6 +88,9 @@ def lib():
     L.attn_fwd_varlen.restype = i
     L.attn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp, sz, vp]
     L.attn_bwd.restype = i
+    L.attn_bwd_layout.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, i, ctypes.POINTER(Layout), vp,
+                                  sz, vp]
+    L.attn_bwd_layout.restype = i
     L.attn_bwd_workspace_size.argtypes = [i, i, i]
     L.attn_bwd_workspace_size.restype = sz
     L.attn_fwd_host.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp, sz, vp]
@@ -239,19 +242,22 @@ def attn_fwd_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int, caus
 
 
 def attn_bwd(q, k, v, o, lse, dout, causal: bool = False, scale: float | None = None, dq=None, dk=None, dv=None,
-             workspace=None, stream=None):
+             workspace=None, stream=None, causal_align: str = "top-left"):
     """Gradients of attn_fwd's output: returns (dq, dk, dv), bf16, shaped
     like q, k, v.  o and lse are what attn_fwd returned for the same inputs;
     dout is the gradient of the loss with respect to o.  Dense (batch, seq,
-    heads, head_dim) tensors, one key/value head per query head, top-left
-    causal alignment."""
+    heads, head_dim) tensors; k and v may have fewer heads than q (grouped
+    query heads; a shared head's gradient sums its group's)."""
     for name, t in (("q", q), ("k", k), ("v", v), ("o", o), ("dout", dout)):
         if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous() or t.dim() != 4:
             raise ValueError(f"{name} must be a contiguous 4-D bf16 CUDA tensor (batch, seq, heads, head_dim)")
     B, Sq, H, d = q.shape
-    Sk = k.shape[1]
-    if k.shape != (B, Sk, H, d) or v.shape != k.shape or o.shape != q.shape or dout.shape != q.shape:
-        raise ValueError("shape mismatch (the backward takes one key/value head per query head)")
+    Sk, H_kv = k.shape[1], k.shape[2]
+    if (k.shape != (B, Sk, H_kv, d) or H % H_kv != 0 or v.shape != k.shape or o.shape != q.shape
+            or dout.shape != q.shape):
+        raise ValueError("shape mismatch")
+    if causal_align not in CAUSAL_ALIGN:
+        raise ValueError(f"causal_align must be one of {sorted(CAUSAL_ALIGN)}")
     if lse.shape != (B, H, Sq) or lse.dtype != torch.float32 or not lse.is_contiguous():
         raise ValueError("lse must be a contiguous fp32 tensor of shape (B, H, Sq)")
     if scale is None:
@@ -266,10 +272,12 @@ def attn_bwd(q, k, v, o, lse, dout, causal: bool = False, scale: float | None = 
     need = int(L.attn_bwd_workspace_size(B, H, Sq))
     if workspace is None:
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    lay = make_layout(H_kv, CAUSAL_ALIGN[causal_align])
     with torch.cuda.device(q.device):
-        rc = L.attn_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), dout.data_ptr(),
-                        dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, Sq, Sk, d, float(scale), int(bool(causal)),
-                        workspace.data_ptr(), workspace.numel() * workspace.element_size(), _stream_handle(stream))
+        rc = L.attn_bwd_layout(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                               dout.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, Sq, Sk, d,
+                               float(scale), int(bool(causal)), ctypes.byref(lay), workspace.data_ptr(),
+                               workspace.numel() * workspace.element_size(), _stream_handle(stream))
     _check(rc)
     return dq, dk, dv
 

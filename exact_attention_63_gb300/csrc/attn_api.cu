@@ -397,15 +397,29 @@ size_t attn_bwd_workspace_size(int B, int H, int Sq) {
   return (2 * static_cast<size_t>(B) * H * pitch * 4 + 255) & ~static_cast<size_t>(255);
 }
 
-int attn_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dout, void* dq,
-             void* dk, void* dv, int B, int H, int Sq, int Sk, int d, float scale, int causal, void* workspace,
-             size_t workspace_bytes, cudaStream_t stream) {
+int attn_bwd_layout(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dout,
+                    void* dq, void* dk, void* dv, int B, int H, int Sq, int Sk, int d, float scale, int causal,
+                    const attn_layout* layout, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
   int rc = check_args(q, k, v, o, lse, B, H, Sq, Sk, d, scale);
   if (rc != ATTN_OK) return rc;
+  int H_kv = H;
+  bool bottom_right = false;
+  if (layout != nullptr) {
+    if (layout->struct_size < sizeof(attn_layout) || layout->num_kv_heads < 0) return ATTN_ERR_LAYOUT;
+    if (layout->num_kv_heads > 0) H_kv = layout->num_kv_heads;
+    if (H % H_kv != 0) return ATTN_ERR_LAYOUT;
+    if (layout->causal_align != ATTN_CAUSAL_TOP_LEFT && layout->causal_align != ATTN_CAUSAL_BOTTOM_RIGHT)
+      return ATTN_ERR_LAYOUT;
+    bottom_right = causal && layout->causal_align == ATTN_CAUSAL_BOTTOM_RIGHT;
+    for (int i = 0; i < 3; ++i)  // the backward takes dense tensors
+      if (layout->q_strides[i] != 0 || layout->k_strides[i] != 0 || layout->v_strides[i] != 0 ||
+          layout->o_strides[i] != 0)
+        return ATTN_ERR_LAYOUT;
+  }
   if (dout == nullptr || dq == nullptr || dk == nullptr || dv == nullptr) return ATTN_ERR_NULL;
   if (!aligned16(dout) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv)) return ATTN_ERR_ALIGN;
   const long long n_kt = (static_cast<long long>(Sk) + 127) / 128;
-  if (static_cast<long long>(B) * H * n_kt > 0x7FFFFFFFLL) return ATTN_ERR_SHAPE;
+  if (static_cast<long long>(B) * H_kv * n_kt > 0x7FFFFFFFLL) return ATTN_ERR_SHAPE;
   if (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 ||
       workspace_bytes < attn_bwd_workspace_size(B, H, Sq))
     return ATTN_ERR_WORKSPACE;
@@ -418,8 +432,8 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const f
   cudaError_t e = attn::launch_bwd_prep(o, dout, lse, lse2, dvec, B, H, Sq, pitch, d, stream);
   if (e != cudaSuccess) return fail_cuda(e, "backward preparation launch");
 
-  const long long hd = static_cast<long long>(H) * d;
-  const long long qs[3] = {Sq * hd, hd, d}, ks[3] = {Sk * hd, hd, d};
+  const long long hd = static_cast<long long>(H) * d, kd = static_cast<long long>(H_kv) * d;
+  const long long qs[3] = {Sq * hd, hd, d}, ks[3] = {Sk * kd, kd, d};
   attn::BwdLaunchArgs a;
   std::memset(&a, 0, sizeof(a));
   a.p.lse2 = lse2;
@@ -430,7 +444,8 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const f
   a.p.Sq = Sq;
   a.p.Sk = Sk;
   a.p.pitch = pitch;
-  a.p.coff = 0;
+  a.p.coff = bottom_right ? Sk - Sq : 0;  // negative: rows without keys, whose gradients are zero
+  a.p.group = H / H_kv;
   a.p.scale_log2 = scale * 1.4426950408889634f;
   a.p.scale = scale;
   a.p.timeout_ns = static_cast<uint64_t>(kDefaultTimeoutMs) * 1000000ull;
@@ -438,21 +453,21 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const f
   a.device = dev;
   a.stream = stream;
   // dK, dV: rows are keys; the queries' Q and dO stream past them.
-  if ((rc = encode_bshd(&a.x, k, B, Sk, H, d, ks)) != ATTN_OK) return rc;
-  if ((rc = encode_bshd(&a.x2, v, B, Sk, H, d, ks)) != ATTN_OK) return rc;
+  if ((rc = encode_bshd(&a.x, k, B, Sk, H_kv, d, ks)) != ATTN_OK) return rc;
+  if ((rc = encode_bshd(&a.x2, v, B, Sk, H_kv, d, ks)) != ATTN_OK) return rc;
   if ((rc = encode_bshd(&a.a, q, B, Sq, H, d, qs)) != ATTN_OK) return rc;
   if ((rc = encode_bshd(&a.b, dout, B, Sq, H, d, qs)) != ATTN_OK) return rc;
   a.p.out0 = dv;
   a.p.out1 = dk;
   a.p.n_rt = static_cast<int>(n_kt);
-  a.grid = static_cast<int>(n_kt * B * H);
+  a.grid = static_cast<int>(n_kt * B * H_kv);
   a.mode = 1;
   if ((e = attn::launch_bwd(a, d)) != cudaSuccess) return fail_cuda(e, "backward dK/dV launch");
   // dQ: rows are queries; K and V stream past them.
   if ((rc = encode_bshd(&a.x, q, B, Sq, H, d, qs)) != ATTN_OK) return rc;
   if ((rc = encode_bshd(&a.x2, dout, B, Sq, H, d, qs)) != ATTN_OK) return rc;
-  if ((rc = encode_bshd(&a.a, k, B, Sk, H, d, ks)) != ATTN_OK) return rc;
-  if ((rc = encode_bshd(&a.b, v, B, Sk, H, d, ks)) != ATTN_OK) return rc;
+  if ((rc = encode_bshd(&a.a, k, B, Sk, H_kv, d, ks)) != ATTN_OK) return rc;
+  if ((rc = encode_bshd(&a.b, v, B, Sk, H_kv, d, ks)) != ATTN_OK) return rc;
   a.p.out0 = dq;
   a.p.out1 = nullptr;
   a.p.n_rt = (Sq + 127) / 128;
@@ -460,6 +475,13 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const f
   a.mode = 0;
   if ((e = attn::launch_bwd(a, d)) != cudaSuccess) return fail_cuda(e, "backward dQ launch");
   return ATTN_OK;
+}
+
+int attn_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dout, void* dq,
+             void* dk, void* dv, int B, int H, int Sq, int Sk, int d, float scale, int causal, void* workspace,
+             size_t workspace_bytes, cudaStream_t stream) {
+  return attn_bwd_layout(q, k, v, o, lse, dout, dq, dk, dv, B, H, Sq, Sk, d, scale, causal, nullptr, workspace,
+                         workspace_bytes, stream);
 }
 
 size_t attn_fwd_host_workspace_size(int B, int H, int Sq, int Sk, int d) {

@@ -16,6 +16,9 @@
 //   DKV rows = keys (X = K, X2 = V), columns = queries (A = Q, B = dO):
 //       Sᵀ = K Qᵀ, dPᵀ = V dOᵀ, Pᵀ and dSᵀ per (key, query),
 //       dV += Pᵀ dO, dK += dSᵀ Q.
+// With grouped key/value heads the dQ pass reads the K/V head of its query
+// head's group, and the dK/dV pass of a K/V head walks the query blocks of
+// every query head in its group (their contributions add up).
 // In both, S = X·Aᵀ and dP = X2·Bᵀ are K-major products like the forward's
 // Q·Kᵀ, and every accumulation is TMEM operand × MN-major shared-memory
 // operand like the forward's P·V.  No atomics: dQ and dK/dV are separate
@@ -93,9 +96,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const int lane = threadIdx.x & 31;
 
   // ---- the tile and the blocks of 128 columns its rows see
+  const int h_rows = (MODE == kModeDQ) ? p.H : p.H / p.group;  // heads of the row tensor
   const int rt = blockIdx.x % p.n_rt;
   const int bh = blockIdx.x / p.n_rt;
-  const int b = bh / p.H, h = bh % p.H;
+  const int b = bh / h_rows, h = bh % h_rows;  // h: query head (dQ) or key/value head (dK/dV)
   const int r0 = rt * 128;
   const int n_q = (p.Sq + 127) / 128, n_k = (p.Sk + 127) / 128;
   int c_first, c_end;  // column blocks [c_first, c_end)
@@ -109,7 +113,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     if (CAUSAL && r0 - p.coff < 0) c_first = 0;
     c_end = n_q;
   }
-  const int nblk = max(0, c_end - c_first);
+  if (c_end < c_first) c_end = c_first;
+  // The dK/dV pass walks its column blocks once per query head of the group.
+  const int n_per = c_end - c_first;
+  const int nblk = (MODE == kModeDKV) ? n_per * p.group : n_per;
+  // Column block n: its first column, and the head of the A/B tensors.
+  auto col0_of = [&](int n) { return (c_first + (MODE == kModeDKV ? n % max(n_per, 1) : n)) * 128; };
+  auto head_of = [&](int n) { return MODE == kModeDKV ? h * p.group + n / max(n_per, 1) : h / p.group; };
 
   if (warp == kBwdLoaderWarp) {
     tmem_alloc(smem_u32(tmem_slot), 512);
@@ -149,14 +159,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const int slot = n % L::kStages;
         if (!wait_bar(bar_ring_empty(slot), ((n / L::kStages) & 1) ^ 1u, wc)) break;
         const uint32_t dst = sRing + slot * L::kSlotBytes;
-        const int c0 = (c_first + n) * 128;
+        const int c0 = col0_of(n), ha = head_of(n);
         mbar_arrive_expect_tx(bar_ring_full(slot), 2 * L::kTileBytes + L::kVecBytes);
         for (int s = 0; s < L::kSlabs; ++s) {
-          tma_load_4d(dst + s * L::kSlabBytes, &tm_a, 64 * s, h, c0, b, bar_ring_full(slot));
-          tma_load_4d(dst + L::kTileBytes + s * L::kSlabBytes, &tm_b, 64 * s, h, c0, b, bar_ring_full(slot));
+          tma_load_4d(dst + s * L::kSlabBytes, &tm_a, 64 * s, ha, c0, b, bar_ring_full(slot));
+          tma_load_4d(dst + L::kTileBytes + s * L::kSlabBytes, &tm_b, 64 * s, ha, c0, b, bar_ring_full(slot));
         }
         if (MODE == kModeDKV) {
-          const size_t row = static_cast<size_t>(bh) * p.pitch + c0;
+          const size_t row = (static_cast<size_t>(b) * p.H + ha) * p.pitch + c0;
           bulk_load(dst + 2 * L::kTileBytes, p.lse2 + row, 512, bar_ring_full(slot));
           bulk_load(dst + 2 * L::kTileBytes + 512, p.dvec + row, 512, bar_ring_full(slot));
         }
@@ -240,7 +250,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const bool got = wait_bar(bar_s_full, n & 1, wc);
       if (__any_sync(0xffffffffu, !got)) { ok = false; break; }
       tc_fence_after();
-      const int c0 = (c_first + n) * 128;
+      const int c0 = col0_of(n);
       const float* vec = reinterpret_cast<const float*>(smem + L::kRingOff + (n % L::kStages) * L::kSlotBytes +
                                                         2 * L::kTileBytes);
       if (MODE == kModeDKV) {
@@ -313,11 +323,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       tc_fence_after();
     }
     const int rows_total = (MODE == kModeDQ) ? p.Sq : p.Sk;
+    const int heads_out = h_rows;
     for (int o = 0; o < (MODE == kModeDQ ? 1 : 2) && (ok || nblk == 0); ++o) {
       const uint32_t tacc = (o == 0 ? tAcc0 : tAcc1) + lane_off + hh * (D / 2);
       const float mul = (MODE == kModeDQ || o == 1) ? p.scale : 1.f;
       uint16_t* const out = static_cast<uint16_t*>(o == 0 ? p.out0 : p.out1) +
-                            ((static_cast<size_t>(b) * rows_total + row) * p.H + h) * D + hh * (D / 2);
+                            ((static_cast<size_t>(b) * rows_total + row) * heads_out + h) * D + hh * (D / 2);
 #pragma unroll
       for (int c = 0; c < D / 64; ++c) {
         uint32_t x[32];

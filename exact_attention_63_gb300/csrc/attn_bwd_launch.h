@@ -16,8 +16,9 @@ struct BwdParams {
   const float* dvec;   // [B·H, pitch]: D = rowsum(dO ∘ O); 0 beyond Sq
   unsigned int* status;
   int B, H, Sq, Sk, pitch;
-  int coff;            // causal: key j visible to query i iff j ≤ i + coff (≥ 0)
-  int n_rt;            // row tiles per (batch, head)
+  int coff;            // causal: key j visible to query i iff j ≤ i + coff (may be negative)
+  int group;           // query heads per key/value head (H / H_kv)
+  int n_rt;            // row tiles per (batch, row head): row heads are H (dQ pass) or H_kv (dK/dV pass)
   float scale_log2;    // scale · log2(e)
   float scale;
   uint64_t timeout_ns;

@@ -245,6 +245,18 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const f
              void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
 /*
+ * attn_bwd_layout — attn_bwd with grouped key/value heads and the causal
+ * alignment of an attn_layout (layout may be NULL: the same as attn_bwd).
+ * k, v, dk, dv then have num_kv_heads heads: the gradient of a key/value
+ * head sums the contributions of every query head of its group.  Rows that
+ * see no key (bottom-right with Sq > Sk) get zero dQ.  The strides must be
+ * zero (dense tensors), else ATTN_ERR_LAYOUT.
+ */
+int attn_bwd_layout(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dout,
+                    void* dq, void* dk, void* dv, int B, int H, int Sq, int Sk, int d, float scale, int causal,
+                    const attn_layout* layout, void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/*
  * attn_fwd_host — the same operation on HOST buffers, end to end.
  *   q_h, k_h, v_h : host bf16 inputs (layouts above); o_h, lse_h : host outputs.
  *   workspace     : caller-owned DEVICE buffer of at least

@@ -228,17 +228,21 @@ def attention_backward_head(q, k, v, dO, scale: float, causal: bool, causal_offs
 
 def attention_backward(q, k, v, dO, scale: float, causal: bool, causal_offset: int = 0):
     """Gradients over all batches and heads: q, dO [B, Sq, H, d], k, v
-    [B, Sk, H, d] (torch tensors or arrays).  Returns dQ, dK, dV (float64, the
-    shapes of q, k, v)."""
+    [B, Sk, H_kv, d] (torch tensors or arrays; H a multiple of H_kv).  A
+    key/value head shared by a group of query heads gets the sum of their
+    gradients.  Returns dQ, dK, dV (float64, the shapes of q, k, v)."""
     q, k, v, dO = to_f64(q), to_f64(k), to_f64(v), to_f64(dO)
     B, Sq, H, d = q.shape
-    if k.shape[2] != H:
-        raise ValueError("the backward oracle takes one key/value head per query head")
+    H_kv = k.shape[2]
     dQ, dK, dV = np.zeros_like(q), np.zeros_like(k), np.zeros_like(v)
     for b in range(B):
         for h in range(H):
-            dQ[b, :, h], dK[b, :, h], dV[b, :, h], _ = attention_backward_head(
-                q[b, :, h], k[b, :, h], v[b, :, h], dO[b, :, h], scale, causal, causal_offset)
+            g = kv_head(h, H, H_kv)
+            dq, dk, dv, _ = attention_backward_head(q[b, :, h], k[b, :, g], v[b, :, g], dO[b, :, h], scale, causal,
+                                                    causal_offset)
+            dQ[b, :, h] = dq
+            dK[b, :, g] += dk
+            dV[b, :, g] += dv
     return dQ, dK, dV
 
 

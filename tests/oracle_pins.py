@@ -491,4 +491,24 @@ def pin_backward_identities():
             assert np.array_equal(dV[b, :, h], hv)
 
 
+def pin_backward_grouped_heads():
+    """Grouped heads: the gradients equal those of ordinary attention on K/V
+    with each head repeated for its group, with dK and dV summed over the
+    group (the chain rule through the repetition)."""
+    r = _rng(1960)
+    B, S, Sk, H, H_kv, d = 2, 9, 12, 6, 2, 8
+    q = _bf16_like(r.standard_normal((B, S, H, d)))
+    k = _bf16_like(r.standard_normal((B, Sk, H_kv, d)))
+    v = _bf16_like(r.standard_normal((B, Sk, H_kv, d)))
+    dO = r.standard_normal((B, S, H, d))
+    g = H // H_kv
+    for causal, off in ((False, 0), (True, 0), (True, Sk - S)):
+        dQ, dK, dV = oracle.attention_backward(q, k, v, dO, 0.3, causal, causal_offset=off)
+        rQ, rK, rV = oracle.attention_backward(q, np.repeat(k, g, axis=2), np.repeat(v, g, axis=2), dO, 0.3, causal,
+                                               causal_offset=off)
+        assert np.max(np.abs(dQ - rQ)) <= TOL
+        assert np.max(np.abs(dK - rK.reshape(B, Sk, H_kv, g, d).sum(axis=3))) <= TOL
+        assert np.max(np.abs(dV - rV.reshape(B, Sk, H_kv, g, d).sum(axis=3))) <= TOL
+
+
 ALL_PINS = [v for k_, v in sorted(globals().items()) if k_.startswith("pin_") and callable(v)]

@@ -159,3 +159,14 @@ def test_varlen_rejected_before_launch(L, args, expect):
 
 def test_varlen_bad_alignment_rejected(L):
     assert attn.raw_fwd_varlen(A, A, A, A, A, A, A, 2, 100, 100, 64, 4, 2, 64, 0.125, 1, causal_align=5) == -12
+
+
+def test_backward_layout_checks(L):
+    bad = attn.make_layout(num_kv_heads=3)
+    assert L.attn_bwd_layout(A, A, A, A, A, A, A, A, A, 1, 4, 8, 8, 64, 0.125, 1, ctypes.byref(bad), A, 1 << 20,
+                             None) == -12
+    strided = attn.make_layout(q_strides=(4096, 512, 64))
+    assert L.attn_bwd_layout(A, A, A, A, A, A, A, A, A, 1, 4, 8, 8, 64, 0.125, 1, ctypes.byref(strided), A,
+                             1 << 20, None) == -12
+    assert L.attn_bwd(A, A, A, A, A, A, A, A, A, 1, 4, 8, 8, 64, 0.125, 1, A, 16, None) == -10  # workspace too small
+    assert L.attn_bwd(A, A, A, A, A, 0, A, A, A, 1, 4, 8, 8, 64, 0.125, 1, A, 1 << 20, None) == -1

@@ -29,14 +29,20 @@ CASES = [
     C(1, 2, 500, 64, 64, True, seed=105),
     C(1, 1, 1000, 1000, 128, True, seed=106),
     C(1, 2, 640, 640, 64, False, sigma_qk=3.0, seed=107),
+    # grouped key/value heads, bottom-right alignment (Sq < Sk and Sq > Sk)
+    C(2, 8, 300, 300, 128, True, seed=110, H_kv=2),
+    C(1, 4, 257, 383, 64, False, seed=111, H_kv=1),
+    C(1, 2, 200, 520, 128, True, seed=112, causal_align="bottom-right"),
+    C(1, 2, 520, 200, 64, True, seed=113, causal_align="bottom-right"),
+    C(1, 6, 700, 333, 128, True, seed=114, H_kv=3, causal_align="bottom-right"),
 ]
 
 
 def grads(w, q, k, v, dout):
     dev = torch.device("cuda:0")
     qd, kd, vd, gd = (t.to(dev) for t in (q, k, v, dout))
-    o, lse = attn.attn_fwd(qd, kd, vd, causal=w.causal, scale=w.scale)
-    dq, dk, dv = attn.attn_bwd(qd, kd, vd, o, lse, gd, causal=w.causal, scale=w.scale)
+    o, lse = attn.attn_fwd(qd, kd, vd, causal=w.causal, scale=w.scale, causal_align=w.causal_align)
+    dq, dk, dv = attn.attn_bwd(qd, kd, vd, o, lse, gd, causal=w.causal, scale=w.scale, causal_align=w.causal_align)
     torch.cuda.synchronize()
     assert attn.get_status() == 0
     return dq, dk, dv
@@ -58,7 +64,8 @@ def test_backward_matches_oracle(w):
     g = torch.Generator().manual_seed(w.seed + 1000)
     dout = torch.randn(q.shape, generator=g).to(torch.bfloat16)
     dq, dk, dv = grads(w, q, k, v, dout)
-    rq, rk, rv = oracle.attention_backward(q, k, v, dout, w.scale, w.causal)
+    off = (w.Sk - w.Sq) if (w.causal and w.causal_align == "bottom-right") else 0
+    rq, rk, rv = oracle.attention_backward(q, k, v, dout, w.scale, w.causal, causal_offset=off)
     check("dq", dq, rq, w.name)
     check("dk", dk, rk, w.name)
     check("dv", dv, rv, w.name)

@@ -44,6 +44,7 @@ MUTANTS = {
     "rows_drop_offset": ("rows=rows, causal_offset=causal_offset)", "rows=rows)"),
     "bwd_dv_untransposed": ("    dV = P.T @ dO", "    dV = P @ dO[:P.shape[1]] if P.shape[0] >= P.shape[1] else P.T @ dO * 0.5"),
     "bwd_ds_drops_d": ("    dS = P * (dP - D[:, None])", "    dS = P * dP"),
+    "bwd_group_overwrites": ("            dK[b, :, g] += dk", "            dK[b, :, g] = dk"),
     "bwd_dk_unscaled": ("scale * (dS.T @ q), dV, D", "(dS.T @ q), dV, D"),
     "bwd_dq_uses_v": ("return scale * (dS @ k), scale", "return scale * (dS @ v), scale"),
     "varlen_global_offset": ("        off = (k1 - k0) - (q1 - q0) if (causal and bottom_right) else 0",
