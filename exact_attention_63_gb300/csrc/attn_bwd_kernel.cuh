@@ -28,8 +28,12 @@
 // columns [64h, 64h+64) of each block; one thread per row) and write the
 // tile's outputs; warp 8 loads X, X2 once and streams (A, B) blocks — plus, in
 // DKV, the 128 log2-LSE and D values of the block's queries — through a ring;
-// warp 9 issues the MMAs.  S and dP are single-buffered: the next block's
-// products wait until the accumulations that read P and dS from them are done.
+// warp 9 issues the MMAs.  Each block is done as two halves of 64 columns
+// with their own barriers, so the MMAs of one half overlap the other
+// warpgroup's work: S and dP of half 1 run while warpgroup 0 turns half 0
+// into P and dS, half 0's accumulations while warpgroup 1 works on half 1,
+// and the next block's half-0 products as soon as half 0's accumulations
+// have released its columns.
 //
 // TMEM columns: S [0, 128), dP [128, 256), acc0 [256, 256+D) (dQ or dV),
 // acc1 [256+D, 256+2D) (dK).  P (bf16 pairs) overwrites S's columns and dS
@@ -63,8 +67,8 @@ struct BwdLayout {
   static constexpr uint32_t kXOff = 0;                       // X, X2
   static constexpr uint32_t kRingOff = 2 * kTileBytes;
   static constexpr uint32_t kBarOff = kRingOff + kStages * kSlotBytes;
-  // barriers: fix_full, ring_full[S], ring_empty[S], s_full, p_full, acc_done, done
-  static constexpr int kNumBars = 1 + 2 * kStages + 4;
+  // barriers: fix_full, ring_full[S], ring_empty[S], s_full[2], p_full[2], acc_done[2], done
+  static constexpr int kNumBars = 1 + 2 * kStages + 7;
   static constexpr uint32_t kMiscOff = kBarOff + 8 * kNumBars;
   static constexpr uint32_t kSmemBytes = kMiscOff + 16 + 1024;
 };
@@ -85,10 +89,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const uint32_t bar_fix = bars;
   auto bar_ring_full = [&](int s) { return bars + 8u * (1 + s); };
   auto bar_ring_empty = [&](int s) { return bars + 8u * (1 + L::kStages + s); };
-  const uint32_t bar_s_full = bars + 8u * (1 + 2 * L::kStages);
-  const uint32_t bar_p_full = bar_s_full + 8u;
-  const uint32_t bar_acc_done = bar_s_full + 16u;
-  const uint32_t bar_done = bar_s_full + 24u;
+  const uint32_t bar_half0 = bars + 8u * (1 + 2 * L::kStages);
+  auto bar_s_full = [&](int hh) { return bar_half0 + 8u * hh; };     // S, dP of a half written
+  auto bar_p_full = [&](int hh) { return bar_half0 + 8u * (2 + hh); };  // P, dS of a half written
+  auto bar_acc_done = [&](int hh) { return bar_half0 + 8u * (4 + hh); };  // a half's accumulations done
+  const uint32_t bar_done = bar_half0 + 8u * 6;                      // every MMA done
   uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMiscOff);
   volatile uint32_t* const abort_flag = reinterpret_cast<volatile uint32_t*>(smem + L::kMiscOff + 4);
 
@@ -133,9 +138,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       mbar_init(bar_ring_full(s), 1);
       mbar_init(bar_ring_empty(s), 1);
     }
-    mbar_init(bar_s_full, 1);
-    mbar_init(bar_p_full, 8);  // one arrival per softmax-gradient warp
-    mbar_init(bar_acc_done, 1);
+    for (int hh = 0; hh < 2; ++hh) {
+      mbar_init(bar_s_full(hh), 1);
+      mbar_init(bar_p_full(hh), 4);  // one arrival per warp of the half's warpgroup
+      mbar_init(bar_acc_done(hh), 1);
+    }
     mbar_init(bar_done, 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     fence_proxy_async_smem();
@@ -182,50 +189,69 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   } else if (warp == kBwdMmaWarp) {
     // ======================================================== MMA issuer
     if (lane == 0 && nblk > 0) {
-      constexpr uint32_t idS = idesc_bf16(128, 128, false);
+      constexpr uint32_t idS = idesc_bf16(128, 64, false);  // one half: 64 columns
       constexpr uint32_t idAcc = idesc_bf16(128, D, true);
       const uint64_t dX = sdesc_kmajor_sw128(sX);
       const uint64_t dX2 = sdesc_kmajor_sw128(sX + L::kTileBytes);
-      bool ok = wait_bar(bar_fix, 0, wc);
-      for (int n = 0; n < nblk && ok; ++n) {
-        const int slot = n % L::kStages;
-        const uint32_t sA = sRing + slot * L::kSlotBytes, sB = sA + L::kTileBytes;
-        if (!wait_bar(bar_ring_full(slot), (n / L::kStages) & 1, wc)) { ok = false; break; }
-        // S and dP overwrite P and dS of the previous block: its accumulations
-        // must have completed.
-        if (n > 0 && !wait_bar(bar_acc_done, (n - 1) & 1, wc)) { ok = false; break; }
-        tc_fence_after();
-        const uint64_t dA = sdesc_kmajor_sw128(sA), dB = sdesc_kmajor_sw128(sB);
+      // S and dP of half hh of block n: columns [64hh, 64hh+64) are rows
+      // [64hh, 64hh+64) of the A and B tiles (8 KB into the tile).
+      auto products = [&](int n, int hh) {
+        const uint32_t sA = sRing + (n % L::kStages) * L::kSlotBytes, sB = sA + L::kTileBytes;
+        const uint64_t dA = sdesc_kmajor_sw128(sA + 8192u * hh), dB = sdesc_kmajor_sw128(sB + 8192u * hh);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = ((kk / 4) * L::kSlabBytes + (kk % 4) * 32) >> 4;
-          mma_ss(tS, dX + off, dA + off, idS, kk > 0 ? 1u : 0u);
+          mma_ss(tS + 64 * hh, dX + off, dA + off, idS, kk > 0 ? 1u : 0u);
         }
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = ((kk / 4) * L::kSlabBytes + (kk % 4) * 32) >> 4;
-          mma_ss(tdP, dX2 + off, dB + off, idS, kk > 0 ? 1u : 0u);
+          mma_ss(tdP + 64 * hh, dX2 + off, dB + off, idS, kk > 0 ? 1u : 0u);
         }
-        mma_commit(bar_s_full);
-        if (!wait_bar(bar_p_full, n & 1, wc)) { ok = false; break; }
-        tc_fence_after();
+        mma_commit(bar_s_full(hh));
+      };
+      // The accumulations of half hh of block n (P, dS from TMEM).
+      auto accumulate = [&](int n, int hh) {
+        const uint32_t sA = sRing + (n % L::kStages) * L::kSlotBytes, sB = sA + L::kTileBytes;
         const uint64_t dAm = sdesc_mnmajor_sw128(sA, L::kSlabBytes), dBm = sdesc_mnmajor_sw128(sB, L::kSlabBytes);
 #pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            const uint32_t acc = (n > 0 || hh > 0 || kk > 0) ? 1u : 0u;
-            const uint32_t rows = ((4 * hh + kk) * 2048) >> 4;  // 16 columns of the block per step
-            if (MODE == kModeDQ) {
-              mma_ts(tAcc0, tdP + 64 * hh + 8 * kk, dAm + rows, idAcc, acc);      // dQ += dS K
-            } else {
-              mma_ts(tAcc0, tS + 64 * hh + 8 * kk, dBm + rows, idAcc, acc);       // dV += Pᵀ dO
-              mma_ts(tAcc1, tdP + 64 * hh + 8 * kk, dAm + rows, idAcc, acc);      // dK += dSᵀ Q
-            }
+        for (int kk = 0; kk < 4; ++kk) {
+          const uint32_t acc = (n > 0 || hh > 0 || kk > 0) ? 1u : 0u;
+          const uint32_t rows = ((4 * hh + kk) * 2048) >> 4;  // 16 columns of the block per step
+          if (MODE == kModeDQ) {
+            mma_ts(tAcc0, tdP + 64 * hh + 8 * kk, dAm + rows, idAcc, acc);      // dQ += dS K
+          } else {
+            mma_ts(tAcc0, tS + 64 * hh + 8 * kk, dBm + rows, idAcc, acc);       // dV += Pᵀ dO
+            mma_ts(tAcc1, tdP + 64 * hh + 8 * kk, dAm + rows, idAcc, acc);      // dK += dSᵀ Q
           }
         }
-        mma_commit(bar_acc_done);
-        mma_commit(bar_ring_empty(slot));
+        mma_commit(bar_acc_done(hh));
+      };
+      bool ok = wait_bar(bar_fix, 0, wc) && wait_bar(bar_ring_full(0), 0, wc);
+      if (ok) {
+        tc_fence_after();
+        products(0, 0);
+        products(0, 1);
+      }
+      for (int n = 0; n < nblk && ok; ++n) {
+        for (int hh = 0; hh < 2 && ok; ++hh) {
+          if (!wait_bar(bar_p_full(hh), n & 1, wc)) { ok = false; break; }
+          tc_fence_after();
+          accumulate(n, hh);
+        }
+        if (!ok) break;
+        mma_commit(bar_ring_empty(n % L::kStages));  // A(n), B(n) no longer read
+        if (n + 1 < nblk) {
+          const int s1 = (n + 1) % L::kStages;
+          if (!wait_bar(bar_ring_full(s1), ((n + 1) / L::kStages) & 1, wc)) { ok = false; break; }
+          // A half's next products overwrite its P and dS: wait for that
+          // half's accumulations (a completion barrier, not issue order).
+          for (int hh = 0; hh < 2 && ok; ++hh) {
+            if (!wait_bar(bar_acc_done(hh), n & 1, wc)) { ok = false; break; }
+            tc_fence_after();
+            products(n + 1, hh);
+          }
+        }
       }
       // Every MMA must finish before the accumulators are read or TMEM freed.
       mma_commit(bar_done);
@@ -247,7 +273,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const float sc = p.scale_log2;
     bool ok = true;
     for (int n = 0; n < nblk && ok; ++n) {
-      const bool got = wait_bar(bar_s_full, n & 1, wc);
+      const bool got = wait_bar(bar_s_full(hh), n & 1, wc);
       if (__any_sync(0xffffffffu, !got)) { ok = false; break; }
       tc_fence_after();
       const int c0 = col0_of(n);
@@ -312,13 +338,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar_p_full);
+      if (lane == 0) mbar_arrive(bar_p_full(hh));
     }
     // ------------------------------------------------------------ outputs
     // Warpgroup hh writes columns [hh·D/2, (hh+1)·D/2) of its rows.
     bool have = nblk > 0 && ok;
     if (have) {
-      const bool fin = wait_bar(bar_acc_done, (nblk - 1) & 1, wc);
+      // The issuer's last commit: every MMA of the tile has completed.
+      const bool fin = wait_bar(bar_done, 0, wc);
       if (__any_sync(0xffffffffu, !fin)) have = false;
       tc_fence_after();
     }
@@ -366,37 +393,48 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
 // D = rowsum(dO ∘ O) and LSE · log2(e) per query row, in [B·H, pitch] arrays
 // padded to whole 128-row blocks (+inf and 0 beyond Sq, so padded queries get
-// P = 0).  One thread per (batch, head, row).
+// P = 0).  One warp per (batch, head, row): its lanes read the row's D
+// elements of O and dO as consecutive 4- or 8-byte pieces (coalesced) and the
+// products are summed with shuffles.
 template <int D>
 __global__ void attn_bwd_prep_kernel(const uint16_t* o, const uint16_t* dout, const float* lse, float* lse2,
                                      float* dvec, int B, int H, int Sq, int pitch) {
+  constexpr int kPer = D / 32;  // bf16 values per lane: 2 or 4
+  const int lane = threadIdx.x & 31;
   const long long n = static_cast<long long>(B) * H * pitch;
-  for (long long t = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; t < n;
-       t += static_cast<long long>(gridDim.x) * blockDim.x) {
+  const long long warps = static_cast<long long>(gridDim.x) * (blockDim.x >> 5);
+  for (long long t = blockIdx.x * static_cast<long long>(blockDim.x >> 5) + (threadIdx.x >> 5); t < n; t += warps) {
     const int i = static_cast<int>(t % pitch);
     const long long bh = t / pitch;
-    const int b = static_cast<int>(bh / H), h = static_cast<int>(bh % H);
     if (i >= Sq) {
-      lse2[t] = INFINITY;
-      dvec[t] = 0.f;
+      if (lane == 0) {
+        lse2[t] = INFINITY;
+        dvec[t] = 0.f;
+      }
       continue;
     }
-    const size_t off = ((static_cast<size_t>(b) * Sq + i) * H + h) * D;
-    const uint4* a = reinterpret_cast<const uint4*>(o + off);
-    const uint4* g = reinterpret_cast<const uint4*>(dout + off);
-    float acc = 0.f;
-#pragma unroll 4
-    for (int c = 0; c < D / 8; ++c) {
-      const uint4 x = a[c], y = g[c];
-      const uint32_t xs[4] = {x.x, x.y, x.z, x.w}, ys[4] = {y.x, y.y, y.z, y.w};
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        acc = fmaf(__uint_as_float(xs[e] << 16), __uint_as_float(ys[e] << 16), acc);
-        acc = fmaf(__uint_as_float(xs[e] & 0xFFFF0000u), __uint_as_float(ys[e] & 0xFFFF0000u), acc);
-      }
+    const int b = static_cast<int>(bh / H), h = static_cast<int>(bh % H);
+    const size_t off = ((static_cast<size_t>(b) * Sq + i) * H + h) * D + lane * kPer;
+    uint32_t xs[kPer / 2], ys[kPer / 2];
+    if constexpr (kPer == 4) {
+      const uint2 x = *reinterpret_cast<const uint2*>(o + off), y = *reinterpret_cast<const uint2*>(dout + off);
+      xs[0] = x.x; xs[1] = x.y; ys[0] = y.x; ys[1] = y.y;
+    } else {
+      xs[0] = *reinterpret_cast<const uint32_t*>(o + off);
+      ys[0] = *reinterpret_cast<const uint32_t*>(dout + off);
     }
-    dvec[t] = acc;
-    lse2[t] = lse[(static_cast<size_t>(b) * H + h) * Sq + i] * 1.4426950408889634f;
+    float acc = 0.f;
+#pragma unroll
+    for (int e = 0; e < kPer / 2; ++e) {
+      acc = fmaf(__uint_as_float(xs[e] << 16), __uint_as_float(ys[e] << 16), acc);
+      acc = fmaf(__uint_as_float(xs[e] & 0xFFFF0000u), __uint_as_float(ys[e] & 0xFFFF0000u), acc);
+    }
+#pragma unroll
+    for (int m = 16; m > 0; m >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, m);
+    if (lane == 0) {
+      dvec[t] = acc;
+      lse2[t] = lse[(static_cast<size_t>(b) * H + h) * Sq + i] * 1.4426950408889634f;
+    }
   }
 }
 
