@@ -78,7 +78,7 @@ def load_profile_traffic(workload_name):
 
 
 class ClockSampler:
-    """nvidia-smi clock/throttle samples every 200 ms while running."""
+    """nvidia-smi clock/throttle samples every 100 ms while running."""
 
     FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -220,7 +220,7 @@ def run_reference(args, w, rank, world):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--steps", type=int, default=3000)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--config", type=int, default=2, help="workload index 1-5 (default 2)")
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
