@@ -28,16 +28,26 @@
 // columns [64h, 64h+64) of each block; one thread per row) and write the
 // tile's outputs; warp 8 loads X, X2 once and streams (A, B) blocks — plus, in
 // DKV, the 128 log2-LSE and D values of the block's queries — through a ring;
-// warp 9 issues the MMAs.  Each block is done as two halves of 64 columns
-// with their own barriers, so the MMAs of one half overlap the other
-// warpgroup's work: S and dP of half 1 run while warpgroup 0 turns half 0
-// into P and dS, half 0's accumulations while warpgroup 1 works on half 1,
-// and the next block's half-0 products as soon as half 0's accumulations
-// have released its columns.
+// warp 9 issues the MMAs.
+//
+// Schedule.  A shared-memory-operand MMA reads both of its tiles at the
+// shared-memory rate (128 B/clk per SM: a 128×128×16 product takes its 64
+// cycles, a 128×64×16 one 48 instead of 32), so S and dP are each computed
+// for all 128 columns at once and the rest of the block is pipelined around
+// them with TMEM-operand accumulations (which read only their B tile):
+//   DKV: S(n), dP(n); the warpgroups store P over S and signal per half, so
+//        dV += Pᵀ dO starts while they form dS; dK += dSᵀ Q per half as dS
+//        lands over dP.  S(n+1) waits for dV(n) (it overwrites P(n)), dP(n+1)
+//        for dK(n).
+//   DQ:  S(n), dP(n); the warpgroups read S and release its columns at once
+//        (P stays in registers), so S(n+1) overlaps their work; dS goes to
+//        columns of its own (free in this pass) and dQ += dS K runs per half;
+//        dP(n+1) follows as soon as dS(n) — and so the read of dP(n) — is in.
 //
 // TMEM columns: S [0, 128), dP [128, 256), acc0 [256, 256+D) (dQ or dV),
-// acc1 [256+D, 256+2D) (dK).  P (bf16 pairs) overwrites S's columns and dS
-// overwrites dP's, in the packed layout the forward uses for P.
+// acc1 [256+D, 256+2D) (dK; in the dQ pass it holds dS).  P (bf16 pairs)
+// overwrites S's columns and, in DKV, dS overwrites dP's, in the packed layout
+// the forward uses for P.
 #pragma once
 
 #include <cstdint>
@@ -67,8 +77,9 @@ struct BwdLayout {
   static constexpr uint32_t kXOff = 0;                       // X, X2
   static constexpr uint32_t kRingOff = 2 * kTileBytes;
   static constexpr uint32_t kBarOff = kRingOff + kStages * kSlotBytes;
-  // barriers: fix_full, ring_full[S], ring_empty[S], s_full[2], p_full[2], acc_done[2], done
-  static constexpr int kNumBars = 1 + 2 * kStages + 7;
+  // barriers: fix_full, ring_full[S], ring_empty[S], s_full, dp_full, p_full[2], ds_full[2],
+  //           acc_a, acc_b, done
+  static constexpr int kNumBars = 1 + 2 * kStages + 9;
   static constexpr uint32_t kMiscOff = kBarOff + 8 * kNumBars;
   static constexpr uint32_t kSmemBytes = kMiscOff + 16 + 1024;
 };
@@ -89,11 +100,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const uint32_t bar_fix = bars;
   auto bar_ring_full = [&](int s) { return bars + 8u * (1 + s); };
   auto bar_ring_empty = [&](int s) { return bars + 8u * (1 + L::kStages + s); };
-  const uint32_t bar_half0 = bars + 8u * (1 + 2 * L::kStages);
-  auto bar_s_full = [&](int hh) { return bar_half0 + 8u * hh; };     // S, dP of a half written
-  auto bar_p_full = [&](int hh) { return bar_half0 + 8u * (2 + hh); };  // P, dS of a half written
-  auto bar_acc_done = [&](int hh) { return bar_half0 + 8u * (4 + hh); };  // a half's accumulations done
-  const uint32_t bar_done = bar_half0 + 8u * 6;                      // every MMA done
+  const uint32_t bar_b0 = bars + 8u * (1 + 2 * L::kStages);
+  const uint32_t bar_s_full = bar_b0;            // S of the block written
+  const uint32_t bar_dp_full = bar_b0 + 8u;      // dP of the block written
+  // DKV: P of a half stored over S; DQ: S of a half read (its columns are free)
+  auto bar_p_full = [&](int hh) { return bar_b0 + 8u * (2 + hh); };
+  // dS of a half stored (so dP of the half has been read)
+  auto bar_ds_full = [&](int hh) { return bar_b0 + 8u * (4 + hh); };
+  const uint32_t bar_acc_a = bar_b0 + 8u * 6;    // DKV: dV of the block done (S's columns are free)
+  const uint32_t bar_acc_b = bar_b0 + 8u * 7;    // DKV: dK done (dP's columns free); DQ: dQ done (dS's)
+  const uint32_t bar_done = bar_b0 + 8u * 8;     // every MMA done
   uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMiscOff);
   volatile uint32_t* const abort_flag = reinterpret_cast<volatile uint32_t*>(smem + L::kMiscOff + 4);
 
@@ -138,11 +154,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       mbar_init(bar_ring_full(s), 1);
       mbar_init(bar_ring_empty(s), 1);
     }
+    mbar_init(bar_s_full, 1);
+    mbar_init(bar_dp_full, 1);
     for (int hh = 0; hh < 2; ++hh) {
-      mbar_init(bar_s_full(hh), 1);
       mbar_init(bar_p_full(hh), 4);  // one arrival per warp of the half's warpgroup
-      mbar_init(bar_acc_done(hh), 1);
+      mbar_init(bar_ds_full(hh), 4);
     }
+    mbar_init(bar_acc_a, 1);
+    mbar_init(bar_acc_b, 1);
     mbar_init(bar_done, 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     fence_proxy_async_smem();
@@ -152,6 +171,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const uint32_t tmem = *tmem_slot;
   const WaitCtx wc{abort_flag, p.status, p.timeout_ns};
   const uint32_t tS = tmem, tdP = tmem + 128, tAcc0 = tmem + 256, tAcc1 = tmem + 256 + D;
+  // dQ pass: dS gets columns of its own (where dK sits in the other pass), so
+  // the next block's dP need not wait for dQ += dS K.
+  const uint32_t tDS = tAcc1;
 
   if (warp == kBwdLoaderWarp) {
     // ============================================================ loader
@@ -189,68 +211,94 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   } else if (warp == kBwdMmaWarp) {
     // ======================================================== MMA issuer
     if (lane == 0 && nblk > 0) {
-      constexpr uint32_t idS = idesc_bf16(128, 64, false);  // one half: 64 columns
+      constexpr uint32_t idS = idesc_bf16(128, 128, false);
       constexpr uint32_t idAcc = idesc_bf16(128, D, true);
       const uint64_t dX = sdesc_kmajor_sw128(sX);
       const uint64_t dX2 = sdesc_kmajor_sw128(sX + L::kTileBytes);
-      // S and dP of half hh of block n: columns [64hh, 64hh+64) are rows
-      // [64hh, 64hh+64) of the A and B tiles (8 KB into the tile).
-      auto products = [&](int n, int hh) {
-        const uint32_t sA = sRing + (n % L::kStages) * L::kSlotBytes, sB = sA + L::kTileBytes;
-        const uint64_t dA = sdesc_kmajor_sw128(sA + 8192u * hh), dB = sdesc_kmajor_sw128(sB + 8192u * hh);
+      // S = X·Aᵀ (which = 0) or dP = X2·Bᵀ (which = 1) of block n, all 128
+      // columns in one pass over the operands (N = 64 halves would read X
+      // from shared memory twice).
+      auto product = [&](int n, int which) {
+        const uint32_t sT = sRing + (n % L::kStages) * L::kSlotBytes + which * L::kTileBytes;
+        const uint64_t dT = sdesc_kmajor_sw128(sT), dXx = which ? dX2 : dX;
+        const uint32_t tD = which ? tdP : tS;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = ((kk / 4) * L::kSlabBytes + (kk % 4) * 32) >> 4;
-          mma_ss(tS + 64 * hh, dX + off, dA + off, idS, kk > 0 ? 1u : 0u);
+          mma_ss(tD, dXx + off, dT + off, idS, kk > 0 ? 1u : 0u);
         }
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = ((kk / 4) * L::kSlabBytes + (kk % 4) * 32) >> 4;
-          mma_ss(tdP + 64 * hh, dX2 + off, dB + off, idS, kk > 0 ? 1u : 0u);
-        }
-        mma_commit(bar_s_full(hh));
+        mma_commit(which ? bar_dp_full : bar_s_full);
       };
-      // The accumulations of half hh of block n (P, dS from TMEM).
-      auto accumulate = [&](int n, int hh) {
-        const uint32_t sA = sRing + (n % L::kStages) * L::kSlotBytes, sB = sA + L::kTileBytes;
-        const uint64_t dAm = sdesc_mnmajor_sw128(sA, L::kSlabBytes), dBm = sdesc_mnmajor_sw128(sB, L::kSlabBytes);
+      // One half of an accumulation: acc (+)= T[:, 64hh : 64hh+64] · M[64hh : 64hh+64, :]
+      // with T packed bf16 in TMEM at tT and M an MN-major tile of block n's slot.
+      auto acc_half = [&](int n, int hh, uint32_t tAcc, uint32_t tT, int which) {
+        const uint32_t sM = sRing + (n % L::kStages) * L::kSlotBytes + which * L::kTileBytes;
+        const uint64_t dM = sdesc_mnmajor_sw128(sM, L::kSlabBytes);
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) {
           const uint32_t acc = (n > 0 || hh > 0 || kk > 0) ? 1u : 0u;
-          const uint32_t rows = ((4 * hh + kk) * 2048) >> 4;  // 16 columns of the block per step
-          if (MODE == kModeDQ) {
-            mma_ts(tAcc0, tdP + 64 * hh + 8 * kk, dAm + rows, idAcc, acc);      // dQ += dS K
-          } else {
-            mma_ts(tAcc0, tS + 64 * hh + 8 * kk, dBm + rows, idAcc, acc);       // dV += Pᵀ dO
-            mma_ts(tAcc1, tdP + 64 * hh + 8 * kk, dAm + rows, idAcc, acc);      // dK += dSᵀ Q
-          }
+          mma_ts(tAcc, tT + 8 * kk, dM + (((4 * hh + kk) * 2048) >> 4), idAcc, acc);
         }
-        mma_commit(bar_acc_done(hh));
       };
       bool ok = wait_bar(bar_fix, 0, wc) && wait_bar(bar_ring_full(0), 0, wc);
       if (ok) {
         tc_fence_after();
-        products(0, 0);
-        products(0, 1);
+        product(0, 0);
+        product(0, 1);
       }
       for (int n = 0; n < nblk && ok; ++n) {
-        for (int hh = 0; hh < 2 && ok; ++hh) {
-          if (!wait_bar(bar_p_full(hh), n & 1, wc)) { ok = false; break; }
-          tc_fence_after();
-          accumulate(n, hh);
-        }
-        if (!ok) break;
-        mma_commit(bar_ring_empty(n % L::kStages));  // A(n), B(n) no longer read
-        if (n + 1 < nblk) {
-          const int s1 = (n + 1) % L::kStages;
-          if (!wait_bar(bar_ring_full(s1), ((n + 1) / L::kStages) & 1, wc)) { ok = false; break; }
-          // A half's next products overwrite its P and dS: wait for that
-          // half's accumulations (a completion barrier, not issue order).
+        const bool more = n + 1 < nblk;
+        if (MODE == kModeDKV) {
+          // dV += Pᵀ dO, half by half as the warpgroups store P.
           for (int hh = 0; hh < 2 && ok; ++hh) {
-            if (!wait_bar(bar_acc_done(hh), n & 1, wc)) { ok = false; break; }
+            if (!wait_bar(bar_p_full(hh), n & 1, wc)) { ok = false; break; }
             tc_fence_after();
-            products(n + 1, hh);
+            acc_half(n, hh, tAcc0, tS + 64 * hh, 1);
           }
+          if (!ok) break;
+          mma_commit(bar_acc_a);
+          // dK += dSᵀ Q.
+          for (int hh = 0; hh < 2 && ok; ++hh) {
+            if (!wait_bar(bar_ds_full(hh), n & 1, wc)) { ok = false; break; }
+            tc_fence_after();
+            acc_half(n, hh, tAcc1, tdP + 64 * hh, 0);
+          }
+          if (!ok) break;
+          mma_commit(bar_acc_b);
+          mma_commit(bar_ring_empty(n % L::kStages));  // A(n), B(n) no longer read
+          if (more) {
+            if (!wait_bar(bar_ring_full((n + 1) % L::kStages), ((n + 1) / L::kStages) & 1, wc)) { ok = false; break; }
+            // S(n+1) overwrites P(n): dV must have completed; dP(n+1)
+            // overwrites dS(n): dK must have completed (completion
+            // barriers; MMAs into different accumulators are not ordered).
+            if (!wait_bar(bar_acc_a, n & 1, wc)) { ok = false; break; }
+            tc_fence_after();
+            product(n + 1, 0);
+            if (!wait_bar(bar_acc_b, n & 1, wc)) { ok = false; break; }
+            tc_fence_after();
+            product(n + 1, 1);
+          }
+        } else {
+          // S(n+1) as soon as both warpgroups have read S(n).
+          if (more) {
+            if (!wait_bar(bar_ring_full((n + 1) % L::kStages), ((n + 1) / L::kStages) & 1, wc)) { ok = false; break; }
+            for (int hh = 0; hh < 2 && ok; ++hh)
+              if (!wait_bar(bar_p_full(hh), n & 1, wc)) ok = false;
+            if (!ok) break;
+            tc_fence_after();
+            product(n + 1, 0);
+          }
+          // dQ += dS K as the warpgroups store dS (which also means that they
+          // have read dP(n)).
+          for (int hh = 0; hh < 2 && ok; ++hh) {
+            if (!wait_bar(bar_ds_full(hh), n & 1, wc)) { ok = false; break; }
+            tc_fence_after();
+            acc_half(n, hh, tAcc0, tDS + 32 * hh, 0);
+          }
+          if (!ok) break;
+          mma_commit(bar_acc_b);
+          mma_commit(bar_ring_empty(n % L::kStages));
+          if (more) product(n + 1, 1);
         }
       }
       // Every MMA must finish before the accumulators are read or TMEM freed.
@@ -273,15 +321,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const float sc = p.scale_log2;
     bool ok = true;
     for (int n = 0; n < nblk && ok; ++n) {
-      const bool got = wait_bar(bar_s_full(hh), n & 1, wc);
-      if (__any_sync(0xffffffffu, !got)) { ok = false; break; }
-      tc_fence_after();
       const int c0 = col0_of(n);
       const float* vec = reinterpret_cast<const float*>(smem + L::kRingOff + (n % L::kStages) * L::kSlotBytes +
                                                         2 * L::kTileBytes);
       if (MODE == kModeDKV) {
         // The block's log2-LSE and D arrived with its ring slot (which stays
-        // loaded until this block's P is released).
+        // loaded until this block's dS has been consumed).
         const bool in = wait_bar(bar_ring_full(n % L::kStages), (n / L::kStages) & 1, wc);
         if (__any_sync(0xffffffffu, !in)) { ok = false; break; }
       }
@@ -292,53 +337,90 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       } else {
         edge = CAUSAL && r0 + 127 > c0 + 64 * hh + p.coff;
       }
-#pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        const int col0 = 64 * hh + 32 * c;
-        uint32_t us[32], ud[32];
-        tmem_ld32(tS + col0 + lane_off, us);
-        tmem_ld32(tdP + col0 + lane_off, ud);
+      // ---- P = exp2(S·scale·log2 e − LSE₂) over this half's 64 columns
+      {
+        const bool got = wait_bar(bar_s_full, n & 1, wc);
+        if (__any_sync(0xffffffffu, !got)) { ok = false; break; }
+      }
+      tc_fence_after();
+      float pv[64];
+      {
+        uint32_t us[64];
+        tmem_ld32(tS + 64 * hh + lane_off, *reinterpret_cast<uint32_t(*)[32]>(&us[0]));
+        tmem_ld32(tS + 64 * hh + 32 + lane_off, *reinterpret_cast<uint32_t(*)[32]>(&us[32]));
         tmem_wait_ld();
-        reg_fence32(us);
-        reg_fence32(ud);
-        uint32_t pk[16], qk[16];
+        reg_fence32(*reinterpret_cast<uint32_t(*)[32]>(&us[0]));
+        reg_fence32(*reinterpret_cast<uint32_t(*)[32]>(&us[32]));
+        if (MODE == kModeDQ) {
+          // S has been read: its columns may take the next block's S.
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar_p_full(hh));
+        }
 #pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          float lse_a, lse_b, dv_a, dv_b;
-          if (MODE == kModeDQ) {
-            lse_a = lse_b = lse2_row;
-            dv_a = dv_b = d_row;
-          } else {
-            lse_a = vec[col0 + e];
-            lse_b = vec[col0 + e + 1];
-            dv_a = vec[128 + col0 + e];
-            dv_b = vec[128 + col0 + e + 1];
-          }
-          float pa = ex2_mufu(__uint_as_float(us[e]) * sc - lse_a);
-          float pb = ex2_mufu(__uint_as_float(us[e + 1]) * sc - lse_b);
+        for (int e = 0; e < 64; ++e) {
+          const float lse = (MODE == kModeDQ) ? lse2_row : vec[64 * hh + e];
+          float pe = ex2_mufu(__uint_as_float(us[e]) * sc - lse);
           if (edge) {
-            const int ca = c0 + col0 + e, cb = ca + 1;  // global column: DQ key, DKV query
+            const int ce = c0 + 64 * hh + e;  // global column: DQ key, DKV query
             if (MODE == kModeDQ) {
-              if (ca >= p.Sk || (CAUSAL && ca > row + p.coff)) pa = 0.f;
-              if (cb >= p.Sk || (CAUSAL && cb > row + p.coff)) pb = 0.f;
+              if (ce >= p.Sk || (CAUSAL && ce > row + p.coff)) pe = 0.f;
             } else {
-              if (CAUSAL && row > ca + p.coff) pa = 0.f;
-              if (CAUSAL && row > cb + p.coff) pb = 0.f;
+              if (CAUSAL && row > ce + p.coff) pe = 0.f;
             }
           }
-          const float sa = pa * (__uint_as_float(ud[e]) - dv_a);
-          const float sb = pb * (__uint_as_float(ud[e + 1]) - dv_b);
-          pk[e / 2] = pack_bf16x2(pa, pb);
-          qk[e / 2] = pack_bf16x2(sa, sb);
+          pv[e] = pe;
         }
-        // Packed bf16 pairs over the columns this thread has already read.
-        tmem_st16(tS + 64 * hh + 16 * c + lane_off, pk);
-        tmem_st16(tdP + 64 * hh + 16 * c + lane_off, qk);
       }
+      if (MODE == kModeDKV) {
+        // Packed bf16 P over the first 32 columns of this half of S.
+        uint32_t pk[32];
+#pragma unroll
+        for (int e = 0; e < 32; ++e) pk[e] = pack_bf16x2(pv[2 * e], pv[2 * e + 1]);
+        tmem_st32(tS + 64 * hh + lane_off, pk);
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_p_full(hh));
+      }
+      // ---- dS = P ∘ (dP − D)
+      {
+        const bool got = wait_bar(bar_dp_full, n & 1, wc);
+        if (__any_sync(0xffffffffu, !got)) { ok = false; break; }
+      }
+      tc_fence_after();
+      uint32_t qk[32];
+      {
+        uint32_t ud[64];
+        tmem_ld32(tdP + 64 * hh + lane_off, *reinterpret_cast<uint32_t(*)[32]>(&ud[0]));
+        tmem_ld32(tdP + 64 * hh + 32 + lane_off, *reinterpret_cast<uint32_t(*)[32]>(&ud[32]));
+        tmem_wait_ld();
+        reg_fence32(*reinterpret_cast<uint32_t(*)[32]>(&ud[0]));
+        reg_fence32(*reinterpret_cast<uint32_t(*)[32]>(&ud[32]));
+#pragma unroll
+        for (int e = 0; e < 64; e += 2) {
+          const float da = (MODE == kModeDQ) ? d_row : vec[128 + 64 * hh + e];
+          const float db = (MODE == kModeDQ) ? d_row : vec[128 + 64 * hh + e + 1];
+          qk[e / 2] = pack_bf16x2(pv[e] * (__uint_as_float(ud[e]) - da), pv[e + 1] * (__uint_as_float(ud[e + 1]) - db));
+        }
+      }
+      uint32_t tdst;
+      if (MODE == kModeDQ) {
+        // dS(n) replaces dS(n−1): dQ(n−1) must have completed.
+        if (n > 0) {
+          const bool fr = wait_bar(bar_acc_b, (n - 1) & 1, wc);
+          if (__any_sync(0xffffffffu, !fr)) { ok = false; break; }
+          tc_fence_after();
+        }
+        tdst = tDS + 32 * hh + lane_off;
+      } else {
+        tdst = tdP + 64 * hh + lane_off;  // over the half of dP this thread has read
+      }
+      tmem_st32(tdst, qk);
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar_p_full(hh));
+      if (lane == 0) mbar_arrive(bar_ds_full(hh));
     }
     // ------------------------------------------------------------ outputs
     // Warpgroup hh writes columns [hh·D/2, (hh+1)·D/2) of its rows.
