@@ -35,6 +35,12 @@ CASES = [
     C(1, 2, 200, 520, 128, True, seed=112, causal_align="bottom-right"),
     C(1, 2, 520, 200, 64, True, seed=113, causal_align="bottom-right"),
     C(1, 6, 700, 333, 128, True, seed=114, H_kv=3, causal_align="bottom-right"),
+    # more tiles than SMs (several waves of CTAs): short tiles (two blocks),
+    # causal with grouped heads, and tiles whose rows see no key between
+    # tiles that do
+    C(1, 160, 256, 256, 64, False, seed=115),
+    C(1, 80, 384, 384, 128, True, seed=116, H_kv=16),
+    C(1, 64, 520, 200, 64, True, seed=117, causal_align="bottom-right"),
 ]
 
 
