@@ -457,8 +457,8 @@ int attn_bwd_layout(const void* q, const void* k, const void* v, const void* o, 
   if ((rc = encode_bshd(&a.x2, v, B, Sk, H_kv, d, ks)) != ATTN_OK) return rc;
   if ((rc = encode_bshd(&a.a, q, B, Sq, H, d, qs)) != ATTN_OK) return rc;
   if ((rc = encode_bshd(&a.b, dout, B, Sq, H, d, qs)) != ATTN_OK) return rc;
-  a.p.out0 = dv;
-  a.p.out1 = dk;
+  if ((rc = encode_bshd(&a.o0, dv, B, Sk, H_kv, d, ks)) != ATTN_OK) return rc;
+  if ((rc = encode_bshd(&a.o1, dk, B, Sk, H_kv, d, ks)) != ATTN_OK) return rc;
   a.p.n_rt = static_cast<int>(n_kt);
   a.grid = static_cast<int>(n_kt * B * H_kv);
   a.mode = 1;
@@ -468,8 +468,8 @@ int attn_bwd_layout(const void* q, const void* k, const void* v, const void* o, 
   if ((rc = encode_bshd(&a.x2, dout, B, Sq, H, d, qs)) != ATTN_OK) return rc;
   if ((rc = encode_bshd(&a.a, k, B, Sk, H_kv, d, ks)) != ATTN_OK) return rc;
   if ((rc = encode_bshd(&a.b, v, B, Sk, H_kv, d, ks)) != ATTN_OK) return rc;
-  a.p.out0 = dq;
-  a.p.out1 = nullptr;
+  if ((rc = encode_bshd(&a.o0, dq, B, Sq, H, d, qs)) != ATTN_OK) return rc;
+  a.o1 = a.o0;  // unused by the dQ pass
   a.p.n_rt = (Sq + 127) / 128;
   a.grid = a.p.n_rt * B * H;
   a.mode = 0;

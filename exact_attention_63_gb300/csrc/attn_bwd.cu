@@ -18,7 +18,7 @@ cudaError_t launch_bwd_one(const BwdLaunchArgs& a) {
     if (e != cudaSuccess) return e;
     configured[a.device] = true;
   }
-  attn_bwd_kernel<D, CAUSAL, MODE><<<a.grid, kBwdThreads, smem, a.stream>>>(a.x, a.x2, a.a, a.b, a.p);
+  attn_bwd_kernel<D, CAUSAL, MODE><<<a.grid, kBwdThreads, smem, a.stream>>>(a.x, a.x2, a.a, a.b, a.o0, a.o1, a.p);
   return cudaGetLastError();
 }
 

@@ -45,7 +45,7 @@
 //        dP(n+1) follows as soon as dS(n) — and so the read of dP(n) — is in.
 //
 // TMEM columns: S [0, 128), dP [128, 256), acc0 [256, 256+D) (dQ or dV),
-// acc1 [256+D, 256+2D) (dK; in the dQ pass it holds dS).  P (bf16 pairs)
+// acc1 [256+D, 256+2D) (dK; in the dQ pass two 64-column dS buffers).  P (bf16 pairs)
 // overwrites S's columns and, in DKV, dS overwrites dP's, in the packed layout
 // the forward uses for P.
 #pragma once
@@ -78,8 +78,8 @@ struct BwdLayout {
   static constexpr uint32_t kRingOff = 2 * kTileBytes;
   static constexpr uint32_t kBarOff = kRingOff + kStages * kSlotBytes;
   // barriers: fix_full, ring_full[S], ring_empty[S], s_full, dp_full, p_full[2], ds_full[2],
-  //           acc_a, acc_b, done
-  static constexpr int kNumBars = 1 + 2 * kStages + 9;
+  //           acc_a, acc_b, done, dq_done[2]
+  static constexpr int kNumBars = 1 + 2 * kStages + 11;
   static constexpr uint32_t kMiscOff = kBarOff + 8 * kNumBars;
   static constexpr uint32_t kSmemBytes = kMiscOff + 16 + 1024;
 };
@@ -88,6 +88,7 @@ template <int D, bool CAUSAL, int MODE>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_x2,
                     const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
+                    const __grid_constant__ CUtensorMap tm_o0, const __grid_constant__ CUtensorMap tm_o1,
                     const BwdParams p) {
   using L = BwdLayout<D, MODE>;
   extern __shared__ uint8_t smem_raw[];
@@ -108,8 +109,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   // dS of a half stored (so dP of the half has been read)
   auto bar_ds_full = [&](int hh) { return bar_b0 + 8u * (4 + hh); };
   const uint32_t bar_acc_a = bar_b0 + 8u * 6;    // DKV: dV of the block done (S's columns are free)
-  const uint32_t bar_acc_b = bar_b0 + 8u * 7;    // DKV: dK done (dP's columns free); DQ: dQ done (dS's)
+  const uint32_t bar_acc_b = bar_b0 + 8u * 7;    // DKV: dK of the block done (dP's columns are free)
   const uint32_t bar_done = bar_b0 + 8u * 8;     // every MMA done
+  // DQ: dQ of the blocks using dS buffer i done (that buffer is free); one
+  // barrier per buffer, so each is waited on one phase at a time
+  auto bar_dq_done = [&](int i) { return bar_b0 + 8u * (9 + i); };
   uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMiscOff);
   volatile uint32_t* const abort_flag = reinterpret_cast<volatile uint32_t*>(smem + L::kMiscOff + 4);
 
@@ -163,6 +167,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     mbar_init(bar_acc_a, 1);
     mbar_init(bar_acc_b, 1);
     mbar_init(bar_done, 1);
+    for (int i = 0; i < 2; ++i) mbar_init(bar_dq_done(i), 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     fence_proxy_async_smem();
   }
@@ -171,9 +176,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const uint32_t tmem = *tmem_slot;
   const WaitCtx wc{abort_flag, p.status, p.timeout_ns};
   const uint32_t tS = tmem, tdP = tmem + 128, tAcc0 = tmem + 256, tAcc1 = tmem + 256 + D;
-  // dQ pass: dS gets columns of its own (where dK sits in the other pass), so
-  // the next block's dP need not wait for dQ += dS K.
-  const uint32_t tDS = tAcc1;
+  // dQ pass: dS gets columns of its own (where dK sits in the other pass), two
+  // buffers of 64, so neither the next block's dP nor its dS waits for the
+  // previous dQ += dS K.
+  auto tDS = [&](int n) { return tAcc1 + 64u * (n & 1); };
 
   if (warp == kBwdLoaderWarp) {
     // ============================================================ loader
@@ -257,6 +263,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           }
           if (!ok) break;
           mma_commit(bar_acc_a);
+          // S(n+1) overwrites P(n): it goes in as soon as dV(n) has completed
+          // (a completion barrier: MMAs into different accumulators are not
+          // ordered), ahead of dK(n), so the warpgroups find it ready when
+          // they have stored dS(n).
+          if (more) {
+            if (!wait_bar(bar_ring_full((n + 1) % L::kStages), ((n + 1) / L::kStages) & 1, wc)) { ok = false; break; }
+            if (!wait_bar(bar_acc_a, n & 1, wc)) { ok = false; break; }
+            tc_fence_after();
+            product(n + 1, 0);
+          }
           // dK += dSᵀ Q.
           for (int hh = 0; hh < 2 && ok; ++hh) {
             if (!wait_bar(bar_ds_full(hh), n & 1, wc)) { ok = false; break; }
@@ -266,14 +282,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           if (!ok) break;
           mma_commit(bar_acc_b);
           mma_commit(bar_ring_empty(n % L::kStages));  // A(n), B(n) no longer read
+          // dP(n+1) overwrites dS(n): dK must have completed.
           if (more) {
-            if (!wait_bar(bar_ring_full((n + 1) % L::kStages), ((n + 1) / L::kStages) & 1, wc)) { ok = false; break; }
-            // S(n+1) overwrites P(n): dV must have completed; dP(n+1)
-            // overwrites dS(n): dK must have completed (completion
-            // barriers; MMAs into different accumulators are not ordered).
-            if (!wait_bar(bar_acc_a, n & 1, wc)) { ok = false; break; }
-            tc_fence_after();
-            product(n + 1, 0);
             if (!wait_bar(bar_acc_b, n & 1, wc)) { ok = false; break; }
             tc_fence_after();
             product(n + 1, 1);
@@ -293,10 +303,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           for (int hh = 0; hh < 2 && ok; ++hh) {
             if (!wait_bar(bar_ds_full(hh), n & 1, wc)) { ok = false; break; }
             tc_fence_after();
-            acc_half(n, hh, tAcc0, tDS + 32 * hh, 0);
+            acc_half(n, hh, tAcc0, tDS(n) + 32 * hh, 0);
           }
           if (!ok) break;
-          mma_commit(bar_acc_b);
+          mma_commit(bar_dq_done(n & 1));
           mma_commit(bar_ring_empty(n % L::kStages));
           if (more) product(n + 1, 1);
         }
@@ -406,13 +416,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       }
       uint32_t tdst;
       if (MODE == kModeDQ) {
-        // dS(n) replaces dS(n−1): dQ(n−1) must have completed.
-        if (n > 0) {
-          const bool fr = wait_bar(bar_acc_b, (n - 1) & 1, wc);
+        // dS(n) replaces dS(n−2) in buffer n & 1: dQ(n−2) must have completed
+        // (phase (n−2)/2 of that buffer's barrier).
+        if (n >= 2) {
+          const bool fr = wait_bar(bar_dq_done(n & 1), ((n - 2) >> 1) & 1, wc);
           if (__any_sync(0xffffffffu, !fr)) { ok = false; break; }
           tc_fence_after();
         }
-        tdst = tDS + 32 * hh + lane_off;
+        tdst = tDS(n) + 32 * hh + lane_off;
       } else {
         tdst = tdP + 64 * hh + lane_off;  // over the half of dP this thread has read
       }
@@ -423,43 +434,71 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       if (lane == 0) mbar_arrive(bar_ds_full(hh));
     }
     // ------------------------------------------------------------ outputs
-    // Warpgroup hh writes columns [hh·D/2, (hh+1)·D/2) of its rows.
+    // The tile's outputs leave by TMA store (rows beyond the tensor are
+    // clipped by the copy), staged with the 128-byte swizzle in the X / X2
+    // buffers, which are free once the issuer's last commit has completed:
+    // every MMA, the last products included, is done then.  Warpgroup hh
+    // stages columns [hh·D/2, (hh+1)·D/2) of its rows.
     bool have = nblk > 0 && ok;
     if (have) {
-      // The issuer's last commit: every MMA of the tile has completed.
       const bool fin = wait_bar(bar_done, 0, wc);
       if (__any_sync(0xffffffffu, !fin)) have = false;
       tc_fence_after();
     }
-    const int rows_total = (MODE == kModeDQ) ? p.Sq : p.Sk;
-    const int heads_out = h_rows;
-    for (int o = 0; o < (MODE == kModeDQ ? 1 : 2) && (ok || nblk == 0); ++o) {
-      const uint32_t tacc = (o == 0 ? tAcc0 : tAcc1) + lane_off + hh * (D / 2);
-      const float mul = (MODE == kModeDQ || o == 1) ? p.scale : 1.f;
-      uint16_t* const out = static_cast<uint16_t*>(o == 0 ? p.out0 : p.out1) +
-                            ((static_cast<size_t>(b) * rows_total + row) * heads_out + h) * D + hh * (D / 2);
+    // One decision for all eight warps (they meet at a named barrier below):
+    // write the outputs unless a wait anywhere in the CTA ran out.
+    uint32_t good;
+    {
+      const uint32_t mine = ((nblk == 0 || have) && *abort_flag == 0u) ? 1u : 0u;
+      asm volatile(
+          "{\n\t.reg .pred p, q;\n\t"
+          "setp.ne.u32 q, %1, 0;\n\t"
+          "bar.red.and.pred p, 1, 256, q;\n\t"
+          "selp.u32 %0, 1, 0, p;\n\t}"
+          : "=r"(good)
+          : "r"(mine)
+          : "memory");
+    }
+    if (good) {
+      constexpr int kOut = (MODE == kModeDQ) ? 1 : 2;
 #pragma unroll
-      for (int c = 0; c < D / 64; ++c) {
-        uint32_t x[32];
-        if (have) {
-          tmem_ld32(tacc + 32 * c, x);
-          tmem_wait_ld();
-          reg_fence32(x);
-        } else {
+      for (int o = 0; o < kOut; ++o) {
+        const uint32_t tacc = (o == 0 ? tAcc0 : tAcc1) + lane_off + hh * (D / 2);
+        const float mul = (MODE == kModeDQ || o == 1) ? p.scale : 1.f;
+        uint8_t* const stage = smem + L::kXOff + o * L::kTileBytes;
 #pragma unroll
-          for (int i = 0; i < 32; ++i) x[i] = 0u;  // rows that see no column: zero gradient
-        }
-        if (row < rows_total) {
+        for (int c = 0; c < D / 64; ++c) {
+          uint32_t x[32];
+          if (nblk > 0) {
+            tmem_ld32(tacc + 32 * c, x);
+            tmem_wait_ld();
+            reg_fence32(x);
+          } else {
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
+            for (int i = 0; i < 32; ++i) x[i] = 0u;  // rows that see no column: zero gradient
+          }
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {  // four 16-byte chunks of 8 values
             uint4 w;
             w.x = pack_bf16x2(mul * __uint_as_float(x[8 * q]), mul * __uint_as_float(x[8 * q + 1]));
             w.y = pack_bf16x2(mul * __uint_as_float(x[8 * q + 2]), mul * __uint_as_float(x[8 * q + 3]));
             w.z = pack_bf16x2(mul * __uint_as_float(x[8 * q + 4]), mul * __uint_as_float(x[8 * q + 5]));
             w.w = pack_bf16x2(mul * __uint_as_float(x[8 * q + 6]), mul * __uint_as_float(x[8 * q + 7]));
-            *reinterpret_cast<uint4*>(out + 32 * c + 8 * q) = w;
+            const int col = hh * (D / 2) + 32 * c + 8 * q;
+            const int chunk = (col & 63) >> 3;
+            *reinterpret_cast<uint4*>(stage + (col >> 6) * L::kSlabBytes + r * 128 + ((chunk ^ (r & 7)) << 4)) = w;
           }
         }
+      }
+      fence_proxy_async_smem();
+      asm volatile("bar.sync 1, 256;" ::: "memory");
+      if (threadIdx.x == 0) {
+#pragma unroll
+        for (int o = 0; o < kOut; ++o)
+          for (int sl = 0; sl < L::kSlabs; ++sl)
+            tma_store_4d(o == 0 ? &tm_o0 : &tm_o1, sX + o * L::kTileBytes + sl * L::kSlabBytes, 64 * sl, h, r0, b);
+        tma_store_commit();
+        tma_store_wait_read0();  // shared memory must stay valid until the copy has read it
       }
     }
   }

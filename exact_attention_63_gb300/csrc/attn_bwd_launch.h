@@ -10,8 +10,6 @@
 namespace attn {
 
 struct BwdParams {
-  void* out0;          // dQ pass: dQ [B, Sq, H, D]; dK/dV pass: dV [B, Sk, H, D]   (bf16, dense)
-  void* out1;          // dK/dV pass: dK [B, Sk, H, D]
   const float* lse2;   // [B·H, pitch]: LSE · log2(e) of each query row; +inf beyond Sq
   const float* dvec;   // [B·H, pitch]: D = rowsum(dO ∘ O); 0 beyond Sq
   unsigned int* status;
@@ -26,6 +24,8 @@ struct BwdParams {
 
 struct BwdLaunchArgs {
   CUtensorMap x, x2, a, b;  // row tiles X, X2 and the streamed A, B (4-D maps as in the forward)
+  CUtensorMap o0, o1;       // outputs (bf16, dense): dQ pass o0 = dQ [B, Sq, H, D]; dK/dV pass o0 = dV, o1 = dK
+                            // [B, Sk, H_kv, D]
   BwdParams p;
   int grid;
   int mode;                 // 0: dQ pass, 1: dK/dV pass
