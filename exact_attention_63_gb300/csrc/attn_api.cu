@@ -5,6 +5,7 @@
 #include <cstdint>
 #include <cstdio>
 #include <cstring>
+#include <mutex>
 
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -214,6 +215,182 @@ int launch(attn::LaunchArgs& a, const Opts& op, int dev, int d, int causal, floa
 }
 
 }  // namespace
+
+namespace attn {
+namespace {
+
+// attn_fwd_host's pipeline: up to kHostChunks slices of the problem, each
+// copied in on `in`, computed on the caller's stream and copied out on `out`,
+// so the copies of one slice overlap the kernel and the copies of the others
+// (host→device and device→host use separate copy engines).  Created on a
+// device's first call, kept for the process.
+constexpr int kHostChunks = 4;
+struct HostPipe {
+  std::mutex mu;  // one enqueue sequence at a time (the events are reused)
+  bool ready = false;
+  cudaStream_t in = nullptr, out = nullptr;
+  cudaEvent_t start = nullptr, end = nullptr, in_done[kHostChunks] = {}, k_done[kHostChunks] = {};
+};
+HostPipe g_pipe[kMaxDevices];
+
+int make_pipe(HostPipe& hp) {
+  if (hp.ready) return ATTN_OK;
+  cudaError_t e;
+  if ((e = cudaStreamCreateWithFlags(&hp.in, cudaStreamNonBlocking)) != cudaSuccess) return fail_cuda(e, "stream");
+  if ((e = cudaStreamCreateWithFlags(&hp.out, cudaStreamNonBlocking)) != cudaSuccess) return fail_cuda(e, "stream");
+  cudaEvent_t* evs[2 + 2 * kHostChunks] = {&hp.start, &hp.end};
+  for (int c = 0; c < kHostChunks; ++c) {
+    evs[2 + c] = &hp.in_done[c];
+    evs[2 + kHostChunks + c] = &hp.k_done[c];
+  }
+  for (cudaEvent_t* ev : evs)
+    if ((e = cudaEventCreateWithFlags(ev, cudaEventDisableTiming)) != cudaSuccess) return fail_cuda(e, "event");
+  hp.ready = true;
+  return ATTN_OK;
+}
+
+}  // namespace
+
+int fwd_host(const void* q_h, const void* k_h, const void* v_h, void* o_h, float* lse_h, int B, int H, int Sq, int Sk,
+             int d, float scale, int causal, void* workspace, size_t workspace_bytes, cudaStream_t stream,
+             bool pipelined) {
+  if (q_h == nullptr || k_h == nullptr || v_h == nullptr || o_h == nullptr || lse_h == nullptr) return ATTN_ERR_NULL;
+  if (B < 1 || H < 1 || Sq < 1 || Sk < 1) return ATTN_ERR_SHAPE;
+  if (d != 64 && d != 128) return ATTN_ERR_HEAD_DIM;
+  const size_t need = attn_fwd_host_workspace_size(B, H, Sq, Sk, d);
+  if (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 || workspace_bytes < need)
+    return ATTN_ERR_WORKSPACE;
+  auto up = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
+  const size_t qb = static_cast<size_t>(B) * Sq * H * d * 2, kb = static_cast<size_t>(B) * Sk * H * d * 2;
+  const size_t lb = static_cast<size_t>(B) * H * Sq * 4;
+  char* w = static_cast<char*>(workspace);
+  char* q_d = w;
+  char* k_d = w + up(qb);
+  char* v_d = w + up(qb) + up(kb);
+  char* o_d = w + up(qb) + 2 * up(kb);
+  char* l_d = w + 2 * up(qb) + 2 * up(kb);
+  // Every argument error is reported before anything is enqueued.
+  int rc = check_args(q_d, k_d, v_d, o_d, l_d, B, H, Sq, Sk, d, scale);
+  if (rc != ATTN_OK) return rc;
+  const char* qh = static_cast<const char*>(q_h);
+  const char* kh = static_cast<const char*>(k_h);
+  const char* vh = static_cast<const char*>(v_h);
+  char* oh = static_cast<char*>(o_h);
+  char* lh = reinterpret_cast<char*>(lse_h);
+  cudaError_t e;
+  // Head slices need their LSE rows 16-byte aligned (Sq a multiple of 4).
+  if (!pipelined || (B == 1 && (H == 1 || Sq % 4 != 0))) {
+    // One slice, all on the caller's stream.
+    if ((e = cudaMemcpyAsync(q_d, qh, qb, cudaMemcpyHostToDevice, stream)) != cudaSuccess) return fail_cuda(e, "copy q");
+    if ((e = cudaMemcpyAsync(k_d, kh, kb, cudaMemcpyHostToDevice, stream)) != cudaSuccess) return fail_cuda(e, "copy k");
+    if ((e = cudaMemcpyAsync(v_d, vh, kb, cudaMemcpyHostToDevice, stream)) != cudaSuccess) return fail_cuda(e, "copy v");
+    rc = attn_fwd(q_d, k_d, v_d, o_d, reinterpret_cast<float*>(l_d), B, H, Sq, Sk, d, scale, causal, stream);
+    if (rc != ATTN_OK) return rc;
+    if ((e = cudaMemcpyAsync(oh, o_d, qb, cudaMemcpyDeviceToHost, stream)) != cudaSuccess) return fail_cuda(e, "copy o");
+    if ((e = cudaMemcpyAsync(lh, l_d, lb, cudaMemcpyDeviceToHost, stream)) != cudaSuccess)
+      return fail_cuda(e, "copy lse");
+    return ATTN_OK;
+  }
+  int dev = -1;
+  if ((rc = current_device(&dev)) != ATTN_OK) return rc;
+  HostPipe& hp = g_pipe[dev];
+  std::lock_guard<std::mutex> lock(hp.mu);
+  if ((rc = make_pipe(hp)) != ATTN_OK) return rc;
+  // Slices of the batch, or of the heads when B = 1 (strided 2-D copies; the
+  // kernel reads the dense layout through element strides).
+  const bool by_batch = B >= 2;
+  const int units = by_batch ? B : H;
+  const int nc = units < kHostChunks ? units : kHostChunks;
+  const size_t row_b = static_cast<size_t>(H) * d * 2;  // bytes of one (b, s) row of q, k, v, o
+  if ((e = cudaEventRecord(hp.start, stream)) != cudaSuccess) return fail_cuda(e, "record");
+  if ((e = cudaStreamWaitEvent(hp.in, hp.start, 0)) != cudaSuccess) return fail_cuda(e, "wait");
+  if ((e = cudaStreamWaitEvent(hp.out, hp.start, 0)) != cudaSuccess) return fail_cuda(e, "wait");
+  rc = ATTN_OK;
+  for (int c = 0; c < nc && rc == ATTN_OK; ++c) {
+    const int u0 = static_cast<int>(static_cast<long long>(units) * c / nc);
+    const int nu = static_cast<int>(static_cast<long long>(units) * (c + 1) / nc) - u0;
+    size_t qo, ko, lo, ls;  // byte offsets of the slice in q/o, k/v, lse, and its lse bytes
+    if (by_batch) {
+      qo = static_cast<size_t>(u0) * Sq * row_b;
+      ko = static_cast<size_t>(u0) * Sk * row_b;
+      lo = static_cast<size_t>(u0) * H * Sq * 4;
+      ls = static_cast<size_t>(nu) * H * Sq * 4;
+      const size_t qs = static_cast<size_t>(nu) * Sq * row_b, ks = static_cast<size_t>(nu) * Sk * row_b;
+      if ((e = cudaMemcpyAsync(q_d + qo, qh + qo, qs, cudaMemcpyHostToDevice, hp.in)) != cudaSuccess ||
+          (e = cudaMemcpyAsync(k_d + ko, kh + ko, ks, cudaMemcpyHostToDevice, hp.in)) != cudaSuccess ||
+          (e = cudaMemcpyAsync(v_d + ko, vh + ko, ks, cudaMemcpyHostToDevice, hp.in)) != cudaSuccess) {
+        rc = fail_cuda(e, "copy in");
+        break;
+      }
+    } else {
+      qo = ko = static_cast<size_t>(u0) * d * 2;
+      lo = static_cast<size_t>(u0) * Sq * 4;
+      ls = static_cast<size_t>(nu) * Sq * 4;
+      const size_t wb = static_cast<size_t>(nu) * d * 2;
+      if ((e = cudaMemcpy2DAsync(q_d + qo, row_b, qh + qo, row_b, wb, Sq, cudaMemcpyHostToDevice, hp.in)) !=
+              cudaSuccess ||
+          (e = cudaMemcpy2DAsync(k_d + ko, row_b, kh + ko, row_b, wb, Sk, cudaMemcpyHostToDevice, hp.in)) !=
+              cudaSuccess ||
+          (e = cudaMemcpy2DAsync(v_d + ko, row_b, vh + ko, row_b, wb, Sk, cudaMemcpyHostToDevice, hp.in)) !=
+              cudaSuccess) {
+        rc = fail_cuda(e, "copy in");
+        break;
+      }
+    }
+    if ((e = cudaEventRecord(hp.in_done[c], hp.in)) != cudaSuccess ||
+        (e = cudaStreamWaitEvent(stream, hp.in_done[c], 0)) != cudaSuccess) {
+      rc = fail_cuda(e, "order");
+      break;
+    }
+    float* lslice = reinterpret_cast<float*>(l_d + lo);
+    if (by_batch) {
+      rc = attn_fwd(q_d + qo, k_d + ko, v_d + ko, o_d + qo, lslice, nu, H, Sq, Sk, d, scale, causal, stream);
+    } else {
+      attn_layout lay;
+      std::memset(&lay, 0, sizeof(lay));
+      lay.struct_size = sizeof(lay);
+      lay.causal_align = ATTN_CAUSAL_TOP_LEFT;
+      const long long hd = static_cast<long long>(H) * d;
+      for (long long* st : {lay.q_strides, lay.o_strides}) {
+        st[0] = Sq * hd;
+        st[1] = hd;
+        st[2] = d;
+      }
+      for (long long* st : {lay.k_strides, lay.v_strides}) {
+        st[0] = Sk * hd;
+        st[1] = hd;
+        st[2] = d;
+      }
+      rc = attn_fwd_layout(q_d + qo, k_d + ko, v_d + ko, o_d + qo, lslice, 1, nu, Sq, Sk, d, scale, causal, &lay,
+                           nullptr, stream);
+    }
+    if (rc != ATTN_OK) break;
+    if ((e = cudaEventRecord(hp.k_done[c], stream)) != cudaSuccess ||
+        (e = cudaStreamWaitEvent(hp.out, hp.k_done[c], 0)) != cudaSuccess) {
+      rc = fail_cuda(e, "order");
+      break;
+    }
+    if (by_batch) {
+      e = cudaMemcpyAsync(oh + qo, o_d + qo, static_cast<size_t>(nu) * Sq * row_b, cudaMemcpyDeviceToHost, hp.out);
+    } else {
+      e = cudaMemcpy2DAsync(oh + qo, row_b, o_d + qo, row_b, static_cast<size_t>(nu) * d * 2, Sq,
+                            cudaMemcpyDeviceToHost, hp.out);
+    }
+    if (e == cudaSuccess) e = cudaMemcpyAsync(lh + lo, l_d + lo, ls, cudaMemcpyDeviceToHost, hp.out);
+    if (e != cudaSuccess) rc = fail_cuda(e, "copy out");
+  }
+  // Whatever happened, the caller's stream waits for everything enqueued on
+  // the internal streams.
+  cudaError_t e1 = cudaEventRecord(hp.end, hp.out), e2 = cudaSuccess, e3 = cudaSuccess, e4 = cudaSuccess;
+  if (e1 == cudaSuccess) e2 = cudaStreamWaitEvent(stream, hp.end, 0);
+  e3 = cudaEventRecord(hp.end, hp.in);  // (the copies in precede the kernels, which precede the copies out)
+  if (e3 == cudaSuccess) e4 = cudaStreamWaitEvent(stream, hp.end, 0);
+  if (rc == ATTN_OK && (e1 != cudaSuccess || e2 != cudaSuccess || e3 != cudaSuccess || e4 != cudaSuccess))
+    rc = fail_cuda(e1 != cudaSuccess ? e1 : e2 != cudaSuccess ? e2 : e3 != cudaSuccess ? e3 : e4, "join");
+  return rc;
+}
+
+}  // namespace attn
 
 extern "C" {
 
@@ -496,31 +673,8 @@ size_t attn_fwd_host_workspace_size(int B, int H, int Sq, int Sk, int d) {
 int attn_fwd_host(const void* q_h, const void* k_h, const void* v_h, void* o_h, float* lse_h, int B, int H, int Sq,
                   int Sk, int d, float scale, int causal, void* workspace, size_t workspace_bytes,
                   cudaStream_t stream) {
-  if (q_h == nullptr || k_h == nullptr || v_h == nullptr || o_h == nullptr || lse_h == nullptr) return ATTN_ERR_NULL;
-  if (B < 1 || H < 1 || Sq < 1 || Sk < 1) return ATTN_ERR_SHAPE;
-  if (d != 64 && d != 128) return ATTN_ERR_HEAD_DIM;
-  const size_t need = attn_fwd_host_workspace_size(B, H, Sq, Sk, d);
-  if (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 || workspace_bytes < need)
-    return ATTN_ERR_WORKSPACE;
-  auto up = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
-  const size_t qb = static_cast<size_t>(B) * Sq * H * d * 2, kb = static_cast<size_t>(B) * Sk * H * d * 2;
-  const size_t lb = static_cast<size_t>(B) * H * Sq * 4;
-  char* w = static_cast<char*>(workspace);
-  void* q_d = w;
-  void* k_d = w + up(qb);
-  void* v_d = w + up(qb) + up(kb);
-  void* o_d = w + up(qb) + 2 * up(kb);
-  float* l_d = reinterpret_cast<float*>(w + 2 * up(qb) + 2 * up(kb));
-  cudaError_t e;
-  if ((e = cudaMemcpyAsync(q_d, q_h, qb, cudaMemcpyHostToDevice, stream)) != cudaSuccess) return fail_cuda(e, "copy q");
-  if ((e = cudaMemcpyAsync(k_d, k_h, kb, cudaMemcpyHostToDevice, stream)) != cudaSuccess) return fail_cuda(e, "copy k");
-  if ((e = cudaMemcpyAsync(v_d, v_h, kb, cudaMemcpyHostToDevice, stream)) != cudaSuccess) return fail_cuda(e, "copy v");
-  int rc = attn_fwd(q_d, k_d, v_d, o_d, l_d, B, H, Sq, Sk, d, scale, causal, stream);
-  if (rc != ATTN_OK) return rc;
-  if ((e = cudaMemcpyAsync(o_h, o_d, qb, cudaMemcpyDeviceToHost, stream)) != cudaSuccess) return fail_cuda(e, "copy o");
-  if ((e = cudaMemcpyAsync(lse_h, l_d, lb, cudaMemcpyDeviceToHost, stream)) != cudaSuccess)
-    return fail_cuda(e, "copy lse");
-  return ATTN_OK;
+  return attn::fwd_host(q_h, k_h, v_h, o_h, lse_h, B, H, Sq, Sk, d, scale, causal, workspace, workspace_bytes,
+                        stream, true);
 }
 
 int attn_get_status(cudaStream_t stream) {

@@ -30,6 +30,13 @@ inline bool poly_mask_supported(uint32_t m) {
   return false;
 }
 
+// attn_fwd_host with or without the chunked copy/compute pipeline (the
+// single-slice form uses only the caller's stream and creates no streams or
+// events: attn_fwd_host_static uses it).
+int fwd_host(const void* q_h, const void* k_h, const void* v_h, void* o_h, float* lse_h, int B, int H, int Sq, int Sk,
+             int d, float scale, int causal, void* workspace, size_t workspace_bytes, cudaStream_t stream,
+             bool pipelined);
+
 cudaError_t launch_fwd_d64(const LaunchArgs& a);
 cudaError_t launch_fwd_d64_causal(const LaunchArgs& a);
 cudaError_t launch_fwd_d128(const LaunchArgs& a);

@@ -8,6 +8,7 @@
 #include <cuda_runtime.h>
 
 #include "attn_gb300.h"
+#include "attn_launch.h"
 
 namespace {
 
@@ -51,6 +52,7 @@ extern "C" int attn_fwd_host_static(const void* q_h, const void* k_h, const void
   // Every byte the kernel and the copies read back is written earlier in the
   // same call (q/k/v by the host-to-device copies, o/lse by the kernel), so
   // nothing in the array needs clearing between calls.
-  return attn_fwd_host(q_h, k_h, v_h, o_h, lse_h, B, H, Sq, Sk, d, scale, causal, g_static_addr[dev],
-                       kStaticBytes, stream);
+  // The single-slice form: it creates no streams or events either.
+  return attn::fwd_host(q_h, k_h, v_h, o_h, lse_h, B, H, Sq, Sk, d, scale, causal, g_static_addr[dev], kStaticBytes,
+                        stream, false);
 }

@@ -262,10 +262,19 @@ int attn_bwd_layout(const void* q, const void* k, const void* v, const void* o, 
  *   workspace     : caller-owned DEVICE buffer of at least
  *                   attn_fwd_host_workspace_size(B, H, Sq, Sk, d) bytes,
  *                   256-byte aligned; it holds device copies of q, k, v, o, lse.
- * Enqueues, on `stream`: three host→device copies, the attention kernel, and
- * two device→host copies (one cudaMemcpyAsync per buffer).  The call returns
- * after enqueueing; synchronise `stream` before reading o_h / lse_h.  Host
- * buffers should be page-locked for the copies to be asynchronous.
+ * The problem is cut into up to four slices (of the batch, or of the heads
+ * when B = 1 and Sq is a multiple of 4, whose rows are then copied as strided
+ * 2-D copies; otherwise it runs as one slice on `stream`); each slice's
+ * host→device copies run on a library-owned stream, its kernel on `stream`
+ * and its device→host copies on a second library-owned stream, ordered by
+ * events, so one slice's copies overlap the others' compute and copies.  The
+ * library creates these two streams and their events on a device's first
+ * call and keeps them; enqueueing is serialised per device by a mutex.
+ * `stream` waits for every copy before any later work on it runs, and the
+ * first copy waits for earlier work on `stream`.  The call returns after
+ * enqueueing; synchronise `stream` before reading o_h / lse_h.  Host buffers
+ * should be page-locked for the copies to be asynchronous.  Argument errors
+ * are returned before anything is enqueued.
  */
 size_t attn_fwd_host_workspace_size(int B, int H, int Sq, int Sk, int d);
 int attn_fwd_host(const void* q_h, const void* k_h, const void* v_h, void* o_h, float* lse_h,
@@ -283,7 +292,8 @@ int attn_fwd_host(const void* q_h, const void* k_h, const void* v_h, void* o_h, 
  * Such callers pass host inputs and outputs only; the device staging area is
  * a fixed array of ATTN_STATIC_WORKSPACE_BYTES (32 MiB) inside this library,
  * which every GPU that loads the library keeps until the process exits.
- *   Arguments and layouts as attn_fwd_host, without the workspace.
+ *   Arguments and layouts as attn_fwd_host, without the workspace.  Everything
+ *   runs on `stream` in one slice (no library streams or events are created).
  *   Problems whose attn_fwd_host_workspace_size() exceeds
  *   ATTN_STATIC_WORKSPACE_BYTES are rejected with ATTN_ERR_STATIC_LIMIT
  *   before anything is enqueued.

@@ -155,15 +155,55 @@ def test_side_stream():
     assert_close(o, lse, O_ref, L_ref, w.name)
 
 
-def test_host_buffer_entry_point_matches_device_path():
-    need_gpu()
-    w = inputs.custom(2, 2, 700, 600, 128, True, seed=47)
-    q, k, v = inputs.make_inputs(w)
+# Host-buffer call: one slice (B = H = 1; B = 1 with Sq not a multiple of 4),
+# batch slices (B = 2; B = 5 in four uneven slices) and head slices with
+# strided copies (B = 1).
+HOST_CASES = [
+    inputs.custom(2, 2, 700, 600, 128, True, seed=47),
+    inputs.custom(5, 2, 300, 260, 64, False, seed=48),
+    inputs.custom(1, 3, 777, 1000, 128, True, seed=49),
+    inputs.custom(1, 3, 780, 1000, 128, True, seed=54),
+    inputs.custom(1, 6, 256, 256, 64, False, seed=50),
+    inputs.custom(1, 1, 300, 300, 64, True, seed=51),
+]
+
+
+def _host_call(w, q, k, v, ws):
     qh, kh, vh = (t.pin_memory() for t in (q, k, v))
-    oh = torch.empty_like(qh).pin_memory()
-    lh = torch.empty((w.B, w.H, w.Sq), dtype=torch.float32).pin_memory()
-    ws = torch.empty(attn.workspace_size(w.B, w.H, w.Sq, w.Sk, w.d), dtype=torch.uint8, device="cuda")
+    oh = torch.full_like(qh, float("nan")).pin_memory()
+    lh = torch.full((w.B, w.H, w.Sq), float("nan"), dtype=torch.float32).pin_memory()
     attn.attn_fwd_host(qh, kh, vh, oh, lh, w.causal, w.scale, ws)
     torch.cuda.synchronize()
+    return oh, lh
+
+
+@pytest.mark.parametrize("w", HOST_CASES, ids=lambda w: w.name)
+def test_host_buffer_entry_point_matches_device_path(w):
+    """Every slice of the pipelined host call lands where it belongs: the
+    outputs equal the device call's bit for bit."""
+    need_gpu()
+    q, k, v = inputs.make_inputs(w)
+    ws = torch.empty(attn.workspace_size(w.B, w.H, w.Sq, w.Sk, w.d), dtype=torch.uint8, device="cuda")
+    oh, lh = _host_call(w, q, k, v, ws)
     o, lse = run(w, q, k, v)
     assert torch.equal(oh, o.cpu()) and torch.equal(lh, lse.cpu())
+
+
+def test_host_buffer_calls_back_to_back():
+    """Two calls enqueued without a synchronisation in between, reusing one
+    workspace: the second waits for the first's copies out."""
+    need_gpu()
+    w1 = inputs.custom(4, 2, 512, 512, 128, False, seed=52)
+    w2 = inputs.custom(4, 2, 512, 512, 128, False, seed=53)
+    ws = torch.empty(attn.workspace_size(4, 2, 512, 512, 128), dtype=torch.uint8, device="cuda")
+    outs = []
+    for w in (w1, w2):
+        q, k, v = (t.pin_memory() for t in inputs.make_inputs(w))
+        oh = torch.empty_like(q).pin_memory()
+        lh = torch.empty((w.B, w.H, w.Sq), dtype=torch.float32).pin_memory()
+        attn.attn_fwd_host(q, k, v, oh, lh, w.causal, w.scale, ws)
+        outs.append((w, q, k, v, oh, lh))
+    torch.cuda.synchronize()
+    for w, q, k, v, oh, lh in outs:
+        o, lse = run(w, q, k, v)
+        assert torch.equal(oh, o.cpu()) and torch.equal(lh, lse.cpu())
