@@ -95,6 +95,11 @@ constexpr int kSWarp = 10;
 constexpr int kStoreWarp = 11;
 constexpr int kSoftmaxWarps = 8;
 constexpr uint32_t kTmemCols = 512;
+// Packed sequences without a causal mask: up to this many sequences, each
+// CTA builds a prefix table of their tile counts in shared memory and walks
+// only the tiles that hold rows (see tile_info).
+constexpr int kSeqTableCap = 4095;
+constexpr uint32_t kSeqTableBytes = (kSeqTableCap + 1) * 4;
 
 struct FwdParams {
   void* o;                       // bf16 [B, Sq, H, D] (element strides o_sb, o_ss, o_sh)
@@ -140,6 +145,9 @@ struct Layout {
   static constexpr int kNumBars = 2 + 2 * kStages + 3 * kSBufs + 1 + 2 + 2 + 2 + 2;
   static constexpr uint32_t kMiscOff = kBarOff + 8 * kNumBars;  // tmem base (4 B) + abort flag (4 B)
   static constexpr uint32_t kSmemBytes = kMiscOff + 16 + 1024;  // + slack to align the base to 1024
+  // (packed sequences) the sequence tile table, in the extra kSeqTableBytes
+  // those launches request
+  static constexpr uint32_t kTableOff = kMiscOff + 16;
   __device__ static constexpr uint32_t col_s(int buf) { return 128u * buf; }
   __device__ static constexpr uint32_t col_o(int half) {
     return 128u * kSBufs + static_cast<uint32_t>(D) * half;
@@ -212,11 +220,28 @@ __device__ __forceinline__ bool runs(const Tile& t) {
 // Tile order.  Causal: heaviest query tiles first (longest-processing-time
 // order for the static round-robin below).  Otherwise: the tiles of one head
 // are consecutive, so CTAs working side by side share that head's K/V in L2.
+//
+// Packed sequences without a causal mask, given seq_tab (seq_tab[s] = H × the
+// q tiles of sequences before s; seq_tab[B] = all): the index runs over the
+// tiles that hold rows only, in the same order (sequence, head, q tile), so
+// the round-robin over CTAs does not deal out the empty slots of sequences
+// shorter than the longest (which left some CTAs with far more work).
 template <bool CAUSAL, bool VARLEN>
-__device__ __forceinline__ Tile tile_info(int idx, const FwdParams& p) {
+__device__ __forceinline__ Tile tile_info(int idx, const FwdParams& p, const int* seq_tab = nullptr) {
   const int BH = p.B * p.H;
   int qt, bh;
-  if (CAUSAL) {
+  if (VARLEN && !CAUSAL && seq_tab != nullptr) {
+    // The sequence s with seq_tab[s] ≤ idx < seq_tab[s+1] (it has a tile).
+    int lo = 0, hi = p.B;
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (seq_tab[mid] <= idx) lo = mid; else hi = mid;
+    }
+    const int local = idx - seq_tab[lo];
+    const int c = (seq_tab[lo + 1] - seq_tab[lo]) / p.H;  // q tiles of sequence lo
+    bh = lo * p.H + local / c;
+    qt = local % c;
+  } else if (CAUSAL) {
     qt = p.n_qt - 1 - idx / BH;
     bh = idx % BH;
   } else {
@@ -287,11 +312,12 @@ __device__ __forceinline__ long long lse0_of(const Tile& t, const FwdParams& p) 
 }
 
 // The first tile index ≥ idx (stepping by stride) that the pipeline runs, with
-// its description in T; p.n_tiles or more when there is none.
+// its description in T; n_tiles or more when there is none.
 template <bool CAUSAL, bool VARLEN>
-__device__ __forceinline__ int next_running(int idx, int stride, const FwdParams& p, Tile& T) {
-  for (; idx < p.n_tiles; idx += stride) {
-    T = tile_info<CAUSAL, VARLEN>(idx, p);
+__device__ __forceinline__ int next_running(int idx, int stride, const FwdParams& p, Tile& T, int n_tiles,
+                                            const int* seq_tab) {
+  for (; idx < n_tiles; idx += stride) {
+    T = tile_info<CAUSAL, VARLEN>(idx, p, seq_tab);
     if (runs<VARLEN>(T)) break;
   }
   return idx;
@@ -378,6 +404,43 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *tmem_slot;
   const WaitCtx wc{abort_flag, p.status, p.timeout_ns};
 
+  // Packed sequences without a causal mask: the tile prefix table (above).
+  const int* seq_tab = nullptr;
+  int n_tiles = p.n_tiles;
+  if constexpr (VARLEN && !CAUSAL) {
+    if (p.B <= kSeqTableCap) {
+      int* const tab = reinterpret_cast<int*>(smem + L::kTableOff);
+      int* const warp_sums = reinterpret_cast<int*>(smem + L::kStatsOff);  // unused until the first exchange
+      const int n = p.B, nth = static_cast<int>(blockDim.x), tid = static_cast<int>(threadIdx.x);
+      const int per = (n + nth - 1) / nth, s0 = min(n, tid * per), s1 = min(n, s0 + per);
+      auto q_tiles = [&](int sq) {  // clamped as in tile_info
+        const int qa = min(max(p.cu_q[sq], 0), p.total_q), qz = min(max(p.cu_q[sq + 1], qa), p.total_q);
+        return (qz - qa + kBM - 1) / kBM;
+      };
+      int mine = 0;
+      for (int sq = s0; sq < s1; ++sq) mine += q_tiles(sq);
+      int incl = mine;  // inclusive scan over the warp, then over the warps
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      if (lane == 31) warp_sums[warp] = incl;
+      __syncthreads();
+      int before = 0;
+      for (int w = 0; w < warp; ++w) before += warp_sums[w];
+      int run = before + incl - mine;
+      for (int sq = s0; sq < s1; ++sq) {
+        tab[sq] = run * p.H;
+        run += q_tiles(sq);
+      }
+      if (tid == nth - 1) tab[n] = (before + incl) * p.H;
+      __syncthreads();
+      seq_tab = tab;
+      n_tiles = tab[n];
+    }
+  }
+
   if (warp == kLoaderWarp) {
     // =========================================================== loader
     if (lane == 0) {
@@ -388,7 +451,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // thread never waits for a Q buffer: with one-block tiles, the K look-
       // ahead would otherwise wait for a store that needs a V not yet loaded.)
       Tile k_T, v_T;
-      int k_idx = next_running<CAUSAL, VARLEN>(blockIdx.x, stride, p, k_T), k_j = 0, gK = 0;
+      int k_idx = next_running<CAUSAL, VARLEN>(blockIdx.x, stride, p, k_T, n_tiles, seq_tab), k_j = 0, gK = 0;
       int v_idx = k_idx, v_j = 0, gV = 0;
       v_T = k_T;
       auto ring_load = [&](const CUtensorMap* m, const Tile& T, int j) -> bool {
@@ -407,19 +470,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++gK;
         if (++k_j == k_T.nb) {
           k_j = 0;
-          k_idx = next_running<CAUSAL, VARLEN>(k_idx + stride, stride, p, k_T);
+          k_idx = next_running<CAUSAL, VARLEN>(k_idx + stride, stride, p, k_T, n_tiles, seq_tab);
         }
         return true;
       };
-      while (ok && k_idx < p.n_tiles && gK < gV + NB) ok = load_k();
-      while (ok && v_idx < p.n_tiles) {
+      while (ok && k_idx < n_tiles && gK < gV + NB) ok = load_k();
+      while (ok && v_idx < n_tiles) {
         if (!ring_load(&tm_v, v_T, v_j)) { ok = false; break; }
         ++gV;
         if (++v_j == v_T.nb) {
           v_j = 0;
-          v_idx = next_running<CAUSAL, VARLEN>(v_idx + stride, stride, p, v_T);
+          v_idx = next_running<CAUSAL, VARLEN>(v_idx + stride, stride, p, v_T, n_tiles, seq_tab);
         }
-        while (ok && k_idx < p.n_tiles && gK < gV + NB) ok = load_k();
+        while (ok && k_idx < n_tiles && gK < gV + NB) ok = load_k();
       }
       // Let every copy still in flight land before the CTA can exit (the
       // newest load of each slot; older ones completed before their slot was
@@ -439,7 +502,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Q buffers' turnover off the K/V loader.
     if (lane == 0) {
       Tile Tq;
-      int q_idx = next_running<CAUSAL, VARLEN>(blockIdx.x, stride, p, Tq), q_issued = 0;
+      int q_idx = next_running<CAUSAL, VARLEN>(blockIdx.x, stride, p, Tq, n_tiles, seq_tab), q_issued = 0;
       auto load_q = [&]() {
         const int qb = q_issued & 1;
         mbar_arrive_expect_tx(bar_q_full(qb), L::kTileBytes);
@@ -447,13 +510,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           tma_load_4d(sQ + qb * L::kTileBytes + sl * L::kSlabBytes, &tm_q, 64 * sl, Tq.h, qrow_of<VARLEN>(Tq),
                       bcoord_of<VARLEN>(Tq), bar_q_full(qb));
         ++q_issued;
-        q_idx = next_running<CAUSAL, VARLEN>(q_idx + stride, stride, p, Tq);
+        q_idx = next_running<CAUSAL, VARLEN>(q_idx + stride, stride, p, Tq, n_tiles, seq_tab);
       };
-      for (int n = 0; n < 2 && q_idx < p.n_tiles; ++n) load_q();
+      for (int n = 0; n < 2 && q_idx < n_tiles; ++n) load_q();
       int tc = 0;
       Tile T;
-      for (int idx = next_running<CAUSAL, VARLEN>(blockIdx.x, stride, p, T); idx < p.n_tiles;
-           idx = next_running<CAUSAL, VARLEN>(idx + stride, stride, p, T), ++tc) {
+      for (int idx = next_running<CAUSAL, VARLEN>(blockIdx.x, stride, p, T, n_tiles, seq_tab); idx < n_tiles;
+           idx = next_running<CAUSAL, VARLEN>(idx + stride, stride, p, T, n_tiles, seq_tab), ++tc) {
         const int qb = tc & 1;
         if (!wait_bar(bar_stage_full(qb), (tc >> 1) & 1, wc)) break;
         // A packed sequence's last tile is written by the softmax threads
@@ -465,7 +528,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tma_store_commit();
           tma_store_wait_read0();
         }
-        if (q_idx < p.n_tiles) load_q();  // tile tc + 2, into buffer qb
+        if (q_idx < n_tiles) load_q();  // tile tc + 2, into buffer qb
       }
       // Let the Q copies still in flight land before the CTA can exit.
       const uint64_t t0 = globaltimer_ns();
@@ -490,8 +553,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint64_t dK = sdesc_kmajor_sw128(sRing);
         int g = 0, tc = 0;
         Tile T;
-        for (int idx = next_running<CAUSAL, VARLEN>(blockIdx.x, stride, p, T); idx < p.n_tiles && ok;
-             idx = next_running<CAUSAL, VARLEN>(idx + stride, stride, p, T), ++tc) {
+        for (int idx = next_running<CAUSAL, VARLEN>(blockIdx.x, stride, p, T, n_tiles, seq_tab); idx < n_tiles && ok;
+             idx = next_running<CAUSAL, VARLEN>(idx + stride, stride, p, T, n_tiles, seq_tab), ++tc) {
           const int qb = tc & 1;
           for (int j = 0; j < T.nb; ++j, ++g) {
             const int buf = g % NB;
@@ -524,12 +587,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint64_t dV = sdesc_mnmajor_sw128(sRing, L::kSlabBytes);
         Tile T;
         int G = 0;  // blocks of this CTA
-        for (int idx = next_running<CAUSAL, VARLEN>(blockIdx.x, stride, p, T); idx < p.n_tiles;
-             idx = next_running<CAUSAL, VARLEN>(idx + stride, stride, p, T))
+        for (int idx = next_running<CAUSAL, VARLEN>(blockIdx.x, stride, p, T, n_tiles, seq_tab); idx < n_tiles;
+             idx = next_running<CAUSAL, VARLEN>(idx + stride, stride, p, T, n_tiles, seq_tab))
           G += T.nb;
         int g = 0;
-        for (int idx = next_running<CAUSAL, VARLEN>(blockIdx.x, stride, p, T); idx < p.n_tiles && ok;
-             idx = next_running<CAUSAL, VARLEN>(idx + stride, stride, p, T)) {
+        for (int idx = next_running<CAUSAL, VARLEN>(blockIdx.x, stride, p, T, n_tiles, seq_tab); idx < n_tiles && ok;
+             idx = next_running<CAUSAL, VARLEN>(idx + stride, stride, p, T, n_tiles, seq_tab)) {
           for (int j = 0; j < T.nb; ++j, ++g) {
             const int buf = g % NB;
             // V_j first (loaded well ahead; its slot was freed by a P·V this
@@ -579,8 +642,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       return static_cast<uint16_t*>(p.o) + bcoord_of<VARLEN>(T) * p.o_sb +
              static_cast<long long>(qrow_of<VARLEN>(T) + r) * p.o_ss + T.h * p.o_sh;
     };
-    for (int idx = blockIdx.x; idx < p.n_tiles && ok; idx += stride) {
-      const Tile T = tile_info<CAUSAL, VARLEN>(idx, p);
+    for (int idx = blockIdx.x; idx < n_tiles && ok; idx += stride) {
+      const Tile T = tile_info<CAUSAL, VARLEN>(idx, p, seq_tab);
       const int q_row = T.q0 + r;
       if constexpr (VARLEN) {
         if (!runs<VARLEN>(T)) {

@@ -46,7 +46,7 @@ cudaError_t launch_fwd_d128_causal(const LaunchArgs& a);
 // each device uses it.
 template <int D, bool CAUSAL, uint32_t POLY, bool COUNT, bool VARLEN>
 cudaError_t launch_one(const LaunchArgs& a) {
-  constexpr unsigned int smem = Layout<D>::kSmemBytes;
+  constexpr unsigned int smem = Layout<D>::kSmemBytes + (VARLEN && !CAUSAL ? kSeqTableBytes : 0u);
   static volatile bool configured[64] = {};
   if (a.device < 0 || a.device >= 64) return cudaErrorInvalidDevice;
   if (!configured[a.device]) {

@@ -24,6 +24,11 @@ CASES = [
      86),
     ("one_sequence", [777], [777], 2, 2, 128, True, "top-left", 87),
     ("mix_d128", inputs.varlen_lengths(12, 700, 88), None, 8, 2, 128, True, "bottom-right", 88),
+    # non-causal, many sequences: the compacted tile order (300 sequences,
+    # several tiles per CTA) and, past its table's capacity of 4095
+    # sequences, the padded order
+    ("many_d64", [(i * 37) % 401 for i in range(300)], None, 2, 1, 64, False, "top-left", 92),
+    ("beyond_table_d64", [(i * 7) % 13 for i in range(4100)], None, 2, 2, 64, False, "top-left", 93),
 ]
 
 
