@@ -413,9 +413,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       int* const warp_sums = reinterpret_cast<int*>(smem + L::kStatsOff);  // unused until the first exchange
       const int n = p.B, nth = static_cast<int>(blockDim.x), tid = static_cast<int>(threadIdx.x);
       const int per = (n + nth - 1) / nth, s0 = min(n, tid * per), s1 = min(n, s0 + per);
-      auto q_tiles = [&](int sq) {  // clamped as in tile_info
+      auto q_tiles = [&](int sq) {  // clamped as in tile_info; at most the n_qt tiles max_seqlen_q covers
         const int qa = min(max(p.cu_q[sq], 0), p.total_q), qz = min(max(p.cu_q[sq + 1], qa), p.total_q);
-        return (qz - qa + kBM - 1) / kBM;
+        return min((qz - qa + kBM - 1) / kBM, p.n_qt);
       };
       int mine = 0;
       for (int sq = s0; sq < s1; ++sq) mine += q_tiles(sq);

@@ -101,3 +101,28 @@ def test_varlen_writes_only_its_rows():
     assert torch.isnan(o_buf[:G]).all() and torch.isnan(o_buf[G + T * H * d:]).all()
     assert (l_buf[:G] == 12345.0).all() and (l_buf[G + H * T:] == 12345.0).all()
     assert bool(torch.isfinite(o).all()) and bool(torch.isfinite(lse).all())
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_varlen_rows_beyond_max_seqlen_not_written(causal):
+    """max_seqlen_q shorter than a sequence: that sequence's rows from
+    max_seqlen_q on are left untouched (both tile orders), the rest is exact."""
+    need_gpu()
+    lens = [300, 700, 90]
+    H, d, m = 2, 64, 384  # 384 = three q tiles; the 700-row sequence is cut there
+    q, k, v, cu_q, cu_k = inputs.make_varlen_inputs(lens, lens, H, H, d, 94)
+    dev = torch.device("cuda:0")
+    o = torch.full(q.shape, float("nan"), dtype=torch.bfloat16, device=dev)
+    lse = torch.full((H, q.shape[0]), 777.0, dtype=torch.float32, device=dev)
+    attn.attn_fwd_varlen(q.to(dev), k.to(dev), v.to(dev), cu_q.to(dev), cu_k.to(dev), m, causal=causal,
+                         out=o, lse=lse)
+    torch.cuda.synchronize()
+    O_ref, L_ref = oracle.attention_varlen(q, k, v, cu_q.numpy(), cu_k.numpy(), 1.0 / np.sqrt(d), causal)
+    start = int(cu_q[1])
+    cut = np.zeros(q.shape[0], dtype=bool)
+    cut[start + m:start + lens[1]] = True
+    o_c, l_c = o.cpu(), lse.cpu()
+    assert torch.isnan(o_c[torch.from_numpy(cut)]).all()
+    assert (l_c[:, torch.from_numpy(cut)] == 777.0).all()
+    keep = ~cut
+    check(o_c[torch.from_numpy(keep)], l_c[:, torch.from_numpy(keep)], O_ref[keep], L_ref[:, keep], "cut")
