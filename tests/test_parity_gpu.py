@@ -8,6 +8,7 @@ import torch
 
 import oracle
 from exact_attention_63_gb300 import attn, inputs
+import oracle_pool
 from gpu_common import assert_close, f64, need_gpu, run, sample_rows
 
 pytestmark = pytest.mark.gpu
@@ -66,6 +67,19 @@ def test_full_size_sampled_rows(idx):
     for b, h, rows in sample_rows(w, seed=idx):
         O_ref, L_ref = oracle.attention_rows(q, k, v, w.scale, w.causal, b, h, rows)
         assert_close(f64(o_c[b, rows, h, :]), f64(l_c[b, h, rows]), O_ref, L_ref, f"{w.name} b{b} h{h}")
+
+
+@pytest.mark.parametrize("idx", [3, 4, 5])
+def test_full_size_all_elements(idx):
+    """Workloads 3–5 at full size compared on every element (the oracle runs
+    one head per process over a spawned pool; workload 5 is 4.4 TFLOP of
+    float64)."""
+    need_gpu()
+    w = inputs.WORKLOADS[idx]
+    q, k, v = inputs.make_inputs(w)
+    o, lse = run(w, q, k, v)
+    O_ref, L_ref = oracle_pool.attention_forward_pool(q, k, v, w.scale, w.causal)
+    assert_close(o, lse, O_ref, L_ref, w.name)
 
 
 def test_config2_all_elements():
