@@ -8,6 +8,7 @@ import pytest
 import torch
 
 import oracle
+import oracle_pool
 from exact_attention_63_gb300 import attn, inputs
 from gpu_common import f64, need_gpu
 
@@ -72,6 +73,24 @@ def test_backward_matches_oracle(w):
     dq, dk, dv = grads(w, q, k, v, dout)
     off = (w.Sk - w.Sq) if (w.causal and w.causal_align == "bottom-right") else 0
     rq, rk, rv = oracle.attention_backward(q, k, v, dout, w.scale, w.causal, causal_offset=off)
+    check("dq", dq, rq, w.name)
+    check("dk", dk, rk, w.name)
+    check("dv", dv, rv, w.name)
+
+
+@pytest.mark.parametrize("idx", [2, 3, 4])
+def test_backward_full_size_all_elements(idx):
+    """The bench's backward workloads at full size (B4 H16 S2048 d128; B2 H16
+    S8192 d128 causal; B8 H32 S4096 d64, σ_QK = 3), every element of dQ, dK,
+    dV against the oracle (one head per process).  (Workload 5's oracle would
+    hold 32768² float64 matrices per head.)"""
+    need_gpu()
+    w = inputs.WORKLOADS[idx]
+    q, k, v = inputs.make_inputs(w)
+    g = torch.Generator().manual_seed(w.seed + 2000)
+    dout = torch.randn(q.shape, generator=g).to(torch.bfloat16)
+    dq, dk, dv = grads(w, q, k, v, dout)
+    rq, rk, rv = oracle_pool.attention_backward_pool(q, k, v, dout, w.scale, w.causal)
     check("dq", dq, rq, w.name)
     check("dk", dk, rk, w.name)
     check("dv", dv, rv, w.name)
