@@ -123,3 +123,14 @@ def test_grouped_equals_repeated_heads():
     rep = w.H // w.kv_heads
     o2, l2 = run(w, q, k.repeat_interleave(rep, dim=2), v.repeat_interleave(rep, dim=2))
     assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+def test_grouped_bench_variant_full_size_all_elements():
+    """The bench's grouped-query variant (`--kv-heads 4`: B4 H16 H_kv 4 S2048
+    d128) at full size, every element."""
+    need_gpu()
+    w = C(4, 16, 2048, 2048, 128, False, seed=2, H_kv=4)
+    q, k, v = inputs.make_inputs(w)
+    o, lse = run(w, q.cuda(), k.cuda(), v.cuda())
+    O_ref, L_ref = reference(w, q, k, v)
+    check(o, lse, O_ref, L_ref, w.name)

@@ -126,3 +126,12 @@ def test_varlen_rows_beyond_max_seqlen_not_written(causal):
     assert (l_c[:, torch.from_numpy(cut)] == 777.0).all()
     keep = ~cut
     check(o_c[torch.from_numpy(keep)], l_c[:, torch.from_numpy(keep)], O_ref[keep], L_ref[:, keep], "cut")
+
+
+def test_varlen_bench_mix_full_size_all_elements():
+    """The bench's packed workload `--config 2 --varlen 32` (32 sequences of up
+    to 2048 rows, H16, d128) at full size, every element."""
+    need_gpu()
+    lens = inputs.varlen_lengths(32, 2048, inputs.WORKLOADS[2].seed)
+    o, lse, O_ref, L_ref = run_case(lens, None, 16, 16, 128, False, "top-left", inputs.WORKLOADS[2].seed)
+    check(o, lse, O_ref, L_ref, "bench mix")
