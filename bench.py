@@ -394,7 +394,7 @@ def main():
     peak = float(peaks["bf16_tflops"])
     traffic = load_profile_traffic(w.name)
     cpu = None
-    if args.cpu_budget > 0:
+    if args.cpu_budget > 0 and world == 1:  # the CPU baseline is taken at N = 1 only
         rate, sample, cores, _, _ = cpu_oracle_rate(w, args.cpu_budget)
         cpu = {"value": rate, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": sample}
     line = {
