@@ -18,6 +18,16 @@ barrier and a max-reduction.
 
 ``--impl reference`` times the CPU fp64 oracle (the reference arm of this
 comparison) on a bounded sample of the same workload.
+
+Variants of the workload (each its own JSON line, the metric unchanged):
+``--kv-heads H_kv`` grouped-query K/V heads; ``--causal-align bottom-right``;
+``--varlen N`` N sequences of seeded lengths packed along the rows (FLOPs
+counted per sequence); ``--backward`` a step is the backward instead — the
+preparation kernel and the dK/dV and dQ passes, three launches — with FLOPs
+counted as 2.5× the forward's (S, dP, dV, dK, dQ).  The variants report no
+``e2e`` (the host-buffer entry point takes the dense forward only), and
+``roofline.traffic`` is given only for workloads whose ncu counters are in
+``profiles/traffic.json`` for the current kernel sources (else null).
 """
 
 from __future__ import annotations
