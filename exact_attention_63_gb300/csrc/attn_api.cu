@@ -217,6 +217,9 @@ int launch(attn::LaunchArgs& a, const Opts& op, int dev, int d, int causal, floa
 }  // namespace
 
 namespace attn {
+
+int record_cuda_error(cudaError_t e, const char* what) { return fail_cuda(e, what); }
+
 namespace {
 
 // attn_fwd_host's pipeline: up to kHostChunks slices of the problem, each

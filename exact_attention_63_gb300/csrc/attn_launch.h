@@ -37,6 +37,9 @@ int fwd_host(const void* q_h, const void* k_h, const void* v_h, void* o_h, float
              int d, float scale, int causal, void* workspace, size_t workspace_bytes, cudaStream_t stream,
              bool pipelined);
 
+// Record a failed CUDA call for attn_last_cuda_error(); returns ATTN_ERR_LAUNCH.
+int record_cuda_error(cudaError_t e, const char* what);
+
 cudaError_t launch_fwd_d64(const LaunchArgs& a);
 cudaError_t launch_fwd_d64_causal(const LaunchArgs& a);
 cudaError_t launch_fwd_d128(const LaunchArgs& a);

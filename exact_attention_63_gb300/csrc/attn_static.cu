@@ -1,7 +1,9 @@
 // attn_fwd_host_static: the host-buffer attention call for callers that
 // cannot allocate device memory.  The device staging area for q, k, v, o and
-// lse is a fixed-size array that is part of this library's device image, so
-// it exists as soon as the library's module is loaded on a device.
+// lse is a fixed-size array in this library's device image.  It is reserved
+// when the CUDA runtime loads this file's module on a device: with lazy
+// module loading (the default) that is the first call on the device, with
+// eager loading it is library load.
 #include <cstdint>
 #include <cstdio>
 
@@ -12,15 +14,11 @@
 
 namespace {
 
-constexpr int kMaxDevices = 64;
 constexpr size_t kStaticBytes = ATTN_STATIC_WORKSPACE_BYTES;
 
 // Staging area of attn_fwd_host_static.  In host code this name is only a
 // handle for the runtime; the device address comes from cudaGetSymbolAddress.
 __device__ __align__(256) unsigned char g_static_workspace[kStaticBytes];
-
-// Device address of g_static_workspace, looked up once per device.
-void* g_static_addr[kMaxDevices] = {};
 
 }  // namespace
 
@@ -34,25 +32,27 @@ extern "C" int attn_fwd_host_static(const void* q_h, const void* k_h, const void
   if (need == 0 || need > kStaticBytes) return ATTN_ERR_STATIC_LIMIT;
 
   int dev = -1;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return ATTN_ERR_ARCH;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return attn::record_cuda_error(e, "cudaGetDevice");
   int major = 0, minor = 0;
   if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess || major != 10 ||
       minor != 3)
     return ATTN_ERR_ARCH;
 
-  // Set-up, once per device, with that device current: translate the array's
-  // host-side handle into its device address.  This allocates nothing.
-  if (g_static_addr[dev] == nullptr) {
-    void* addr = nullptr;
-    const cudaError_t e = cudaGetSymbolAddress(&addr, g_static_workspace);
-    if (e != cudaSuccess || addr == nullptr) return ATTN_ERR_LAUNCH;
-    g_static_addr[dev] = addr;
-  }
+  // The array's device address on the current device, looked up on every
+  // call (no cache: a context torn down and re-created may place the module
+  // elsewhere).  Once the module is loaded this is a host-side table lookup
+  // that allocates nothing; the first lookup on a device loads the module,
+  // which reserves the array and can fail with out-of-memory.
+  void* addr = nullptr;
+  e = cudaGetSymbolAddress(&addr, g_static_workspace);
+  if (e != cudaSuccess) return attn::record_cuda_error(e, "cudaGetSymbolAddress(static workspace)");
+  if (addr == nullptr) return attn::record_cuda_error(cudaErrorInvalidSymbol, "cudaGetSymbolAddress(static workspace)");
   // Every byte the kernel and the copies read back is written earlier in the
   // same call (q/k/v by the host-to-device copies, o/lse by the kernel), so
   // nothing in the array needs clearing between calls.
   // The single-slice form: it creates no streams or events either.
-  return attn::fwd_host(q_h, k_h, v_h, o_h, lse_h, B, H, Sq, Sk, d, scale, causal, g_static_addr[dev], kStaticBytes,
-                        stream, false);
+  return attn::fwd_host(q_h, k_h, v_h, o_h, lse_h, B, H, Sq, Sk, d, scale, causal, addr, kStaticBytes, stream,
+                        false);
 }

@@ -19,7 +19,7 @@ the error of float32 Horner evaluation is reported.  Run:
 
     python fit_exp2_poly.py
 
-and copy the printed constants into attn_fwd.cu (kPolyC1..kPolyC3).
+and copy the printed constants into attn_device.cuh (kPolyC1..kPolyC3).
 """
 
 import numpy as np

@@ -110,7 +110,11 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
  *   (row, block) softmax updates to counters[1].
  * timeout_ms — time limit of every pipeline wait inside the kernel (default
  *   4000 ms); on expiry the kernel stops, leaves outputs invalid and flags
- *   ATTN_ERR_TIMEOUT for attn_get_status().
+ *   ATTN_ERR_TIMEOUT for attn_get_status().  The limit is measured in wall
+ *   time (the GPU's global timer): on a GPU time-sliced between processes,
+ *   time spent while this context is switched out counts too, so a very long
+ *   call on a heavily shared GPU can report ATTN_ERR_TIMEOUT without any
+ *   fault; raise the limit there.
  * test_flags — for testing the wait limits only; 0 in normal use.
  *   ATTN_TEST_WITHHOLD_KV: the loader never issues the K/V copies, so the
  *   MMA issuer's first wait cannot complete and must run into timeout_ms; the
@@ -297,9 +301,17 @@ int attn_fwd_host(const void* q_h, const void* k_h, const void* v_h, void* o_h, 
  *   Problems whose attn_fwd_host_workspace_size() exceeds
  *   ATTN_STATIC_WORKSPACE_BYTES are rejected with ATTN_ERR_STATIC_LIMIT
  *   before anything is enqueued.
- *   The first call on each device looks up the array's device address
- *   (cudaGetSymbolAddress, no allocation) with that device current; make that
- *   first call before any stream capture on the device.
+ *   Every call looks up the array's device address on the current device
+ *   (cudaGetSymbolAddress), which allocates nothing once the array exists.
+ *   When the array comes into existence depends on CUDA's module loading:
+ *   with lazy loading (the default) the first call on each device loads this
+ *   part of the library and reserves the 32 MiB then; with eager loading
+ *   (CUDA_MODULE_LOADING=EAGER) loading the library reserves it on every
+ *   device.  That reservation is a device allocation and can fail with out
+ *   of memory (ATTN_ERR_LAUNCH; attn_last_cuda_error() has the CUDA error)
+ *   once another allocator has taken the device, so make one call on each
+ *   device at start-up, before pools reserve the device and before any
+ *   stream capture.  Later calls allocate nothing.
  *   All calls share the one array, which keeps the last call's contents:
  *   calls whose GPU work overlaps (different streams without ordering, or
  *   several host threads) race on it and must be serialised by the caller.

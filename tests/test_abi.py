@@ -170,3 +170,12 @@ def test_backward_layout_checks(L):
                              1 << 20, None) == -12
     assert L.attn_bwd(A, A, A, A, A, A, A, A, A, 1, 4, 8, 8, 64, 0.125, 1, A, 16, None) == -10  # workspace too small
     assert L.attn_bwd(A, A, A, A, A, 0, A, A, A, 1, 4, 8, 8, 64, 0.125, 1, A, 1 << 20, None) == -1
+
+
+def test_static_workspace_size_matches_header():
+    """The binding's copy of ATTN_STATIC_WORKSPACE_BYTES (used by the GPU test's
+    limit checks) equals the header's definition."""
+    src = open(HEADER).read()
+    m = re.search(r"#define\s+ATTN_STATIC_WORKSPACE_BYTES\s+\((\d+)u\s*<<\s*(\d+)\)", src)
+    assert m, "ATTN_STATIC_WORKSPACE_BYTES not found in the header"
+    assert int(m.group(1)) << int(m.group(2)) == attn.STATIC_WORKSPACE_BYTES

@@ -4,10 +4,13 @@ through its own allocator, or a code path where allocating after start-up is
 forbidden because cudaMalloc may synchronise the device).  The library stages
 the data in its own fixed 32 MiB device array instead of a caller workspace.
 
-Its results must match the existing host-buffer entry point (which uses a
-caller-allocated workspace) within the parity tolerance, call after call,
-whether this file runs alone in a fresh process or after the other tests.
-This file is named so that pytest collects it last.
+Both entry points run the same copies and the same kernel, so its results
+must equal the existing host-buffer entry point's (which uses a
+caller-allocated workspace) bit for bit, call after call, whether this file
+runs alone in a fresh process or after the other tests; and once the first
+call on the device has reserved the array, further calls must not change the
+device's free memory or the allocator's counts.  This file is named so that
+pytest collects it last.
 """
 
 import ctypes
@@ -16,7 +19,8 @@ import pytest
 import torch
 
 from exact_attention_63_gb300 import attn, inputs
-from gpu_common import assert_close, f64, need_gpu
+import oracle
+from gpu_common import assert_close, need_gpu
 
 
 def _host(w):
@@ -53,7 +57,31 @@ def test_static_entry_matches_workspace_entry_on_consecutive_calls():
         ws = torch.empty(attn.workspace_size(w.B, w.H, w.Sq, w.Sk, w.d), dtype=torch.uint8, device="cuda")
         attn.attn_fwd_host(qh, kh, vh, o_ref, l_ref, w.causal, w.scale, ws)
         torch.cuda.current_stream().synchronize()
-        assert_close(oh, lh, f64(o_ref), f64(l_ref), f"static vs workspace {w.name}")
+        assert torch.equal(oh, o_ref), f"static vs workspace {w.name}: O differs"
+        assert torch.equal(lh, l_ref), f"static vs workspace {w.name}: LSE differs"
+        # and both within the parity bar of the oracle
+        O_ref, L_ref = oracle.attention_forward(qh, kh, vh, w.scale, w.causal)
+        assert_close(oh, lh, O_ref, L_ref, f"static {w.name}")
+
+
+@pytest.mark.gpu
+def test_static_entry_allocates_nothing_after_its_first_call():
+    need_gpu()
+    w = inputs.custom(1, 4, 1000, 1000, 64, False, sigma_qk=3.0, seed=74)
+    qh, kh, vh, oh, lh = _host(w)
+    assert _call_static(w, qh, kh, vh, oh, lh) == 0  # the first call may load the module (reserves the array)
+    torch.cuda.synchronize()
+    free0, _ = torch.cuda.mem_get_info()
+    stats0 = torch.cuda.memory_stats()
+    for _ in range(5):
+        assert _call_static(w, qh, kh, vh, oh, lh) == 0
+    torch.cuda.synchronize()
+    assert attn.get_status() == 0
+    free1, _ = torch.cuda.mem_get_info()
+    stats1 = torch.cuda.memory_stats()
+    assert free1 == free0, f"device free memory moved by {free0 - free1} bytes"
+    for key in ("allocation.all.allocated", "segment.all.allocated"):
+        assert stats1.get(key, 0) == stats0.get(key, 0), key
 
 
 @pytest.mark.gpu
