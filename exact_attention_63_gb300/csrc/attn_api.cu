@@ -201,6 +201,7 @@ int launch(attn::LaunchArgs& a, const Opts& op, int dev, int d, int causal, floa
   a.p.counters = op.counters;
   a.p.scale_log2 = scale * 1.4426950408889634f;
   a.p.tau = op.tau;
+  a.p.sum_limit = std::exp2(op.tau);
   a.p.timeout_ns = static_cast<uint64_t>(op.timeout_ms) * 1000000ull;
   a.p.test_flags = op.test_flags;
   a.grid = a.p.n_tiles < g_dev[dev].sms ? a.p.n_tiles : g_dev[dev].sms;

@@ -299,14 +299,18 @@ constexpr float kPolyC2 = 0.22764499485492706f;
 constexpr float kPolyC3 = 0.07706703990697861f;
 // 1.5 · 2^23: adding it with round-toward-−∞ leaves ⌊x⌋ in the low mantissa bits.
 constexpr float kFloorMagic = 12582912.0f;
-// Inputs are clamped here; −127 gives exactly +0.0 (p(0) = 1 with exponent 0).
+// Inputs are clamped to [−127, 127]: −127 gives exactly +0.0 (p(0) = 1 with
+// exponent 0), 127 gives 2^127, the largest power of two below overflow (so
+// an input beyond the range still yields a huge, finite value, never a
+// wrapped exponent).
 constexpr float kPolyMinX = -127.0f;
+constexpr float kPolyMaxX = 127.0f;
 
 // 2^x for a pair of values, entirely on the FMA/ALU pipes:
 // x = j + f with j = ⌊x⌋, f ∈ [0,1); 2^x = bits(p(f)) + (j << 23).
 __device__ __forceinline__ void ex2_poly2(float& a, float& b) {
-  a = fmaxf(a, kPolyMinX);
-  b = fmaxf(b, kPolyMinX);
+  a = fminf(fmaxf(a, kPolyMinX), kPolyMaxX);
+  b = fminf(fmaxf(b, kPolyMinX), kPolyMaxX);
   const uint64_t x = pack2(a, b);
   const uint64_t magic = pack2(kFloorMagic, kFloorMagic);
   const uint64_t y = fadd2_rm(x, magic);     // 1.5·2^23 + ⌊x⌋

@@ -7,7 +7,16 @@
 // FlashAttention 4": blocks of Q, K, V streamed through on-chip memory).
 //
 // Warp roles (384 threads):
-//   warps 0-7  softmax, two warpgroups: warpgroup h owns keys [64h, 64h+64)
+//   warp  0    loader — TMA loads of K and V tiles into a ring of shared-
+//              memory slots guarded by full/empty mbarriers, in the order the
+//              MMA issuers consume them (K_0 … K_{NB−1}, then V_g, K_{g+NB} for
+//              every block g, across tile boundaries), so slots free up in the
+//              order they are refilled; allocates and frees tensor memory
+//   warp  1    P·V issuer (one thread) — tcgen05.mma O_h += P_h V_j[64h:64h+64]
+//   warp  2    S issuer (one thread) — tcgen05.mma S = Q K_jᵀ
+//   warp  3    Q and output (one thread) — TMA loads of each tile's Q into one
+//              of two Q buffers and the TMA store of each finished tile
+//   warps 4-11 softmax, two warpgroups: warpgroup h owns keys [64h, 64h+64)
 //              of every 128-key block, one thread per query row (= TMEM
 //              lane).  Each half is an independent online softmax with its
 //              own running maximum, row sum and O accumulator; the halves are
@@ -15,15 +24,6 @@
 //              (the merge a split over keys needs).  Splitting the columns
 //              halves each thread's serial work and puts two softmax warps on
 //              every scheduler, while no value crosses warpgroups per block.
-//   warp  8    loader — TMA loads of K and V tiles into a ring of shared-
-//              memory slots guarded by full/empty mbarriers, in the order the
-//              MMA issuers consume them (K_0 … K_{NB−1}, then V_g, K_{g+NB} for
-//              every block g, across tile boundaries), so slots free up in the
-//              order they are refilled; allocates and frees tensor memory
-//   warp  9    P·V issuer (one thread) — tcgen05.mma O_h += P_h V_j[64h:64h+64]
-//   warp 10    S issuer (one thread) — tcgen05.mma S = Q K_jᵀ
-//   warp 11    Q and output (one thread) — TMA loads of each tile's Q into one
-//              of two Q buffers and the TMA store of each finished tile
 //              Accumulators live in tensor memory.  An MMA issue stalls while
 //              the tensor core's queue is full, so a single issuer leaves the
 //              tensor core idle during each of its barrier waits; with two,
@@ -89,10 +89,15 @@ namespace attn {
 constexpr int kBM = 128;       // query rows per tile (= TMEM lanes)
 constexpr int kBN = 128;       // keys per block
 constexpr int kThreads = 384;  // 8 softmax warps + loader + 2 MMA issuers + output store
-constexpr int kLoaderWarp = 8;
-constexpr int kPvWarp = 9;
-constexpr int kSWarp = 10;
-constexpr int kStoreWarp = 11;
+// The single-thread roles take the lowest warp indices: the schedulers favour
+// older (lower-numbered) warps, and these warps' issue latency — above all the
+// MMA issuers' — sits on the pipeline's critical path, while the softmax warps
+// always have other eligible warps to overlap with.
+constexpr int kLoaderWarp = 0;
+constexpr int kPvWarp = 1;
+constexpr int kSWarp = 2;
+constexpr int kStoreWarp = 3;
+constexpr int kSoftmaxWarp0 = 4;  // softmax warps 4-11
 constexpr int kSoftmaxWarps = 8;
 constexpr uint32_t kTmemCols = 512;
 // Packed sequences without a causal mask: up to this many sequences, each
@@ -121,6 +126,7 @@ struct FwdParams {
   int n_tiles;                   // n_qt · B · H
   float scale_log2;              // scale · log2(e)
   float tau;                     // rescale threshold, log2 domain
+  float sum_limit;               // 2^tau: a half-block row sum above it sends the warp to the maximum
   uint64_t timeout_ns;
   uint32_t test_flags;           // bit 0: loader withholds K/V (exercises the wait limit)
 };
@@ -626,7 +632,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ========================================================== softmax
-    const int h = warp >> 2;         // key half owned by this warpgroup
+    const int h = (warp - kSoftmaxWarp0) >> 2;  // key half owned by this warpgroup
     const int r = threadIdx.x & 127;  // row within the tile = TMEM lane
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t tOh = tmem + L::col_o(h) + lane_off;
@@ -732,24 +738,43 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (key >= len_k_of<VARLEN>(T, p) || (CAUSAL && key > q_row + coff_of<VARLEN>(T, p))) s[c] = -INFINITY;
           }
         }
-        const float mx = row_max(s);
-        const bool need = mx > m_run + p.tau;
-        if (__any_sync(0xffffffffu, need)) {
-          const float m_new = need ? mx : m_run;
-          const float alpha = need ? ex2_mufu(m_run - m_new) : 1.f;
-          // O_h holds the tile's blocks < j once the last P_h·V has landed.
-          if (j > 0 && !rescale_o<D>(bar_pv_done((g - 1) % NB), ((g - 1) / NB) & 1, wc, tOh, alpha))
-            return false;
-          l_run *= alpha;
-          m_run = m_new;
-          if constexpr (COUNT) {
-            const unsigned int nres = __popc(__ballot_sync(0xffffffffu, need));
-            if (lane == 0) atomicAdd(p.counters, static_cast<unsigned long long>(nres));
-          }
-        }
-        __syncwarp();
+        // The exponentials are taken straight away against the running
+        // reference maximum.  Only when a row has no reference yet (its first
+        // visible block), or when its half-block sum shows a key far above the
+        // reference (Σp > 2^τ, so some p may exceed 2^τ; this also catches an
+        // overflow to inf), does the warp compute the block maximum, rescale
+        // where the maximum moved by more than τ, and redo the exponentials.
+        // The outputs are those of computing the maximum first: a row that
+        // passes the sum test has no key above m_run + τ, so it would not
+        // have been rescaled.  After a tile's first block the sum test almost
+        // never fails, so the maximum leaves the per-block path.
         uint32_t pk[kHalf / 2];
-        const float lsum = exps(s, pk);
+        float lsum;
+        bool redo = __any_sync(0xffffffffu, m_run == -INFINITY);
+#pragma unroll 1
+        for (;;) {
+          if (redo) {
+            const float mx = row_max(s);
+            const bool need = mx > m_run + p.tau;
+            if (__any_sync(0xffffffffu, need)) {
+              const float m_new = need ? mx : m_run;
+              const float alpha = need ? ex2_mufu(m_run - m_new) : 1.f;
+              // O_h holds the tile's blocks < j once the last P_h·V has landed.
+              if (j > 0 && !rescale_o<D>(bar_pv_done((g - 1) % NB), ((g - 1) / NB) & 1, wc, tOh, alpha))
+                return false;
+              l_run *= alpha;
+              m_run = m_new;
+              if constexpr (COUNT) {
+                const unsigned int nres = __popc(__ballot_sync(0xffffffffu, need));
+                if (lane == 0) atomicAdd(p.counters, static_cast<unsigned long long>(nres));
+              }
+            }
+            __syncwarp();
+          }
+          lsum = exps(s, pk);
+          if (redo || !__any_sync(0xffffffffu, !(lsum <= p.sum_limit))) break;
+          redo = true;
+        }
         if constexpr (COUNT) {
           if (lane == 0 && h == 0) atomicAdd(p.counters + 1, 32ull);
         }
