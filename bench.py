@@ -13,8 +13,10 @@ every step inside the timed region.
 
 Multi-GPU (torchrun, one process per GPU): every rank runs the same workload
 on its own independently seeded batch — attention heads are independent, so
-nothing is exchanged on the data path (weak scaling).  Only the timing uses a
-barrier and a max-reduction.
+nothing is exchanged on the data path (weak scaling).  ``--shard heads``
+splits the B·H heads of one problem across the ranks instead (strong
+scaling; each rank computes its contiguous share of the heads, again with no
+exchange).  Only the timing uses a barrier and a max-reduction.
 
 ``--impl reference`` times the CPU fp64 oracle (the reference arm of this
 comparison) on a bounded sample of the same workload.
@@ -280,6 +282,9 @@ def main():
     ap.add_argument("--varlen", type=int, default=0,
                     help="packed-sequence variant: this many sequences with a seeded mix of lengths up to the "
                          "workload's S (same H, d, mask); FLOPs counted per sequence")
+    ap.add_argument("--shard", choices=["replicas", "heads"], default="replicas",
+                    help="N > 1: every rank its own batch (weak scaling, default) or one problem's heads split "
+                         "across the ranks (strong scaling)")
     ap.add_argument("--causal-align", choices=["top-left", "bottom-right"], default="top-left",
                     help="causal alignment when Sq != Sk (only the square workloads ship, where both agree)")
     args = ap.parse_args()
@@ -291,6 +296,8 @@ def main():
     w = inputs.WORKLOADS[args.config]
     if args.backward and (args.kv_heads or args.varlen or args.causal_align != "top-left"):
         ap.error("--backward takes the plain workloads")
+    if args.shard == "heads" and (args.backward or args.varlen or args.kv_heads):
+        ap.error("--shard heads takes the plain forward workloads")
     if args.kv_heads or args.causal_align != "top-left" or args.varlen:
         import dataclasses
 
@@ -345,6 +352,22 @@ def main():
         def step():
             attn.attn_fwd_varlen(qd, kd, vd, cqd, ckd, max(lens), causal=w.causal, scale=w.scale, out=od, lse=ld,
                                  options=opts, causal_align=w.causal_align)
+    elif args.shard == "heads":
+        # One problem (the workload's own seed on every rank); this rank's
+        # contiguous share of its B·H heads, as (batch, head) units.
+        units = adist.shard_heads(w.B, w.H, world, rank)
+        q, k, v = inputs.make_inputs(w)
+        sel = lambda t: torch.stack([t[b_, :, h_, :] for b_, h_ in units], dim=1).unsqueeze(0).contiguous()
+        q, k, v = sel(q), sel(k), sel(v)  # [1, S, n_units, d]
+        qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
+        od = torch.empty_like(qd)
+        ld = torch.empty((1, len(units), w.Sq), dtype=torch.float32, device=dev)
+        shard_flops = w.flops * len(units) / (w.B * w.H)
+
+        def step():
+            attn.attn_fwd(qd, kd, vd, causal=w.causal, scale=w.scale, out=od, lse=ld, options=opts,
+                          causal_align=w.causal_align)
+        args.no_e2e = True
     else:
         q, k, v = inputs.make_inputs(w, seed=seed)
         qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
@@ -392,8 +415,13 @@ def main():
     flops = varlen_flops if lens is not None else w.flops
     if args.backward:
         flops *= 2.5
-    value = flops * world * args.steps / (total_ms * 1e-3) / 1e12
-    achieved = flops / (statistics.mean(times_ms) * 1e-3) / 1e12
+    if args.shard == "heads":
+        # strong scaling: the whole problem's FLOPs over the slowest rank's time
+        value = flops * args.steps / (total_ms * 1e-3) / 1e12
+        achieved = shard_flops / (statistics.mean(times_ms) * 1e-3) / 1e12
+    else:
+        value = flops * world * args.steps / (total_ms * 1e-3) / 1e12
+        achieved = flops / (statistics.mean(times_ms) * 1e-3) / 1e12
 
     # ---- end to end through the host-buffer entry point
     e2e = None
@@ -453,7 +481,7 @@ def main():
         "warmup": args.warmup,
         "ms_per_step": ms_per_step,
         "higher_is_better": True,
-        "scaling": "weak",
+        "scaling": "strong" if args.shard == "heads" else "weak",
         "vs_baseline": None,
         "dtype": "bf16",
         "data": "synthetic",
@@ -461,7 +489,8 @@ def main():
                    "causal": w.causal, "causal_align": w.causal_align, "sigma_qk": w.sigma_qk, "seed": w.seed,
                    **({"varlen_lengths": lens} if lens is not None else {}),
                    "l2": "flushed between timed steps (256 MiB write)",
-                   "parallelism": f"replicas{world}" if world > 1 else "single"},
+                   "parallelism": (f"heads{world}" if args.shard == "heads" else f"replicas{world}")
+                   if world > 1 else "single"},
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak, "traffic": traffic,
                      "peak_source": f"{peak_kind} bf16_tflops (burst cuBLAS)",
