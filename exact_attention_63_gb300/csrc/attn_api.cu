@@ -205,6 +205,7 @@ int launch(attn::LaunchArgs& a, const Opts& op, int dev, int d, int causal, floa
   a.p.timeout_ns = static_cast<uint64_t>(op.timeout_ms) * 1000000ull;
   a.p.test_flags = op.test_flags;
   a.grid = a.p.n_tiles < g_dev[dev].sms ? a.p.n_tiles : g_dev[dev].sms;
+  a.sms = g_dev[dev].sms;
   a.poly = op.poly;
   a.device = dev;
   a.stream = stream;

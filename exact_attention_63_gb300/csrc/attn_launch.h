@@ -8,6 +8,7 @@
 #include <cuda_runtime.h>
 
 #include "attn_fwd_kernel.cuh"
+#include "attn_fwd_rows.cuh"
 
 namespace attn {
 
@@ -15,6 +16,7 @@ struct LaunchArgs {
   CUtensorMap q, k, v, o;  // 4-D tiled maps, box (64, 1, 128, 1), 128-byte swizzle
   FwdParams p;
   int grid;             // persistent: min(tiles, SMs)
+  int sms;              // multiprocessors of the device
   uint32_t poly;           // exp2 chunk mask; one of kPolyMasks
   int device;
   cudaStream_t stream;
@@ -75,6 +77,34 @@ cudaError_t launch_poly(const LaunchArgs& a) {
   }
 }
 
+// The d = 64 full-row kernel (two CTAs per SM).  Its register split relies on
+// the kernel being compiled to exactly kRowsLaunchRegs registers; a build
+// where it is not runs the two-warpgroup kernel instead (cudaErrorNotSupported
+// tells the caller to).
+template <bool CAUSAL, bool COUNT>
+cudaError_t launch_rows(const LaunchArgs& a) {
+  constexpr unsigned int smem = RowsLayout::kSmemBytes;
+  static volatile int state[64] = {};  // per device: 0 not checked, 1 usable, -1 not usable
+  if (a.device < 0 || a.device >= 64) return cudaErrorInvalidDevice;
+  if (state[a.device] == 0) {
+    cudaFuncAttributes fa;
+    cudaError_t e = cudaFuncGetAttributes(&fa, attn_fwd_rows_kernel<CAUSAL, COUNT>);
+    if (e != cudaSuccess) return e;
+    if (fa.numRegs != kRowsLaunchRegs) {
+      state[a.device] = -1;
+    } else {
+      e = cudaFuncSetAttribute(attn_fwd_rows_kernel<CAUSAL, COUNT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               smem);
+      if (e != cudaSuccess) return e;
+      state[a.device] = 1;
+    }
+  }
+  if (state[a.device] < 0) return cudaErrorNotSupported;
+  const int grid = a.p.n_tiles < 2 * a.sms ? a.p.n_tiles : 2 * a.sms;
+  attn_fwd_rows_kernel<CAUSAL, COUNT><<<grid, kRowsThreads, smem, a.stream>>>(a.q, a.k, a.v, a.o, a.p);
+  return cudaGetLastError();
+}
+
 // The counting kernels are separate instantiations, so the default ones carry
 // no diagnostic code.  Packed sequences (offset tables given) have their own
 // instantiations, compiled with the default exp2 split only.
@@ -84,6 +114,12 @@ cudaError_t launch_variant(const LaunchArgs& a) {
     if (a.poly != 0x00u) return cudaErrorInvalidValue;
     return a.p.counters != nullptr ? launch_one<D, CAUSAL, 0x00u, true, true>(a)
                                    : launch_one<D, CAUSAL, 0x00u, false, true>(a);
+  }
+  if constexpr (D == 64) {
+    if (a.poly == 0x00u) {  // dense tensors, exp2 on MUFU: the full-row kernel
+      const cudaError_t e = a.p.counters != nullptr ? launch_rows<CAUSAL, true>(a) : launch_rows<CAUSAL, false>(a);
+      if (e != cudaErrorNotSupported) return e;
+    }
   }
   return a.p.counters != nullptr ? launch_poly<D, CAUSAL, true>(a) : launch_poly<D, CAUSAL, false>(a);
 }
