@@ -28,9 +28,9 @@
 //   warp 2     S issuer (one thread): S = Q · K_jᵀ
 //   warp 3     Q loads and output stores (one thread), as in attn_fwd_kernel
 //   warps 4-7  softmax, one thread per query row
-// Registers: launched at 128 per thread; the role warpgroup gives back to 64
-// and the softmax warpgroup takes 192 (setmaxnreg), which holds a row's 128
-// scores in registers.  The host launches this kernel only when it was
+// Registers: launched at 128 per thread; the role warpgroup gives back to 56
+// and the softmax warpgroup takes 200 (setmaxnreg), which holds a row's 128
+// scores in registers while it computes the exponentials.  The host launches this kernel only when it was
 // compiled to exactly 128 registers, the total both shares add up to.
 //
 // TMEM columns (256): S [0, 128), P [128, 192) (bf16 pairs), O [192, 256).
@@ -67,8 +67,8 @@ struct RowsLayout {
 
 constexpr int kRowsThreads = 256;
 constexpr int kRowsLaunchRegs = 128;  // 65536 / (2 CTAs × 256 threads)
-constexpr int kRowsRoleRegs = 64;
-constexpr int kRowsSoftmaxRegs = 192;  // 128·64 + 128·192 = 256·128
+constexpr int kRowsRoleRegs = 56;
+constexpr int kRowsSoftmaxRegs = 200;  // 128·56 + 128·200 = 256·128
 static_assert(kRowsThreads / 2 * (kRowsRoleRegs + kRowsSoftmaxRegs) == kRowsThreads * kRowsLaunchRegs,
               "the two register shares must add up to the launch allocation");
 
@@ -333,68 +333,92 @@ __global__ void __launch_bounds__(kRowsThreads, 2)
             if (key >= len_k_of<VARLEN>(T, p) || (CAUSAL && key > q_row + coff_of<VARLEN>(T, p))) s[c] = -INFINITY;
           }
         }
-        // Row maximum (log2 domain): eight independent 16-wide chains.
-        float m8[8];
-#pragma unroll
-        for (int gg = 0; gg < 8; ++gg) {
-          const float* x = s + 16 * gg;
-          float a = fmax3(x[0], x[1], x[2]);
-          float b2 = fmax3(x[3], x[4], x[5]);
-          a = fmax3(a, x[6], x[7]);
-          b2 = fmax3(b2, x[8], x[9]);
-          a = fmax3(a, x[10], x[11]);
-          b2 = fmax3(b2, x[12], x[13]);
-          m8[gg] = fmax3(a, b2, fmaxf(x[14], x[15]));
-        }
-        const float mx =
-            fmaxf(fmax3(m8[0], m8[1], m8[2]), fmax3(fmax3(m8[3], m8[4], m8[5]), m8[6], m8[7])) * sc;
-        const bool need = mx > m_run + p.tau;
+        // The exponentials are taken straight away against the running
+        // reference maximum, and P goes into its buffer in two halves of 64
+        // keys: the wait for P·V(g−1), the buffer's reader, sits between them,
+        // by when it has long completed.  Only when a row has no reference
+        // yet (its first visible block), or when its sum shows a key far
+        // above the reference (Σp > 2^τ, so some p may exceed 2^τ; this also
+        // catches an overflow to inf), does the warp compute the block
+        // maximum, rescale where it moved by more than τ, and redo the
+        // exponentials (S is still in registers).  The outputs are those of
+        // computing the maximum first: a row that passes the sum test has no
+        // key above m_run + τ, so it would not have been rescaled.
+        bool redo = __any_sync(0xffffffffu, m_run == -INFINITY);
         bool pv_seen = (g == 0);  // P·V(g−1) known complete (nothing before the CTA's first block)
-        if (__any_sync(0xffffffffu, need)) {
-          const float m_new = need ? mx : m_run;
-          const float alpha = need ? ex2_mufu(m_run - m_new) : 1.f;
-          if (j > 0) {
-            // O holds the tile's blocks < j once the last P·V has landed.
-            if (!rescale_o<L::D>(bar_pv_done, (g - 1) & 1, wc, tO, alpha)) return false;
-            pv_seen = true;
-          }
-          l_run *= alpha;
-          m_run = m_new;
-          if constexpr (COUNT) {
-            const unsigned int nres = __popc(__ballot_sync(0xffffffffu, need));
-            if (lane == 0) atomicAdd(p.counters, static_cast<unsigned long long>(nres));
-          }
-        }
-        __syncwarp();
-        // p = 2^(s·scale·log2 e − m_run), bf16 pairs over the row's 128 keys.
-        const float negm = (m_run == -INFINITY) ? 0.f : -m_run;
-        const uint64_t nm2 = pack2(negm, negm);
-        uint32_t pk[kBN / 2];
-        uint64_t acc[4] = {0, 0, 0, 0};
+        float lsum;
+#pragma unroll 1
+        for (;;) {
+          if (redo) {
+            float m8[8];  // row maximum (log2 domain): eight independent 16-wide chains
 #pragma unroll
-        for (int i = 0; i < kBN / 2; ++i) {
-          float x0, x1;
-          unpack2(ffma2(pack2(s[2 * i], s[2 * i + 1]), sc2, nm2), x0, x1);
-          x0 = ex2_mufu(x0);
-          x1 = ex2_mufu(x1);
-          acc[i & 3] = fadd2(acc[i & 3], pack2(x0, x1));
-          pk[i] = pack_bf16x2(x0, x1);
+            for (int gg = 0; gg < 8; ++gg) {
+              const float* x = s + 16 * gg;
+              float a = fmax3(x[0], x[1], x[2]);
+              float b2 = fmax3(x[3], x[4], x[5]);
+              a = fmax3(a, x[6], x[7]);
+              b2 = fmax3(b2, x[8], x[9]);
+              a = fmax3(a, x[10], x[11]);
+              b2 = fmax3(b2, x[12], x[13]);
+              m8[gg] = fmax3(a, b2, fmaxf(x[14], x[15]));
+            }
+            const float mx =
+                fmaxf(fmax3(m8[0], m8[1], m8[2]), fmax3(fmax3(m8[3], m8[4], m8[5]), m8[6], m8[7])) * sc;
+            const bool need = mx > m_run + p.tau;
+            if (__any_sync(0xffffffffu, need)) {
+              const float m_new = need ? mx : m_run;
+              const float alpha = need ? ex2_mufu(m_run - m_new) : 1.f;
+              if (j > 0) {
+                // O holds the tile's blocks < j once the last P·V has landed.
+                if (!rescale_o<L::D>(bar_pv_done, (g - 1) & 1, wc, tO, alpha)) return false;
+                pv_seen = true;
+              }
+              l_run *= alpha;
+              m_run = m_new;
+              if constexpr (COUNT) {
+                const unsigned int nres = __popc(__ballot_sync(0xffffffffu, need));
+                if (lane == 0) atomicAdd(p.counters, static_cast<unsigned long long>(nres));
+              }
+            }
+            __syncwarp();
+          }
+          // p = 2^(s·scale·log2 e − m_run), bf16 pairs, 64 keys at a time.
+          const float negm = (m_run == -INFINITY) ? 0.f : -m_run;
+          const uint64_t nm2 = pack2(negm, negm);
+          uint64_t acc[4] = {0, 0, 0, 0};
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh) {
+            uint32_t pk[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              float x0, x1;
+              const int c = 64 * hh + 2 * i;
+              unpack2(ffma2(pack2(s[c], s[c + 1]), sc2, nm2), x0, x1);
+              x0 = ex2_mufu(x0);
+              x1 = ex2_mufu(x1);
+              acc[i & 3] = fadd2(acc[i & 3], pack2(x0, x1));
+              pk[i] = pack_bf16x2(x0, x1);
+            }
+            if (hh == 0 && !pv_seen) {
+              // The P buffer is free once P·V(g−1) has read it.
+              const bool landed = wait_bar_cold(bar_pv_done, (g - 1) & 1, wc);
+              if (__any_sync(0xffffffffu, !landed)) return false;
+              tc_fence_after();
+              pv_seen = true;
+            }
+            tmem_st32(tP + 32 * hh, pk);
+          }
+          float a0, a1, b0, b1;
+          unpack2(fadd2(acc[0], acc[1]), a0, a1);
+          unpack2(fadd2(acc[2], acc[3]), b0, b1);
+          lsum = (a0 + a1) + (b0 + b1);
+          if (redo || !__any_sync(0xffffffffu, !(lsum <= p.sum_limit))) break;
+          redo = true;
         }
-        float a0, a1, b0, b1;
-        unpack2(fadd2(acc[0], acc[1]), a0, a1);
-        unpack2(fadd2(acc[2], acc[3]), b0, b1);
-        l_run += (a0 + a1) + (b0 + b1);
+        l_run += lsum;
         if constexpr (COUNT) {
           if (lane == 0) atomicAdd(p.counters + 1, 32ull);
         }
-        // The P buffer is free once P·V(g−1) has read it.
-        if (!pv_seen) {
-          const bool landed = wait_bar_cold(bar_pv_done, (g - 1) & 1, wc);
-          if (__any_sync(0xffffffffu, !landed)) return false;
-          tc_fence_after();
-        }
-        tmem_st32(tP, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
-        tmem_st32(tP + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
         tmem_wait_st();
         tc_fence_before();
         warp_arrive(bar_p_full, lane);
