@@ -305,6 +305,7 @@ __global__ void __launch_bounds__(kRowsThreads, 2)
     const uint64_t sc2 = pack2(sc, sc);
     bool ok = true;
     int g = 0, tc = 0;
+    bool s_ready = false;  // S(g) known complete (tested at the end of block g − 1)
     for (int idx = blockIdx.x; idx < n_tiles && ok; idx += stride) {
       const Tile T = tile_info<CAUSAL, VARLEN>(idx, p, seq_tab);
       const int q_row = T.q0 + r;
@@ -312,7 +313,7 @@ __global__ void __launch_bounds__(kRowsThreads, 2)
       float l_run = 0.f;        // running row sum (fp32, unrounded p)
       auto block = [&](int j, auto mask_tag) -> bool {
         constexpr bool MASK = decltype(mask_tag)::value;
-        const bool got = wait_bar_cold(bar_s_full, g & 1, wc);
+        const bool got = s_ready || wait_bar_cold(bar_s_full, g & 1, wc);
         if (__any_sync(0xffffffffu, !got)) return false;
         tc_fence_after();
         uint32_t u[kBN];
@@ -415,6 +416,9 @@ __global__ void __launch_bounds__(kRowsThreads, 2)
           if (redo || !__any_sync(0xffffffffu, !(lsum <= p.sum_limit))) break;
           redo = true;
         }
+        // Test the next block's S without blocking; the answer is needed only
+        // at that block's start, so the test's latency overlaps this block's end.
+        s_ready = mbar_test_wait(bar_s_full, (g + 1) & 1);
         l_run += lsum;
         if constexpr (COUNT) {
           if (lane == 0) atomicAdd(p.counters + 1, 32ull);
