@@ -62,7 +62,8 @@ def load_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
-KERNEL_SOURCES = ["exact_attention_63_gb300/csrc/attn_fwd_kernel.cuh", "exact_attention_63_gb300/csrc/attn_device.cuh"]
+KERNEL_SOURCES = ["exact_attention_63_gb300/csrc/attn_fwd_kernel.cuh", "exact_attention_63_gb300/csrc/attn_fwd_rows.cuh",
+                  "exact_attention_63_gb300/csrc/attn_device.cuh"]
 
 
 def kernel_source_hash():
@@ -458,7 +459,12 @@ def main():
                                                 counters=cnt))
         torch.cuda.synchronize()
         c = cnt.cpu().tolist()
-        diag = {"rescales_per_row_half_block": c[0] / max(1, 2 * c[1]), "row_block_updates": c[1]}
+        # d = 64 runs the full-row kernel (one running maximum per row); the
+        # d = 128 kernel keeps one per 64-key half of each row.
+        parts = 1 if w.d == 64 else 2
+        diag = {"rescales": c[0], "row_block_updates": c[1], "tau": args.tau or 32.0,
+                "rescale_unit": "row x 128-key block" if parts == 1 else "row x 64-key half block",
+                "rescales_per_unit": c[0] / max(1, parts * c[1])}
 
     if rank != 0:
         if world > 1:

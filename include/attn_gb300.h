@@ -104,10 +104,12 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
  *   0xFF (all); 0x100 selects none (all MUFU); 0 selects the default for the
  *   head dim; any other value is rejected with ATTN_ERR_OPTION.
  * counters — optional device pointer to 2 zero-initialised uint64 values; when
- *   non-NULL the kernel adds the number of rescales to counters[0] (counted
- *   per row, key block and key half: each 128-key block is processed as two
- *   64-key halves with their own running maxima) and the number of
- *   (row, block) softmax updates to counters[1].
+ *   non-NULL the kernel adds the number of rescales to counters[0] and the
+ *   number of (row, block) softmax updates to counters[1].  A rescale is
+ *   counted per row, key block and running maximum: at d = 128 (and for
+ *   packed sequences or a polynomial exp2 split at d = 64) each 128-key block
+ *   is processed as two 64-key halves with running maxima of their own; the
+ *   other d = 64 calls keep one running maximum per row.
  * timeout_ms — time limit of every pipeline wait inside the kernel (default
  *   4000 ms); on expiry the kernel stops, leaves outputs invalid and flags
  *   ATTN_ERR_TIMEOUT for attn_get_status().  The limit is measured in wall
