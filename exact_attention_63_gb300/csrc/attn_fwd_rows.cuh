@@ -72,7 +72,9 @@ constexpr int kRowsSoftmaxRegs = 200;  // 128·56 + 128·200 = 256·128
 static_assert(kRowsThreads / 2 * (kRowsRoleRegs + kRowsSoftmaxRegs) == kRowsThreads * kRowsLaunchRegs,
               "the two register shares must add up to the launch allocation");
 
-template <bool CAUSAL, bool COUNT>
+// POLY: bit c selects the FMA-pipe polynomial exp2 for 16-key chunk c of
+// every 128-key block (compile time, so the exp loop is one basic block).
+template <bool CAUSAL, bool COUNT, uint32_t POLY>
 __global__ void __launch_bounds__(kRowsThreads, 2)
     attn_fwd_rows_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                          const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
@@ -395,8 +397,12 @@ __global__ void __launch_bounds__(kRowsThreads, 2)
               float x0, x1;
               const int c = 64 * hh + 2 * i;
               unpack2(ffma2(pack2(s[c], s[c + 1]), sc2, nm2), x0, x1);
-              x0 = ex2_mufu(x0);
-              x1 = ex2_mufu(x1);
+              if ((POLY >> (c / 16)) & 1u) {  // folded after unrolling
+                ex2_poly2(x0, x1);
+              } else {
+                x0 = ex2_mufu(x0);
+                x1 = ex2_mufu(x1);
+              }
               acc[i & 3] = fadd2(acc[i & 3], pack2(x0, x1));
               pk[i] = pack_bf16x2(x0, x1);
             }

@@ -81,28 +81,40 @@ cudaError_t launch_poly(const LaunchArgs& a) {
 // the kernel being compiled to exactly kRowsLaunchRegs registers; a build
 // where it is not runs the two-warpgroup kernel instead (cudaErrorNotSupported
 // tells the caller to).
-template <bool CAUSAL, bool COUNT>
-cudaError_t launch_rows(const LaunchArgs& a) {
+template <bool CAUSAL, bool COUNT, uint32_t POLY>
+cudaError_t launch_rows_one(const LaunchArgs& a) {
   constexpr unsigned int smem = RowsLayout::kSmemBytes;
   static volatile int state[64] = {};  // per device: 0 not checked, 1 usable, -1 not usable
   if (a.device < 0 || a.device >= 64) return cudaErrorInvalidDevice;
   if (state[a.device] == 0) {
     cudaFuncAttributes fa;
-    cudaError_t e = cudaFuncGetAttributes(&fa, attn_fwd_rows_kernel<CAUSAL, COUNT>);
+    cudaError_t e = cudaFuncGetAttributes(&fa, attn_fwd_rows_kernel<CAUSAL, COUNT, POLY>);
     if (e != cudaSuccess) return e;
     if (fa.numRegs != kRowsLaunchRegs) {
       state[a.device] = -1;
     } else {
-      e = cudaFuncSetAttribute(attn_fwd_rows_kernel<CAUSAL, COUNT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               smem);
+      e = cudaFuncSetAttribute(attn_fwd_rows_kernel<CAUSAL, COUNT, POLY>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
       if (e != cudaSuccess) return e;
       state[a.device] = 1;
     }
   }
   if (state[a.device] < 0) return cudaErrorNotSupported;
   const int grid = a.p.n_tiles < 2 * a.sms ? a.p.n_tiles : 2 * a.sms;
-  attn_fwd_rows_kernel<CAUSAL, COUNT><<<grid, kRowsThreads, smem, a.stream>>>(a.q, a.k, a.v, a.o, a.p);
+  attn_fwd_rows_kernel<CAUSAL, COUNT, POLY><<<grid, kRowsThreads, smem, a.stream>>>(a.q, a.k, a.v, a.o, a.p);
   return cudaGetLastError();
+}
+
+template <bool CAUSAL, bool COUNT>
+cudaError_t launch_rows(const LaunchArgs& a) {
+  switch (a.poly) {
+    case 0x00u: return launch_rows_one<CAUSAL, COUNT, 0x00u>(a);
+    case 0x01u: return launch_rows_one<CAUSAL, COUNT, 0x01u>(a);
+    case 0x11u: return launch_rows_one<CAUSAL, COUNT, 0x11u>(a);
+    case 0x55u: return launch_rows_one<CAUSAL, COUNT, 0x55u>(a);
+    case 0xFFu: return launch_rows_one<CAUSAL, COUNT, 0xFFu>(a);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 // The counting kernels are separate instantiations, so the default ones carry
@@ -115,11 +127,9 @@ cudaError_t launch_variant(const LaunchArgs& a) {
     return a.p.counters != nullptr ? launch_one<D, CAUSAL, 0x00u, true, true>(a)
                                    : launch_one<D, CAUSAL, 0x00u, false, true>(a);
   }
-  if constexpr (D == 64) {
-    if (a.poly == 0x00u) {  // dense tensors, exp2 on MUFU: the full-row kernel
-      const cudaError_t e = a.p.counters != nullptr ? launch_rows<CAUSAL, true>(a) : launch_rows<CAUSAL, false>(a);
-      if (e != cudaErrorNotSupported) return e;
-    }
+  if constexpr (D == 64) {  // dense tensors: the full-row kernel
+    const cudaError_t e = a.p.counters != nullptr ? launch_rows<CAUSAL, true>(a) : launch_rows<CAUSAL, false>(a);
+    if (e != cudaErrorNotSupported) return e;
   }
   return a.p.counters != nullptr ? launch_poly<D, CAUSAL, true>(a) : launch_poly<D, CAUSAL, false>(a);
 }
