@@ -347,7 +347,9 @@ __global__ void __launch_bounds__(kRowsThreads, 2)
         // exponentials (S is still in registers).  The outputs are those of
         // computing the maximum first: a row that passes the sum test has no
         // key above m_run + τ, so it would not have been rescaled.
-        bool redo = __any_sync(0xffffffffu, m_run == -INFINITY);
+        // (Every row sees key 0 of its tile's first block, the only block where
+        // m_run is still −inf.)
+        bool redo = (j == 0);
         bool pv_seen = (g == 0);  // P·V(g−1) known complete (nothing before the CTA's first block)
         float lsum;
 #pragma unroll 1
