@@ -130,3 +130,37 @@ def make_varlen_inputs(lens_q, lens_k, H: int, H_kv: int, d: int, seed: int, sig
     if device is not None:
         out = tuple(t.to(device) for t in out)
     return out
+
+
+# ------------------------------------------------------------------- FP8
+E4M3_MAX = 448.0  # largest finite FP8 E4M3 value
+
+
+def make_fp8_inputs(w: Workload, seed: int | None = None, device=None):
+    """FP8 (E4M3) q, k, v for workload ``w`` and their per-tensor scale factors.
+
+    The same fp32 draws as ``make_inputs`` (seed, order Q, K, V, the
+    workload's standard deviations), each tensor divided by its scale factor
+    descale = max|x| / 448 and rounded to E4M3 (round to nearest even), so its
+    largest magnitude lands on 448.  Returns (q8, k8, v8, descale_q, descale_k,
+    descale_v) with the tensors as torch.float8_e4m3fn, shaped like the bf16
+    inputs; the values they stand for are descale · x8.
+    """
+    g = torch.Generator(device="cpu")
+    g.manual_seed(w.seed if seed is None else seed)
+    q = torch.randn((w.B, w.Sq, w.H, w.d), generator=g, dtype=torch.float32)
+    k = torch.randn((w.B, w.Sk, w.kv_heads, w.d), generator=g, dtype=torch.float32)
+    v = torch.randn((w.B, w.Sk, w.kv_heads, w.d), generator=g, dtype=torch.float32)
+    if w.sigma_qk != 1.0:
+        q.mul_(w.sigma_qk)
+        k.mul_(w.sigma_qk)
+    if w.sigma_v != 1.0:
+        v.mul_(w.sigma_v)
+    out, scales = [], []
+    for t in (q, k, v):
+        descale = float(t.abs().max()) / E4M3_MAX
+        out.append((t / descale).to(torch.float8_e4m3fn))
+        scales.append(descale)
+    if device is not None:
+        out = [t.to(device) for t in out]
+    return (*out, *scales)

@@ -15,6 +15,7 @@ from .attention import (  # noqa: F401
     attention_backward,
     attention_backward_head,
     attention_forward,
+    attention_forward_fp8,
     attention_head,
     attention_rows,
     attention_varlen,
@@ -23,5 +24,6 @@ from .attention import (  # noqa: F401
     kv_head,
     visible_mask,
     combine_partials,
+    e4m3_to_f64,
     to_f64,
 )

@@ -267,3 +267,35 @@ def combine_partials(O_parts, LSE_parts):
         w = np.where(finite[None], W / np.where(tot > 0, tot, 1.0)[None], 0.0)
     O = (w[..., None] * Os).sum(axis=0)
     return O, LSE
+
+
+def e4m3_to_f64(x8) -> np.ndarray:
+    """Exact float64 values of FP8 E4M3 data (a torch float8_e4m3fn tensor, or
+    its raw bytes as uint8)."""
+    import torch  # local import, as in to_f64
+
+    if isinstance(x8, torch.Tensor) and x8.dtype == torch.uint8:
+        x8 = x8.view(torch.float8_e4m3fn)
+    return x8.detach().to("cpu", torch.float32).numpy().astype(np.float64)
+
+
+def attention_forward_fp8(q8, k8, v8, descale_q: float, descale_k: float, descale_v: float, scale: float,
+                          causal: bool, causal_offset: int = 0):
+    """Exact attention over FP8 (E4M3) inputs with per-tensor scale factors.
+
+    "FlashAttention-3: Pipeline Assíncrono …", section "Estabilidade em FP8":
+    the FP8 forward keeps Q, K and V in E4M3 (1 sign, 4 exponent, 3 mantissa
+    bits, range ±448), accumulates the products in fp32 and applies static
+    scale factors.  The values these tensors stand for are x = descale_x · x8
+    (one factor per tensor, the reading adopted for "static scale factors"),
+    so the exact result is the plain definition over the dequantized values:
+      s_ij = scale · Σ_c (descale_q q8_ic)(descale_k k8_jc),
+      O_i  = Σ_j softmax_j(s_ij) · descale_v v8_j,  LSE_i = ln Σ_j exp(s_ij).
+    The two passes of the method (exact row maximum, then exponentials and
+    P·V with P in FP8) are how a kernel reaches this result; the rounding of
+    P to E4M3 is the kernel's error, bounded by the tests.
+    """
+    q = e4m3_to_f64(q8) * float(descale_q)
+    k = e4m3_to_f64(k8) * float(descale_k)
+    v = e4m3_to_f64(v8) * float(descale_v)
+    return attention_forward(q, k, v, scale, causal, causal_offset)

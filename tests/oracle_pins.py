@@ -511,4 +511,75 @@ def pin_backward_grouped_heads():
         assert np.max(np.abs(dV - rV.reshape(B, Sk, H_kv, g, d).sum(axis=3))) <= TOL
 
 
+# ---------------------------------------------------------------- FP8 (E4M3)
+def _e4m3_by_hand(b: int) -> float:
+    """Decode one E4M3 byte from its fields (1 sign, 4 exponent bits with bias
+    7, 3 mantissa bits; exponent 0 is subnormal; 0x7F/0xFF are NaN; no inf)."""
+    sign = -1.0 if b & 0x80 else 1.0
+    e, m = (b >> 3) & 0xF, b & 0x7
+    if e == 0xF and m == 0x7:
+        return math.nan
+    if e == 0:
+        return sign * (m / 8.0) * 2.0 ** -6
+    return sign * (1.0 + m / 8.0) * 2.0 ** (e - 7)
+
+
+def pin_e4m3_decoding():
+    import torch
+
+    codes = torch.arange(256, dtype=torch.int32).to(torch.uint8)
+    got = oracle.e4m3_to_f64(codes)
+    want = np.array([_e4m3_by_hand(b) for b in range(256)])
+    assert np.array_equal(np.isnan(got), np.isnan(want))
+    ok = ~np.isnan(want)
+    assert np.array_equal(got[ok], want[ok])
+    assert want[ok].max() == 448.0 and want[ok].min() == -448.0
+
+
+def _fp8_case(seed, B=1, Sq=5, Sk=7, H=2, d=64):
+    import torch
+
+    g = torch.Generator().manual_seed(seed)
+    q8 = (torch.randn((B, Sq, H, d), generator=g) * 40).to(torch.float8_e4m3fn)
+    k8 = (torch.randn((B, Sk, H, d), generator=g) * 40).to(torch.float8_e4m3fn)
+    v8 = (torch.randn((B, Sk, H, d), generator=g) * 40).to(torch.float8_e4m3fn)
+    return q8, k8, v8
+
+
+def pin_fp8_brute_force():
+    """The FP8 forward over the hand-decoded values, with the scale factors, by
+    pure-Python loops (math.fsum / math.exp)."""
+    q8, k8, v8 = _fp8_case(5)
+    dq, dk, dv, scale = 0.011, 0.02, 0.007, 0.125
+    dec = lambda t: np.vectorize(_e4m3_by_hand)(t.view(__import__("torch").uint8).numpy().astype(np.int64))
+    q, k, v = dec(q8) * dq, dec(k8) * dk, dec(v8) * dv
+    for causal in (False, True):
+        O, L = oracle.attention_forward_fp8(q8, k8, v8, dq, dk, dv, scale, causal)
+        B, Sq, H, d = q.shape
+        for h in range(H):
+            for i in range(Sq):
+                keys = [j for j in range(k.shape[1]) if not causal or j <= i]
+                s = [scale * math.fsum(q[0, i, h, c] * k[0, j, h, c] for c in range(d)) for j in keys]
+                mx = max(s)
+                e = [math.exp(x - mx) for x in s]
+                tot = math.fsum(e)
+                assert abs(L[0, h, i] - (mx + math.log(tot))) <= 1e-12
+                for c in range(d):
+                    o = math.fsum(e[n] * v[0, j, h, c] for n, j in enumerate(keys)) / tot
+                    assert abs(O[0, i, h, c] - o) <= 1e-12
+
+
+def pin_fp8_scale_factors():
+    """descale_q and descale_k act as a factor on the logits, descale_v as a
+    factor on O (LSE unchanged)."""
+    q8, k8, v8 = _fp8_case(6, Sq=9, Sk=11)
+    O1, L1 = oracle.attention_forward_fp8(q8, k8, v8, 0.02, 0.01, 0.5, 0.1, True)
+    O2, L2 = oracle.attention_forward_fp8(q8, k8, v8, 0.01, 0.01, 0.5, 0.2, True)
+    O3, L3 = oracle.attention_forward_fp8(q8, k8, v8, 0.02, 0.01, 1.5, 0.1, True)
+    assert np.allclose(O1, O2, atol=1e-13) and np.allclose(L1, L2, atol=1e-13)
+    assert np.allclose(3 * O1, O3, atol=1e-12) and np.allclose(L1, L3, atol=1e-13)
+    O4, L4 = oracle.attention_forward_fp8(q8, k8, v8, 0.02, 0.03, 0.5, 0.1, True)
+    assert not np.allclose(L1, L4)  # descale_k is not ignored
+
+
 ALL_PINS = [v for k_, v in sorted(globals().items()) if k_.startswith("pin_") and callable(v)]

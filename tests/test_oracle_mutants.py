@@ -37,6 +37,8 @@ MUTANTS = {
                              "            g = min(h, H_kv - 1)\n            O[b, :, h, :]"),
     "varlen_ignores_grouping": ("            g = kv_head(h, H, H_kv)\n            if k1 <= k0:",
                                 "            g = min(h, H_kv - 1)\n            if k1 <= k0:"),
+    "fp8_drops_descale_v": ("v = e4m3_to_f64(v8) * float(descale_v)", "v = e4m3_to_f64(v8)"),
+    "fp8_descale_k_for_q": ("q = e4m3_to_f64(q8) * float(descale_q)", "q = e4m3_to_f64(q8) * float(descale_k)"),
     "offset_ignored": ("keys[None, :] <= rows[:, None] + causal_offset", "keys[None, :] <= rows[:, None]"),
     "offset_negated": ("keys[None, :] <= rows[:, None] + causal_offset", "keys[None, :] <= rows[:, None] - causal_offset"),
     "forward_drops_offset": ("                                                         causal_offset=causal_offset)",
@@ -72,7 +74,7 @@ def test_mutant_is_caught(name, monkeypatch):
     mod = _load_mutant(*MUTANTS[name])
     for fn in ("attention_forward", "attention_head", "attention_rows", "attention_varlen", "attention_backward",
                "attention_backward_head", "head_probabilities", "head_scores", "kv_head", "visible_mask",
-               "combine_partials"):
+               "combine_partials", "attention_forward_fp8", "e4m3_to_f64"):
         monkeypatch.setattr(oracle, fn, getattr(mod, fn))
     caught = []
     for pin in oracle_pins.ALL_PINS:
