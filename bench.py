@@ -26,7 +26,10 @@ Variants of the workload (each its own JSON line, the metric unchanged):
 ``--varlen N`` N sequences of seeded lengths packed along the rows (FLOPs
 counted per sequence); ``--backward`` a step is the backward instead — the
 preparation kernel and the dK/dV and dQ passes, three launches — with FLOPs
-counted as 2.5× the forward's (S, dP, dV, dK, dQ).  The variants report no
+counted as 2.5× the forward's (S, dP, dV, dK, dQ); ``--fp8`` the FP8 (E4M3)
+forward on the workload's E4M3 inputs (head dim 128; FLOPs counted as for
+bf16, against twice the measured bf16 peak — the nominal FP8/BF16 ratio of
+the tensor core).  The variants report no
 ``e2e`` (the host-buffer entry point takes the dense forward only), and
 ``roofline.traffic`` is given only for workloads whose ncu counters are in
 ``profiles/traffic.json`` for the current kernel sources (else null).
@@ -286,6 +289,8 @@ def main():
     ap.add_argument("--varlen", type=int, default=0,
                     help="packed-sequence variant: this many sequences with a seeded mix of lengths up to the "
                          "workload's S (same H, d, mask); FLOPs counted per sequence")
+    ap.add_argument("--fp8", action="store_true",
+                    help="the FP8 (E4M3) forward on the workload's E4M3 inputs (head dim 128 workloads)")
     ap.add_argument("--shard", choices=["replicas", "heads"], default="replicas",
                     help="N > 1: every rank its own batch (weak scaling, default) or one problem's heads split "
                          "across the ranks (strong scaling)")
@@ -300,6 +305,9 @@ def main():
     w = inputs.WORKLOADS[args.config]
     if args.backward and (args.kv_heads or args.varlen or args.causal_align != "top-left"):
         ap.error("--backward takes the plain workloads")
+    if args.fp8 and (w.d != 128 or args.backward or args.varlen or args.kv_heads or args.shard != "replicas"
+                     or args.causal_align != "top-left"):
+        ap.error("--fp8 takes the plain head-dim-128 workloads (--config 2, 3 or 5)")
     if args.shard == "heads" and (args.backward or args.varlen or args.kv_heads):
         ap.error("--shard heads takes the plain forward workloads")
     if args.kv_heads or args.causal_align != "top-left" or args.varlen:
@@ -356,6 +364,15 @@ def main():
         def step():
             attn.attn_fwd_varlen(qd, kd, vd, cqd, ckd, max(lens), causal=w.causal, scale=w.scale, out=od, lse=ld,
                                  options=opts, causal_align=w.causal_align)
+    elif args.fp8:
+        q8, k8, v8, dq8, dk8, dv8 = inputs.make_fp8_inputs(w, seed=seed)
+        qd, kd, vd = q8.to(dev), k8.to(dev), v8.to(dev)
+        od = torch.empty(q8.shape, dtype=torch.bfloat16, device=dev)
+        ld = torch.empty((w.B, w.H, w.Sq), dtype=torch.float32, device=dev)
+
+        def step():
+            attn.attn_fwd_fp8(qd, kd, vd, dq8, dk8, dv8, causal=w.causal, scale=w.scale, out=od, lse=ld)
+        args.no_e2e = True
     elif args.shard == "heads":
         # One problem (the workload's own seed on every rank); this rank's
         # contiguous share of its B·H heads, as (batch, head) units.
@@ -475,7 +492,7 @@ def main():
         return
 
     peaks, peak_kind = load_peaks()
-    peak = float(peaks["bf16_tflops"])
+    peak = float(peaks["bf16_tflops"]) * (2.0 if args.fp8 else 1.0)
     traffic = load_profile_traffic(w.name)
     cpu = None
     if args.cpu_budget > 0 and world == 1:  # the CPU baseline is taken at N = 1 only
@@ -492,9 +509,9 @@ def main():
         "higher_is_better": True,
         "scaling": "strong" if args.shard == "heads" else "weak",
         "vs_baseline": None,
-        "dtype": "bf16",
+        "dtype": "e4m3" if args.fp8 else "bf16",
         "data": "synthetic",
-        "config": {"workload": w.name + ("_backward" if args.backward else ""), "B": w.B, "H": w.H, "H_kv": w.kv_heads, "Sq": w.Sq, "Sk": w.Sk, "d": w.d,
+        "config": {"workload": w.name + ("_backward" if args.backward else "") + ("_fp8" if args.fp8 else ""), "B": w.B, "H": w.H, "H_kv": w.kv_heads, "Sq": w.Sq, "Sk": w.Sk, "d": w.d,
                    "causal": w.causal, "causal_align": w.causal_align, "sigma_qk": w.sigma_qk, "seed": w.seed,
                    **({"varlen_lengths": lens} if lens is not None else {}),
                    "l2": "flushed between timed steps (256 MiB write)",
@@ -502,8 +519,10 @@ def main():
                    if world > 1 else "single"},
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak, "traffic": traffic,
-                     "peak_source": f"{peak_kind} bf16_tflops (burst cuBLAS)",
-                     "frac_of_contract_2250": achieved / CONTRACT_PEAK_TFLOPS},
+                     "peak_source": f"{peak_kind} bf16_tflops (burst cuBLAS)"
+                     + (" x 2 (nominal FP8/BF16 tensor ratio)" if args.fp8 else ""),
+                     **({"frac_of_nominal_fp8_4500": achieved / (2 * CONTRACT_PEAK_TFLOPS)} if args.fp8 else
+                        {"frac_of_contract_2250": achieved / CONTRACT_PEAK_TFLOPS})},
         "cpu_baseline": cpu,
         "e2e": e2e,
         "gpu_launches": args.steps * (3 if args.backward else 1),

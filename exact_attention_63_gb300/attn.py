@@ -27,7 +27,7 @@ ERRORS = {
 # Every symbol the header declares (checked by the CPU test-suite).
 EXPORTS = ["attn_fwd", "attn_fwd_ex", "attn_fwd_host", "attn_fwd_host_workspace_size", "attn_get_status",
            "attn_strerror", "attn_last_cuda_error", "attn_version", "attn_fwd_host_static", "attn_fwd_layout",
-           "attn_fwd_varlen", "attn_bwd", "attn_bwd_workspace_size", "attn_bwd_layout"]
+           "attn_fwd_varlen", "attn_bwd", "attn_bwd_workspace_size", "attn_bwd_layout", "attn_fwd_fp8"]
 
 CAUSAL_ALIGN = {"top-left": 0, "bottom-right": 1}
 
@@ -99,6 +99,8 @@ def lib():
     L.attn_fwd_host_workspace_size.restype = sz
     L.attn_fwd_host_static.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp]
     L.attn_fwd_host_static.restype = i
+    L.attn_fwd_fp8.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, f, f, f, i, vp]
+    L.attn_fwd_fp8.restype = i
     L.attn_get_status.argtypes = [vp]
     L.attn_get_status.restype = i
     L.attn_strerror.argtypes = [i]
@@ -327,6 +329,37 @@ def attn_fwd_host_static(q_h, k_h, v_h, o_h, lse_h, causal: bool, scale: float, 
                                     lse_h.data_ptr(), B, H, Sq, Sk, d, float(scale), int(bool(causal)),
                                     _stream_handle(stream))
     _check(rc)
+
+
+def attn_fwd_fp8(q8, k8, v8, descale_q: float, descale_k: float, descale_v: float, causal: bool = False,
+                 scale: float | None = None, out=None, lse=None, stream=None):
+    """Exact attention forward on FP8 (E4M3) inputs: q8 [B,Sq,H,128], k8, v8
+    [B,Sk,H,128] as torch.float8_e4m3fn (or their raw bytes as uint8), standing
+    for descale_x · x8.  Returns (o [B,Sq,H,128] bf16, lse [B,H,Sq] fp32)."""
+    for name, t in (("q8", q8), ("k8", k8), ("v8", v8)):
+        if t.dtype not in (torch.float8_e4m3fn, torch.uint8) or not t.is_cuda or t.dim() != 4 or \
+                not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous 4-D E4M3 CUDA tensor (batch, seq, heads, head_dim)")
+    B, Sq, H, d = q8.shape
+    if k8.shape != v8.shape or k8.shape[0] != B or k8.shape[2] != H or k8.shape[3] != d:
+        raise ValueError(f"shape mismatch: q8 {tuple(q8.shape)}, k8 {tuple(k8.shape)}, v8 {tuple(v8.shape)}")
+    Sk = k8.shape[1]
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty((B, Sq, H, d), dtype=torch.bfloat16, device=q8.device)
+    if lse is None:
+        lse = torch.empty((B, H, Sq), dtype=torch.float32, device=q8.device)
+    if out.dtype != torch.bfloat16 or tuple(out.shape) != (B, Sq, H, d) or not out.is_contiguous():
+        raise ValueError("out must be a contiguous bf16 tensor shaped like q8")
+    if lse.shape != (B, H, Sq) or lse.dtype != torch.float32 or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous fp32 tensor of shape (B, H, Sq)")
+    with torch.cuda.device(q8.device):
+        rc = lib().attn_fwd_fp8(q8.data_ptr(), k8.data_ptr(), v8.data_ptr(), out.data_ptr(), lse.data_ptr(),
+                                B, H, Sq, Sk, d, float(scale), float(descale_q), float(descale_k), float(descale_v),
+                                int(bool(causal)), _stream_handle(stream))
+    _check(rc)
+    return out, lse
 
 
 def get_status(stream=None) -> int:

@@ -24,7 +24,7 @@ BUILD_DIR = os.path.join(ROOT, "_build")
 LIB_NAME = "libattn_gb300.so"
 LIB_PATH = os.path.join(PKG, LIB_NAME)
 SOURCES = ["attn_api.cu", "attn_static.cu", "attn_fwd_d64.cu", "attn_fwd_d64_causal.cu", "attn_fwd_d128.cu",
-           "attn_fwd_d128_causal.cu", "attn_bwd.cu"]
+           "attn_fwd_d128_causal.cu", "attn_bwd.cu", "attn_fwd_fp8.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -69,6 +69,32 @@ int encode_bshd(CUtensorMap* m, const void* ptr, int B, int S, int H, int d, con
   return ATTN_OK;
 }
 
+// 4-D map over an 8-bit [B, S, H, d] tensor, dense, dims innermost first
+// (d, H, S, B); box (d, 1, 128, 1): one 128-row slab of d-byte rows (d = 128:
+// exactly one 128-byte swizzle row).
+int encode_bshd_u8(CUtensorMap* m, const void* ptr, int B, int S, int H, int d) {
+  auto enc = get_encode_fn();
+  if (enc == nullptr) {
+    std::snprintf(t_last_error, sizeof(t_last_error), "cuTensorMapEncodeTiled unavailable");
+    return ATTN_ERR_LAUNCH;
+  }
+  const cuuint64_t dims[4] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(S),
+                              static_cast<cuuint64_t>(B)};
+  const cuuint64_t strides[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(H) * d,
+                                 static_cast<cuuint64_t>(S) * H * d};
+  const cuuint32_t box[4] = {static_cast<cuuint32_t>(d), 1, 128, 1};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void*>(ptr), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    std::snprintf(t_last_error, sizeof(t_last_error), "cuTensorMapEncodeTiled failed (CUresult %d)",
+                  static_cast<int>(r));
+    return ATTN_ERR_LAUNCH;
+  }
+  return ATTN_OK;
+}
+
 struct DeviceInfo {
   int checked = 0;  // 0 unknown, 1 supported, -1 unsupported
   unsigned int* status = nullptr;
@@ -571,6 +597,58 @@ int attn_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse
 int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Sq, int Sk, int d,
              float scale, int causal, cudaStream_t stream) {
   return attn_fwd_ex(q, k, v, o, lse, B, H, Sq, Sk, d, scale, causal, nullptr, stream);
+}
+
+int attn_fwd_fp8(const void* q8, const void* k8, const void* v8, void* o, float* lse, int B, int H, int Sq, int Sk,
+                 int d, float scale, float descale_q, float descale_k, float descale_v, int causal,
+                 cudaStream_t stream) {
+  if (q8 == nullptr || k8 == nullptr || v8 == nullptr || o == nullptr || lse == nullptr) return ATTN_ERR_NULL;
+  if (B < 1 || H < 1 || Sq < 1 || Sk < 1) return ATTN_ERR_SHAPE;
+  const long long n_qt = (static_cast<long long>(Sq) + 127) / 128;
+  if (static_cast<long long>(B) * H * n_qt > 0x7FFFFFFFLL) return ATTN_ERR_SHAPE;
+  if (d != 128) return ATTN_ERR_HEAD_DIM;
+  if (!std::isfinite(scale) || !(scale > 0.f)) return ATTN_ERR_SCALE;
+  for (float f : {descale_q, descale_k, descale_v})
+    if (!std::isfinite(f) || !(f > 0.f)) return ATTN_ERR_SCALE;
+  const float sl = scale * descale_q * descale_k * 1.4426950408889634f;
+  if (!std::isfinite(sl) || !(sl > 0.f)) return ATTN_ERR_SCALE;
+  if (!aligned16(q8) || !aligned16(k8) || !aligned16(v8) || !aligned16(o) || !aligned16(lse)) return ATTN_ERR_ALIGN;
+  int dev = -1;
+  int rc = current_device(&dev);
+  if (rc != ATTN_OK) return rc;
+  attn::LaunchArgs a;
+  std::memset(&a, 0, sizeof(a));
+  const long long hd = static_cast<long long>(H) * d;
+  const long long os[3] = {Sq * hd, hd, d};
+  if ((rc = encode_bshd_u8(&a.q, q8, B, Sq, H, d)) != ATTN_OK) return rc;
+  if ((rc = encode_bshd_u8(&a.k, k8, B, Sk, H, d)) != ATTN_OK) return rc;
+  if ((rc = encode_bshd_u8(&a.v, v8, B, Sk, H, d)) != ATTN_OK) return rc;
+  if ((rc = encode_bshd(&a.o, o, B, Sq, H, d, os)) != ATTN_OK) return rc;
+  a.p.o = o;
+  a.p.lse = lse;
+  a.p.o_sb = os[0];
+  a.p.o_ss = os[1];
+  a.p.o_sh = os[2];
+  a.p.B = B;
+  a.p.H = H;
+  a.p.Sq = Sq;
+  a.p.Sk = Sk;
+  a.p.group = 1;
+  a.p.coff = 0;
+  a.p.lse_pitch = Sq;
+  a.p.n_qt = static_cast<int>(n_qt);
+  a.p.n_tiles = static_cast<int>(n_qt * B * H);
+  a.p.status = g_dev[dev].status;
+  a.p.scale_log2 = sl;
+  a.p.o_scale = descale_v / 448.0f;
+  a.p.timeout_ns = static_cast<uint64_t>(kDefaultTimeoutMs) * 1000000ull;
+  a.grid = a.p.n_tiles < g_dev[dev].sms ? a.p.n_tiles : g_dev[dev].sms;
+  a.sms = g_dev[dev].sms;
+  a.device = dev;
+  a.stream = stream;
+  const cudaError_t e = attn::launch_fwd_fp8(a, causal != 0);
+  if (e != cudaSuccess) return fail_cuda(e, "FP8 attention kernel launch");
+  return ATTN_OK;
 }
 
 size_t attn_bwd_workspace_size(int B, int H, int Sq) {

@@ -127,6 +127,7 @@ struct FwdParams {
   float scale_log2;              // scale · log2(e)
   float tau;                     // rescale threshold, log2 domain
   float sum_limit;               // 2^tau: a half-block row sum above it sends the warp to the maximum
+  float o_scale;                 // FP8 inputs: descale_v / 448 (O = o_scale · P8·V8 / L)
   uint64_t timeout_ns;
   uint32_t test_flags;           // bit 0: loader withholds K/V (exercises the wait limit)
 };

@@ -42,6 +42,9 @@ int fwd_host(const void* q_h, const void* k_h, const void* v_h, void* o_h, float
 // Record a failed CUDA call for attn_last_cuda_error(); returns ATTN_ERR_LAUNCH.
 int record_cuda_error(cudaError_t e, const char* what);
 
+// FP8 (E4M3) inputs, d = 128 (attn_fwd_fp8.cu).
+cudaError_t launch_fwd_fp8(const LaunchArgs& a, bool causal);
+
 cudaError_t launch_fwd_d64(const LaunchArgs& a);
 cudaError_t launch_fwd_d64_causal(const LaunchArgs& a);
 cudaError_t launch_fwd_d128(const LaunchArgs& a);

@@ -327,6 +327,32 @@ int attn_fwd_host_static(const void* q_h, const void* k_h, const void* v_h, void
                          cudaStream_t stream);
 
 /*
+ * attn_fwd_fp8 — exact attention forward on FP8 (E4M3) inputs.
+ *   "FlashAttention-3: Pipeline Assíncrono …", section "Estabilidade em FP8":
+ *   two passes over each query tile's keys — the exact row maximum of the
+ *   scaled logits first (products accumulated in fp32), then p ≤ 1 and O =
+ *   P·V with P rounded to E4M3 under a static scale (448 p).
+ *   q8, k8, v8 : device, E4M3 bytes (1 sign, 4 exponent, 3 mantissa bits),
+ *                dense [B, Sq, H, d] / [B, Sk, H, d] (read only); they stand
+ *                for descale_q·q8, descale_k·k8, descale_v·v8.
+ *   o          : device, bf16 [B, Sq, H, d] (written); lse: fp32 [B, H, Sq],
+ *                natural log of Σ_visible exp(scale · q_i · k_j) over the
+ *                dequantized values.
+ *   d          : 128 only (ATTN_ERR_HEAD_DIM otherwise).
+ *   scale, descale_q, descale_k, descale_v : finite and > 0 (ATTN_ERR_SCALE).
+ *   causal     : top-left alignment (key j visible to row i iff j ≤ i).
+ *   Accuracy: O differs from the exact result over the dequantized inputs by
+ *   at most Σ_j |p̂_ij − p_ij|·|v_j| / Σ_j p_ij (+ the bf16 rounding of O),
+ *   p̂ being p rounded to E4M3 (relative 2^-4, or 2^-10/448 below E4M3's
+ *   normal range); LSE is as accurate as the bf16 path's.
+ *   Asynchronous on `stream`; errors as attn_fwd.
+ */
+int attn_fwd_fp8(const void* q8, const void* k8, const void* v8, void* o, float* lse,
+                 int B, int H, int Sq, int Sk, int d, float scale,
+                 float descale_q, float descale_k, float descale_v, int causal,
+                 cudaStream_t stream);
+
+/*
  * attn_get_status — synchronises `stream`, then returns and clears the current
  * device's status word: ATTN_OK, or ATTN_ERR_TIMEOUT if any kernel launched
  * by this library on this device since the last call hit a wait limit, or

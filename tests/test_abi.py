@@ -179,3 +179,17 @@ def test_static_workspace_size_matches_header():
     m = re.search(r"#define\s+ATTN_STATIC_WORKSPACE_BYTES\s+\((\d+)u\s*<<\s*(\d+)\)", src)
     assert m, "ATTN_STATIC_WORKSPACE_BYTES not found in the header"
     assert int(m.group(1)) << int(m.group(2)) == attn.STATIC_WORKSPACE_BYTES
+
+
+@pytest.mark.parametrize("args,expect", [
+    ((0, A, A, A, A, 1, 1, 8, 8, 128, 0.1, 1.0, 1.0, 1.0, 0), -1),
+    ((A, A, A, A, A, 0, 1, 8, 8, 128, 0.1, 1.0, 1.0, 1.0, 0), -2),
+    ((A, A, A, A, A, 1, 1, 8, 8, 64, 0.1, 1.0, 1.0, 1.0, 0), -3),
+    ((A, A, A, A, A, 1, 1, 8, 8, 128, 0.0, 1.0, 1.0, 1.0, 0), -4),
+    ((A, A, A, A, A, 1, 1, 8, 8, 128, 0.1, 0.0, 1.0, 1.0, 0), -4),
+    ((A, A, A, A, A, 1, 1, 8, 8, 128, 0.1, 1.0, float("inf"), 1.0, 0), -4),
+    ((A, A, A, A, A, 1, 1, 8, 8, 128, 0.1, 1.0, 1.0, -1.0, 0), -4),
+    ((A + 1, A, A, A, A, 1, 1, 8, 8, 128, 0.1, 1.0, 1.0, 1.0, 0), -5),
+])
+def test_fp8_rejects_bad_arguments_before_launch(L, args, expect):
+    assert L.attn_fwd_fp8(*args, None) == expect
