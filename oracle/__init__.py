@@ -14,6 +14,7 @@ library routines and invariants; no function is "parity unpinned".
 from .attention import (  # noqa: F401
     attention_backward,
     attention_backward_head,
+    attention_backward_rows,
     attention_forward,
     attention_forward_fp8,
     attention_head,

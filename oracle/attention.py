@@ -226,6 +226,46 @@ def attention_backward_head(q, k, v, dO, scale: float, causal: bool, causal_offs
     return scale * (dS @ k), scale * (dS.T @ q), dV, D
 
 
+def attention_backward_rows(q, k, v, dO, scale: float, causal: bool, qrows, krows, causal_offset: int = 0):
+    """Selected rows of one head's gradients, without the whole Sq×Sk matrices.
+
+    The same formulas as attention_backward_head, evaluated for query rows
+    ``qrows`` (rows of dQ) and key rows ``krows`` (rows of dK and dV): a query
+    row's dQ needs only its own scores, P_ij = exp(s_ij − LSE_i),
+    dP_ij = dO_i · v_j and D_i = dO_i · O_i; a key row's dK and dV sum over
+    every query row, taken in chunks of ROW_CHUNK rows.  O and LSE come from
+    attention_head.  Returns (dQ [len(qrows), d], dK [len(krows), d],
+    dV [len(krows), d]).
+    """
+    q, k, v, dO = (np.asarray(x, dtype=np.float64) for x in (q, k, v, dO))
+    qrows = np.asarray(qrows, dtype=np.int64)
+    krows = np.asarray(krows, dtype=np.int64)
+    Sq, Sk = q.shape[0], k.shape[0]
+    O, LSE = attention_head(q, k, v, scale, causal, causal_offset=causal_offset)
+    D = (dO * O).sum(axis=1)
+
+    def probs(rows, keys):
+        s = head_scores(q[rows], k[keys], scale)
+        mask = visible_mask(rows, Sk, causal, causal_offset)[:, keys]
+        finite = np.isfinite(LSE[rows])
+        with np.errstate(invalid="ignore"):
+            P = np.where(mask & finite[:, None], np.exp(s - np.where(finite, LSE[rows], 0.0)[:, None]), 0.0)
+        return P
+
+    P = probs(qrows, np.arange(Sk))
+    dS = P * (dO[qrows] @ v.T - D[qrows][:, None])
+    dQ = scale * (dS @ k)
+    dK = np.zeros((krows.shape[0], k.shape[1]))
+    dV = np.zeros((krows.shape[0], v.shape[1]))
+    for c0 in range(0, Sq, ROW_CHUNK):
+        rows = np.arange(c0, min(Sq, c0 + ROW_CHUNK))
+        P = probs(rows, krows)
+        dS = P * (dO[rows] @ v[krows].T - D[rows][:, None])
+        dV += P.T @ dO[rows]
+        dK += scale * (dS.T @ q[rows])
+    return dQ, dK, dV
+
+
 def attention_backward(q, k, v, dO, scale: float, causal: bool, causal_offset: int = 0):
     """Gradients over all batches and heads: q, dO [B, Sq, H, d], k, v
     [B, Sk, H_kv, d] (torch tensors or arrays; H a multiple of H_kv).  A

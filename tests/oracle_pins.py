@@ -511,6 +511,23 @@ def pin_backward_grouped_heads():
         assert np.max(np.abs(dV - rV.reshape(B, Sk, H_kv, g, d).sum(axis=3))) <= TOL
 
 
+def pin_backward_rows_subset():
+    """Selected gradient rows equal the same rows of the whole-head backward
+    (causal with an offset, and non-causal; 1100 query rows, so the key-row
+    sums cross a query chunk)."""
+    rng = np.random.default_rng(17)
+    Sq, Sk, d = 1100, 260, 8
+    q, k, v, dO = (rng.standard_normal((n, d)) for n in (Sq, Sk, Sk, Sq))
+    qrows = np.array([0, 1, 127, 128, 150, 1023, 1024, 1099])
+    krows = np.array([0, 5, 128, 200, 259])
+    for causal, off in ((False, 0), (True, 0), (True, Sk - Sq)):
+        dq, dk, dv, _ = oracle.attention_backward_head(q, k, v, dO, 0.3, causal, off)
+        rq, rk, rv = oracle.attention_backward_rows(q, k, v, dO, 0.3, causal, qrows, krows, off)
+        assert np.allclose(rq, dq[qrows], atol=1e-12)
+        assert np.allclose(rk, dk[krows], atol=1e-12)
+        assert np.allclose(rv, dv[krows], atol=1e-12)
+
+
 # ---------------------------------------------------------------- FP8 (E4M3)
 def _e4m3_by_hand(b: int) -> float:
     """Decode one E4M3 byte from its fields (1 sign, 4 exponent bits with bias

@@ -106,3 +106,26 @@ def test_backward_deterministic():
     b_ = attn.attn_bwd(q, k, v, o, lse, dout, causal=True)
     torch.cuda.synchronize()
     assert all(torch.equal(x, y) for x, y in zip(a, b_))
+
+
+def test_backward_longest_workload_sampled_rows():
+    """Workload 5's backward at full size (B1 H16 S32768 d128 causal): dQ rows
+    and dK, dV rows sampled across the sequence (the first and last tiles,
+    tile edges, the middle, random rows) in two heads, against the oracle's
+    per-row gradients (its whole-head matrices would be 32768² float64).  The
+    tolerance's scale is the largest |value| among the sampled rows."""
+    need_gpu()
+    w = inputs.WORKLOADS[5]
+    q, k, v = inputs.make_inputs(w)
+    g = torch.Generator().manual_seed(w.seed + 2000)
+    dout = torch.randn(q.shape, generator=g).to(torch.bfloat16)
+    dq, dk, dv = grads(w, q, k, v, dout)
+    rng = np.random.default_rng(5)
+    fixed = [0, 1, 127, 128, 255, 256, 16383, 16384, w.Sq - 129, w.Sq - 128, w.Sq - 1]
+    rows = np.array(sorted(set(fixed) | set(int(x) for x in rng.integers(0, w.Sq, 20))))
+    for h in (0, w.H - 1):
+        sel = lambda t: oracle.to_f64(t[0, :, h, :])
+        rq, rk, rv = oracle.attention_backward_rows(sel(q), sel(k), sel(v), sel(dout), w.scale, w.causal, rows, rows)
+        check("dq", dq[0, rows, h], rq, f"{w.name} head {h}")
+        check("dk", dk[0, rows, h], rk, f"{w.name} head {h}")
+        check("dv", dv[0, rows, h], rv, f"{w.name} head {h}")

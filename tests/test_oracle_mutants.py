@@ -39,6 +39,8 @@ MUTANTS = {
                                 "            g = min(h, H_kv - 1)\n            if k1 <= k0:"),
     "fp8_drops_descale_v": ("v = e4m3_to_f64(v8) * float(descale_v)", "v = e4m3_to_f64(v8)"),
     "fp8_descale_k_for_q": ("q = e4m3_to_f64(q8) * float(descale_q)", "q = e4m3_to_f64(q8) * float(descale_k)"),
+    "bwd_rows_drop_d": ("dS = P * (dO[rows] @ v[krows].T - D[rows][:, None])", "dS = P * (dO[rows] @ v[krows].T)"),
+    "bwd_rows_dv_one_chunk": ("        dV += P.T @ dO[rows]", "        dV = P.T @ dO[rows]"),
     "offset_ignored": ("keys[None, :] <= rows[:, None] + causal_offset", "keys[None, :] <= rows[:, None]"),
     "offset_negated": ("keys[None, :] <= rows[:, None] + causal_offset", "keys[None, :] <= rows[:, None] - causal_offset"),
     "forward_drops_offset": ("                                                         causal_offset=causal_offset)",
@@ -74,7 +76,7 @@ def test_mutant_is_caught(name, monkeypatch):
     mod = _load_mutant(*MUTANTS[name])
     for fn in ("attention_forward", "attention_head", "attention_rows", "attention_varlen", "attention_backward",
                "attention_backward_head", "head_probabilities", "head_scores", "kv_head", "visible_mask",
-               "combine_partials", "attention_forward_fp8", "e4m3_to_f64"):
+               "combine_partials", "attention_forward_fp8", "e4m3_to_f64", "attention_backward_rows"):
         monkeypatch.setattr(oracle, fn, getattr(mod, fn))
     caught = []
     for pin in oracle_pins.ALL_PINS:
