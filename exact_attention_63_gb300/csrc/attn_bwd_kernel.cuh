@@ -24,11 +24,16 @@
 // operand like the forward's P·V.  No atomics: dQ and dK/dV are separate
 // passes.
 //
-// Warp roles (320 threads): warps 0-7 turn S, dP into P, dS (warpgroup h owns
+// Warp roles (352 threads): warps 0-7 turn S, dP into P, dS (warpgroup h owns
 // columns [64h, 64h+64) of each block; one thread per row) and write the
 // tile's outputs; warp 8 loads X, X2 once and streams (A, B) blocks — plus, in
 // DKV, the 128 log2-LSE and D values of the block's queries — through a ring;
-// warp 9 issues the MMAs.
+// warp 9 issues S and dP, warp 10 the accumulations.  One thread issues at
+// most one tcgen05.mma every ~45 cycles (more beside busy warps): a block is
+// 24 (d = 64) to 32 (d = 128) MMAs, about as long as the tensor core's own
+// work on them, so the issue is split; every dependency between the two
+// threads' MMAs goes through a completion barrier, and each accumulator is
+// written by one thread only (in issue order).
 //
 // Schedule.  A shared-memory-operand MMA reads both of its tiles at the
 // shared-memory rate (128 B/clk per SM: a 128×128×16 product takes its 64
@@ -58,9 +63,10 @@
 
 namespace attn {
 
-constexpr int kBwdThreads = 320;
+constexpr int kBwdThreads = 352;
 constexpr int kBwdLoaderWarp = 8;
-constexpr int kBwdMmaWarp = 9;
+constexpr int kBwdMmaWarp = 9;   // S and dP
+constexpr int kBwdAccWarp = 10;  // the accumulations (dV, dK or dQ)
 constexpr int kModeDQ = 0;
 constexpr int kModeDKV = 1;
 
@@ -166,7 +172,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
     mbar_init(bar_acc_a, 1);
     mbar_init(bar_acc_b, 1);
-    mbar_init(bar_done, 1);
+    mbar_init(bar_done, 2);  // one commit per issuing thread
     for (int i = 0; i < 2; ++i) mbar_init(bar_dq_done(i), 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     fence_proxy_async_smem();
@@ -214,8 +220,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         while (!mbar_try_wait(bar_ring_full(m % L::kStages), (m / L::kStages) & 1u))
           if (globaltimer_ns() - t0 > p.timeout_ns) break;
     }
-  } else if (warp == kBwdMmaWarp) {
-    // ======================================================== MMA issuer
+  } else if (warp == kBwdMmaWarp || warp == kBwdAccWarp) {
+    // ======================================================= MMA issuers
     if (lane == 0 && nblk > 0) {
       constexpr uint32_t idS = idesc_bf16(128, 128, false);
       constexpr uint32_t idAcc = idesc_bf16(128, D, true);
@@ -246,72 +252,80 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           mma_ts(tAcc, tT + 8 * kk, dM + (((4 * hh + kk) * 2048) >> 4), idAcc, acc);
         }
       };
-      bool ok = wait_bar(bar_fix, 0, wc) && wait_bar(bar_ring_full(0), 0, wc);
-      if (ok) {
-        tc_fence_after();
-        product(0, 0);
-        product(0, 1);
-      }
-      for (int n = 0; n < nblk && ok; ++n) {
-        const bool more = n + 1 < nblk;
-        if (MODE == kModeDKV) {
-          // dV += Pᵀ dO, half by half as the warpgroups store P.
-          for (int hh = 0; hh < 2 && ok; ++hh) {
-            if (!wait_bar(bar_p_full(hh), n & 1, wc)) { ok = false; break; }
-            tc_fence_after();
-            acc_half(n, hh, tAcc0, tS + 64 * hh, 1);
-          }
-          if (!ok) break;
-          mma_commit(bar_acc_a);
-          // S(n+1) overwrites P(n): it goes in as soon as dV(n) has completed
-          // (a completion barrier: MMAs into different accumulators are not
-          // ordered), ahead of dK(n), so the warpgroups find it ready when
-          // they have stored dS(n).
-          if (more) {
-            if (!wait_bar(bar_ring_full((n + 1) % L::kStages), ((n + 1) / L::kStages) & 1, wc)) { ok = false; break; }
+      bool ok = true;
+      if (warp == kBwdMmaWarp) {
+        // ----------------------------------------------- S and dP issuer
+        ok = wait_bar(bar_fix, 0, wc) && wait_bar(bar_ring_full(0), 0, wc);
+        if (ok) {
+          tc_fence_after();
+          product(0, 0);
+          product(0, 1);
+        }
+        for (int n = 0; n + 1 < nblk && ok; ++n) {
+          if (!wait_bar(bar_ring_full((n + 1) % L::kStages), ((n + 1) / L::kStages) & 1, wc)) { ok = false; break; }
+          if (MODE == kModeDKV) {
+            // S(n+1) overwrites P(n): it goes in once dV(n) has completed;
+            // dP(n+1) overwrites dS(n) once dK(n) has.
             if (!wait_bar(bar_acc_a, n & 1, wc)) { ok = false; break; }
             tc_fence_after();
             product(n + 1, 0);
-          }
-          // dK += dSᵀ Q.
-          for (int hh = 0; hh < 2 && ok; ++hh) {
-            if (!wait_bar(bar_ds_full(hh), n & 1, wc)) { ok = false; break; }
-            tc_fence_after();
-            acc_half(n, hh, tAcc1, tdP + 64 * hh, 0);
-          }
-          if (!ok) break;
-          mma_commit(bar_acc_b);
-          mma_commit(bar_ring_empty(n % L::kStages));  // A(n), B(n) no longer read
-          // dP(n+1) overwrites dS(n): dK must have completed.
-          if (more) {
             if (!wait_bar(bar_acc_b, n & 1, wc)) { ok = false; break; }
             tc_fence_after();
             product(n + 1, 1);
-          }
-        } else {
-          // S(n+1) as soon as both warpgroups have read S(n).
-          if (more) {
-            if (!wait_bar(bar_ring_full((n + 1) % L::kStages), ((n + 1) / L::kStages) & 1, wc)) { ok = false; break; }
+          } else {
+            // S(n+1) as soon as both warpgroups have read S(n); dP(n+1) as
+            // soon as they have stored dS(n) (so read dP(n); dS has columns
+            // of its own).
             for (int hh = 0; hh < 2 && ok; ++hh)
               if (!wait_bar(bar_p_full(hh), n & 1, wc)) ok = false;
             if (!ok) break;
             tc_fence_after();
             product(n + 1, 0);
-          }
-          // dQ += dS K as the warpgroups store dS (which also means that they
-          // have read dP(n)).
-          for (int hh = 0; hh < 2 && ok; ++hh) {
-            if (!wait_bar(bar_ds_full(hh), n & 1, wc)) { ok = false; break; }
+            for (int hh = 0; hh < 2 && ok; ++hh)
+              if (!wait_bar(bar_ds_full(hh), n & 1, wc)) ok = false;
+            if (!ok) break;
             tc_fence_after();
-            acc_half(n, hh, tAcc0, tDS(n) + 32 * hh, 0);
+            product(n + 1, 1);
           }
-          if (!ok) break;
-          mma_commit(bar_dq_done(n & 1));
-          mma_commit(bar_ring_empty(n % L::kStages));
-          if (more) product(n + 1, 1);
+        }
+      } else {
+        // --------------------------------------------- accumulation issuer
+        // The ring slot of block n is released after its last accumulation:
+        // S(n) and dP(n), its other readers, have completed by then (the
+        // warpgroups stored dS(n) after reading both).
+        for (int n = 0; n < nblk && ok; ++n) {
+          if (MODE == kModeDKV) {
+            // dV += Pᵀ dO, half by half as the warpgroups store P.
+            for (int hh = 0; hh < 2 && ok; ++hh) {
+              if (!wait_bar(bar_p_full(hh), n & 1, wc)) { ok = false; break; }
+              tc_fence_after();
+              acc_half(n, hh, tAcc0, tS + 64 * hh, 1);
+            }
+            if (!ok) break;
+            mma_commit(bar_acc_a);
+            // dK += dSᵀ Q.
+            for (int hh = 0; hh < 2 && ok; ++hh) {
+              if (!wait_bar(bar_ds_full(hh), n & 1, wc)) { ok = false; break; }
+              tc_fence_after();
+              acc_half(n, hh, tAcc1, tdP + 64 * hh, 0);
+            }
+            if (!ok) break;
+            mma_commit(bar_acc_b);
+          } else {
+            // dQ += dS K as the warpgroups store dS.
+            for (int hh = 0; hh < 2 && ok; ++hh) {
+              if (!wait_bar(bar_ds_full(hh), n & 1, wc)) { ok = false; break; }
+              tc_fence_after();
+              acc_half(n, hh, tAcc0, tDS(n) + 32 * hh, 0);
+            }
+            if (!ok) break;
+            mma_commit(bar_dq_done(n & 1));
+          }
+          mma_commit(bar_ring_empty(n % L::kStages));  // A(n), B(n) no longer read
         }
       }
-      // Every MMA must finish before the accumulators are read or TMEM freed.
+      // Every MMA must finish before the accumulators are read or TMEM freed
+      // (bar_done completes once both issuing threads have committed).
       mma_commit(bar_done);
       const uint64_t t0 = globaltimer_ns();
       while (!mbar_try_wait(bar_done, 0))
