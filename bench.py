@@ -66,7 +66,7 @@ def load_peaks():
 
 
 KERNEL_SOURCES = ["exact_attention_63_gb300/csrc/attn_fwd_kernel.cuh", "exact_attention_63_gb300/csrc/attn_fwd_rows.cuh",
-                  "exact_attention_63_gb300/csrc/attn_device.cuh"]
+                  "exact_attention_63_gb300/csrc/attn_fwd_fp8.cuh", "exact_attention_63_gb300/csrc/attn_device.cuh"]
 
 
 def kernel_source_hash():
@@ -493,7 +493,8 @@ def main():
 
     peaks, peak_kind = load_peaks()
     peak = float(peaks["bf16_tflops"]) * (2.0 if args.fp8 else 1.0)
-    traffic = load_profile_traffic(w.name)
+    # (forward kernels only: the backward's sources are not in the recorded hash)
+    traffic = None if args.backward else load_profile_traffic(w.name + ("_fp8" if args.fp8 else ""))
     cpu = None
     if args.cpu_budget > 0 and world == 1:  # the CPU baseline is taken at N = 1 only
         rate, sample, cores, _, _ = cpu_oracle_rate(w, args.cpu_budget)
