@@ -66,7 +66,8 @@ def load_peaks():
 
 
 KERNEL_SOURCES = ["exact_attention_63_gb300/csrc/attn_fwd_kernel.cuh", "exact_attention_63_gb300/csrc/attn_fwd_rows.cuh",
-                  "exact_attention_63_gb300/csrc/attn_fwd_fp8.cuh", "exact_attention_63_gb300/csrc/attn_device.cuh"]
+                  "exact_attention_63_gb300/csrc/attn_fwd_fp8.cuh", "exact_attention_63_gb300/csrc/attn_fwd_fp8_rows.cuh",
+                  "exact_attention_63_gb300/csrc/attn_device.cuh"]
 
 
 def kernel_source_hash():
