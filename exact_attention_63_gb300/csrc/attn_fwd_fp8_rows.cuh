@@ -18,6 +18,9 @@
 //    128 E4M3 keys is one swizzle row, the layout of Q), and O += P8·V reads
 //    both operands from shared memory.  S is therefore free as soon as the
 //    softmax has loaded it: S(g+1) runs while the softmax is still on block g.
+//  * Pass 1 does not touch O, so its S blocks alternate between S's columns
+//    and O's (once the previous tile's epilogue has read O): S(j+1) of pass 1
+//    is computed while the softmax still loads S(j).
 //  * The factor 448 is folded into the exponent: with m' = m − log2 448,
 //    2^(x − m') = 448 p is what E4M3 rounds, the row sum is 448 L, and
 //    O = descale_v · (P8·V8) / (448 L), LSE = (m' + log2(448 L)) · ln 2.
@@ -42,8 +45,14 @@
 // the tile two ahead into that Q buffer and releases the P8 buffer.
 //
 // Ordering (every wait is within one phase of the phase it waits for):
-//  * s_full(g): S(g) complete.  S(g+1) is issued after s_free(g) (all four
-//    softmax warps have loaded S(g)), so s_full cannot run a phase ahead.
+//  * S buffer b ∈ {0 (S's columns), 1 (O's columns)}: pass-1 block j uses
+//    buffer j & 1, pass 2 buffer 0; issuer and softmax count the uses of each
+//    buffer alike.  Use u of buffer b completes s_full[b] and is issued after
+//    s_free[b] of use u − 1 (all four softmax warps have loaded it), so
+//    s_full[b] cannot run a phase ahead.
+//  * Buffer 1's first use in tile t > 0 waits for o_free of tile t − 1 (the
+//    epilogue has loaded O); that epilogue needs the whole of tile t − 1, and
+//    tile t's first P·V (which overwrites O) needs its pass 1 loaded.
 //  * p_full(g'): P8 of pass-2 block g' stored.  P8(g'+1) is stored after
 //    pv_done(g'), which needs P·V(g'), issued after p_full(g').
 //  * A tile's first P8 is stored after stage_empty of the previous tile (its
@@ -63,8 +72,9 @@ struct Fp8RowsLayout {
   static constexpr uint32_t kRingOff = 2 * kTileBytes;
   static constexpr uint32_t kPOff = kRingOff + kRing * kTileBytes;  // P8 (column slab 1 of the output staging)
   static constexpr uint32_t kBarOff = kPOff + kTileBytes;
-  // q_full[2], kv_full[R], kv_empty[R], s_full, s_free, p_full, pv_done, o_final, stage_full, stage_empty, done[2]
-  static constexpr int kNumBars = 2 + 2 * kRing + 5 + 2 + 2;
+  // q_full[2], kv_full[R], kv_empty[R], s_full[2], s_free[2], p_full, pv_done, o_final, o_free, stage_full,
+  // stage_empty, done[2]
+  static constexpr int kNumBars = 2 + 2 * kRing + 4 + 4 + 2 + 2;
   static constexpr uint32_t kMiscOff = kBarOff + 8 * kNumBars;  // tmem base (4 B) + abort flag (4 B)
   static constexpr uint32_t kSmemBytes = kMiscOff + 16 + 1024;  // + slack to align the base to 1024
   static constexpr uint32_t kTmemCols = 256;
@@ -102,14 +112,15 @@ __global__ void __launch_bounds__(kFp8RowsThreads, 2)
   auto bar_kv_full = [&](int s) { return bars + 8u * (2 + s); };
   auto bar_kv_empty = [&](int s) { return bars + 8u * (2 + L::kRing + s); };
   constexpr uint32_t kB0 = 2 + 2 * L::kRing;
-  const uint32_t bar_s_full = bars + 8u * kB0;
-  const uint32_t bar_s_free = bars + 8u * (kB0 + 1);
-  const uint32_t bar_p_full = bars + 8u * (kB0 + 2);
-  const uint32_t bar_pv_done = bars + 8u * (kB0 + 3);
-  const uint32_t bar_o_final = bars + 8u * (kB0 + 4);
-  const uint32_t bar_stage_full = bars + 8u * (kB0 + 5);
-  const uint32_t bar_stage_empty = bars + 8u * (kB0 + 6);
-  auto bar_done = [&](int i) { return bars + 8u * (kB0 + 7 + i); };
+  auto bar_s_full = [&](int b) { return bars + 8u * (kB0 + b); };
+  auto bar_s_free = [&](int b) { return bars + 8u * (kB0 + 2 + b); };
+  const uint32_t bar_p_full = bars + 8u * (kB0 + 4);
+  const uint32_t bar_pv_done = bars + 8u * (kB0 + 5);
+  const uint32_t bar_o_final = bars + 8u * (kB0 + 6);
+  const uint32_t bar_o_free = bars + 8u * (kB0 + 7);
+  const uint32_t bar_stage_full = bars + 8u * (kB0 + 8);
+  const uint32_t bar_stage_empty = bars + 8u * (kB0 + 9);
+  auto bar_done = [&](int i) { return bars + 8u * (kB0 + 10 + i); };
   uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMiscOff);
   volatile uint32_t* const abort_flag = reinterpret_cast<volatile uint32_t*>(smem + L::kMiscOff + 4);
 
@@ -129,16 +140,17 @@ __global__ void __launch_bounds__(kFp8RowsThreads, 2)
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar_q_full(i), 1);
       mbar_init(bar_done(i), 1);
+      mbar_init(bar_s_full(i), 1);
+      mbar_init(bar_s_free(i), kSmWarps);
     }
     for (int s = 0; s < L::kRing; ++s) {
       mbar_init(bar_kv_full(s), 1);
       mbar_init(bar_kv_empty(s), 1);
     }
-    mbar_init(bar_s_full, 1);
-    mbar_init(bar_s_free, kSmWarps);
     mbar_init(bar_p_full, kSmWarps);
     mbar_init(bar_pv_done, 1);
     mbar_init(bar_o_final, 1);
+    mbar_init(bar_o_free, kSmWarps);
     mbar_init(bar_stage_full, kSmWarps);
     mbar_init(bar_stage_empty, 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -233,26 +245,31 @@ __global__ void __launch_bounds__(kFp8RowsThreads, 2)
         constexpr uint32_t idS = idesc_e4m3(kBM, kBN, false);
         const uint64_t dQ = sdesc_kmajor_sw128(sQ);
         const uint64_t dK = sdesc_kmajor_sw128(sRing);
-        const uint32_t tS = tmem + L::kColS;
-        int g = 0, tc = 0, tbase = 0;
+        int uses0 = 0, uses1 = 0, tc = 0, tbase = 0;  // uses of S buffer 0 and 1 so far
         for (int idx = blockIdx.x; idx < n_tiles && ok; idx += stride, ++tc) {
           const Tile T = tile_info<CAUSAL, VARLEN>(idx, p);
           const int qb = tc & 1;
           if (!wait_bar(bar_q_full(qb), (tc >> 1) & 1, wc)) { ok = false; break; }
           for (int pass = 0; pass < 2 && ok; ++pass) {
-            for (int j = 0; j < T.nb; ++j, ++g) {
+            for (int j = 0; j < T.nb; ++j) {
               const int n = tbase + (pass == 0 ? j : pos_k2(j, T.nb)), slot = n % L::kRing;
+              const int b = (pass == 0) ? (j & 1) : 0;
               if (!wait_bar(bar_kv_full(slot), (n / L::kRing) & 1, wc)) { ok = false; break; }
-              // The S buffer is free once the softmax has loaded S(g−1).
-              if (g > 0 && !wait_bar(bar_s_free, (g - 1) & 1, wc)) { ok = false; break; }
+              // O's columns take S once the previous tile's epilogue has read O.
+              if (b == 1 && j == 1 && tc > 0 && !wait_bar(bar_o_free, (tc - 1) & 1, wc)) { ok = false; break; }
+              // The buffer is free once the softmax has loaded its previous S.
+              const int u = b ? uses1 : uses0;
+              if (u > 0 && !wait_bar(bar_s_free(b), (u - 1) & 1, wc)) { ok = false; break; }
               tc_fence_after();
               const uint64_t dq = dQ + ((qb * L::kTileBytes) >> 4);
               const uint64_t dk = dK + ((slot * L::kTileBytes) >> 4);
+              const uint32_t tS = tmem + (b == 0 ? L::kColS : L::kColO);
 #pragma unroll
               for (int kk = 0; kk < L::D / 32; ++kk)  // K = 32 E4M3 (32 bytes) per step
                 mma_ss_f8(tS, dq + 2 * kk, dk + 2 * kk, idS, kk > 0 ? 1u : 0u);
-              mma_commit(bar_s_full);
+              mma_commit(bar_s_full(b));
               mma_commit(bar_kv_empty(slot));  // K_j no longer read
+              if (b) ++uses1; else ++uses0;
             }
           }
           tbase += 3 * T.nb;
@@ -296,13 +313,12 @@ __global__ void __launch_bounds__(kFp8RowsThreads, 2)
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kFp8RowsSoftmaxRegs));
     const int r = threadIdx.x & 127;  // row within the tile = TMEM lane
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    const uint32_t tS = tmem + L::kColS + lane_off;
     const uint32_t tO = tmem + L::kColO + lane_off;
     const float sc = p.scale_log2;  // scale · descale_q · descale_k · log2(e)
     const uint64_t sc2 = pack2(sc, sc);
     uint8_t* const p_row = smem + L::kPOff + r * 128;  // this row of the P8 tile
     bool ok = true;
-    int g = 0, gp = 0, tc = 0;
+    int uses0 = 0, uses1 = 0, gp = 0, tc = 0;  // uses of S buffer 0 and 1 so far
     for (int idx = blockIdx.x; idx < n_tiles && ok; idx += stride, ++tc) {
       const Tile T = tile_info<CAUSAL, VARLEN>(idx, p);
       const int q_row = T.q0 + r;
@@ -310,19 +326,21 @@ __global__ void __launch_bounds__(kFp8RowsThreads, 2)
       // tile's first row need no mask.
       const int lim = CAUSAL ? min(p.Sk, T.q0 + 1 + p.coff) : p.Sk;
       const int n_full = min(T.nb, max(0, lim / kBN));
-      // The row's 128 scores of block j (raw logits, fp32), masked; S(g) is
-      // released as soon as it is in registers.
-      auto load_s = [&](int j, uint32_t (&u)[kBN]) -> bool {
-        const bool got = wait_bar_cold(bar_s_full, g & 1, wc);
+      // The row's 128 scores of block j (raw logits, fp32) from buffer b,
+      // masked; the buffer is released as soon as they are in registers.
+      auto load_s = [&](int j, int b, uint32_t (&u)[kBN]) -> bool {
+        const bool got = wait_bar_cold(bar_s_full(b), (b ? uses1 : uses0) & 1, wc);
         if (__any_sync(0xffffffffu, !got)) return false;
         tc_fence_after();
+        const uint32_t tS = tmem + (b == 0 ? L::kColS : L::kColO) + lane_off;
 #pragma unroll
         for (int c = 0; c < 4; ++c) tmem_ld32(tS + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(&u[32 * c]));
         tmem_wait_ld();
 #pragma unroll
         for (int c = 0; c < 4; ++c) reg_fence32(*reinterpret_cast<uint32_t(*)[32]>(&u[32 * c]));
         tc_fence_before();
-        warp_arrive(bar_s_free, lane);
+        warp_arrive(bar_s_free(b), lane);
+        if (b) ++uses1; else ++uses0;
         if (j >= n_full) {
           const int k0 = j * kBN;
 #pragma unroll
@@ -335,9 +353,9 @@ __global__ void __launch_bounds__(kFp8RowsThreads, 2)
       };
       // ---------------------------------------------- pass 1: exact maxima
       float m_raw = -INFINITY;
-      for (int j = 0; j < T.nb && ok; ++j, ++g) {
+      for (int j = 0; j < T.nb && ok; ++j) {
         uint32_t u[kBN];
-        if (!(ok = load_s(j, u))) break;
+        if (!(ok = load_s(j, j & 1, u))) break;
         const float* const s = reinterpret_cast<const float*>(u);
         float m8[8];  // eight independent 16-wide chains
 #pragma unroll
@@ -360,9 +378,9 @@ __global__ void __launch_bounds__(kFp8RowsThreads, 2)
       const uint64_t nm2 = pack2(-mref, -mref);
       // --------------------------- pass 2: 448 p = 2^(x − m'), P8 = E4M3(448 p)
       float l_run = 0.f;  // Σ 448 p over the row (unrounded)
-      for (int j = 0; j < T.nb && ok; ++j, ++g, ++gp) {
+      for (int j = 0; j < T.nb && ok; ++j, ++gp) {
         uint32_t u[kBN];
-        if (!(ok = load_s(j, u))) break;
+        if (!(ok = load_s(j, 0, u))) break;
         const float* const s = reinterpret_cast<const float*>(u);
         uint64_t acc[4] = {0, 0, 0, 0};
         uint32_t p8[kBN / 4];
@@ -432,6 +450,9 @@ __global__ void __launch_bounds__(kFp8RowsThreads, 2)
           *reinterpret_cast<uint4*>(stage + r * 128 + ((chunk ^ (r & 7)) << 4)) = wv;
         }
       }
+      // O has been read: its columns may take the next tile's pass-1 S.
+      tc_fence_before();
+      warp_arrive(bar_o_free, lane);
       fence_proxy_async_smem();
       warp_arrive(bar_stage_full, lane);  // the store warp writes the tile out
       if (q_row < p.Sq)
