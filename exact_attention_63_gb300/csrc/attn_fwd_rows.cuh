@@ -22,7 +22,7 @@
 //    buffer's reader) has completed.
 //
 // Warp roles (256 threads):
-//   warp 0     loader (one thread): K/V ring of 4 slots in consumption order
+//   warp 0     loader (one thread): K/V ring of 3 slots in consumption order
 //              K_0, K_1, then V_g, K_{g+2} per block g; allocates TMEM
 //   warp 1     P·V issuer (one thread): O += P(j) · V_j, P from TMEM
 //   warp 2     S issuer (one thread): S = Q · K_jᵀ
@@ -52,7 +52,7 @@ namespace attn {
 struct RowsLayout {
   static constexpr int D = 64;
   static constexpr uint32_t kTileBytes = kBM * 128;  // 128 rows × 64 bf16: one 128-byte-swizzled slab
-  static constexpr int kStages = 4;                   // K/V ring slots
+  static constexpr int kStages = 3;                   // K/V ring slots
   static constexpr int kLook = 2;                     // K runs this many blocks ahead of V in the ring order
   static constexpr uint32_t kQOff = 0;                // two Q buffers (also the output staging)
   static constexpr uint32_t kRingOff = 2 * kTileBytes;
