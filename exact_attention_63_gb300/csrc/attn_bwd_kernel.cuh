@@ -83,9 +83,9 @@ struct BwdLayout {
   static constexpr uint32_t kXOff = 0;                       // X, X2
   static constexpr uint32_t kRingOff = 2 * kTileBytes;
   static constexpr uint32_t kBarOff = kRingOff + kStages * kSlotBytes;
-  // barriers: fix_full, ring_full[S], ring_empty[S], s_full, dp_full, p_full[2], ds_full[2],
+  // barriers: fix_full, ring_full[S], ring_empty[S], s_full, dp_full, p_full[2], ds_full[2][2],
   //           acc_a, acc_b, done, dq_done[2]
-  static constexpr int kNumBars = 1 + 2 * kStages + 11;
+  static constexpr int kNumBars = 1 + 2 * kStages + 13;
   static constexpr uint32_t kMiscOff = kBarOff + 8 * kNumBars;
   static constexpr uint32_t kSmemBytes = kMiscOff + 16 + 1024;
 };
@@ -113,13 +113,19 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   // DKV: P of a half stored over S; DQ: S of a half read (its columns are free)
   auto bar_p_full = [&](int hh) { return bar_b0 + 8u * (2 + hh); };
   // dS of a half stored (so dP of the half has been read)
-  auto bar_ds_full = [&](int hh) { return bar_b0 + 8u * (4 + hh); };
-  const uint32_t bar_acc_a = bar_b0 + 8u * 6;    // DKV: dV of the block done (S's columns are free)
-  const uint32_t bar_acc_b = bar_b0 + 8u * 7;    // DKV: dK of the block done (dP's columns are free)
-  const uint32_t bar_done = bar_b0 + 8u * 8;     // every MMA done
+  // dS of half hh of block n stored (so dP of the half has been read):
+  // barrier (hh, n & 1), phase n >> 1.  Two waiters (the S/dP issuer in DQ,
+  // the accumulation issuer in both passes) and one barrier per block parity:
+  // dS(n+2) is stored only after dQ(n) (DQ: the dS buffer) or dK(n+1) (DKV:
+  // dP(n+2) waits for it), so neither waiter can fall two phases behind.
+  auto bar_ds_full = [&](int hh, int n) { return bar_b0 + 8u * (4 + 2 * hh + (n & 1)); };
+  auto ds_par = [](int n) { return static_cast<uint32_t>(n >> 1) & 1u; };
+  const uint32_t bar_acc_a = bar_b0 + 8u * 8;    // DKV: dV of the block done (S's columns are free)
+  const uint32_t bar_acc_b = bar_b0 + 8u * 9;    // DKV: dK of the block done (dP's columns are free)
+  const uint32_t bar_done = bar_b0 + 8u * 10;    // every MMA done
   // DQ: dQ of the blocks using dS buffer i done (that buffer is free); one
   // barrier per buffer, so each is waited on one phase at a time
-  auto bar_dq_done = [&](int i) { return bar_b0 + 8u * (9 + i); };
+  auto bar_dq_done = [&](int i) { return bar_b0 + 8u * (11 + i); };
   uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMiscOff);
   volatile uint32_t* const abort_flag = reinterpret_cast<volatile uint32_t*>(smem + L::kMiscOff + 4);
 
@@ -168,7 +174,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     mbar_init(bar_dp_full, 1);
     for (int hh = 0; hh < 2; ++hh) {
       mbar_init(bar_p_full(hh), 4);  // one arrival per warp of the half's warpgroup
-      mbar_init(bar_ds_full(hh), 4);
+      mbar_init(bar_ds_full(hh, 0), 4);
+      mbar_init(bar_ds_full(hh, 1), 4);
     }
     mbar_init(bar_acc_a, 1);
     mbar_init(bar_acc_b, 1);
@@ -282,7 +289,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             tc_fence_after();
             product(n + 1, 0);
             for (int hh = 0; hh < 2 && ok; ++hh)
-              if (!wait_bar(bar_ds_full(hh), n & 1, wc)) ok = false;
+              if (!wait_bar(bar_ds_full(hh, n), ds_par(n), wc)) ok = false;
             if (!ok) break;
             tc_fence_after();
             product(n + 1, 1);
@@ -305,7 +312,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             mma_commit(bar_acc_a);
             // dK += dSᵀ Q.
             for (int hh = 0; hh < 2 && ok; ++hh) {
-              if (!wait_bar(bar_ds_full(hh), n & 1, wc)) { ok = false; break; }
+              if (!wait_bar(bar_ds_full(hh, n), ds_par(n), wc)) { ok = false; break; }
               tc_fence_after();
               acc_half(n, hh, tAcc1, tdP + 64 * hh, 0);
             }
@@ -314,7 +321,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           } else {
             // dQ += dS K as the warpgroups store dS.
             for (int hh = 0; hh < 2 && ok; ++hh) {
-              if (!wait_bar(bar_ds_full(hh), n & 1, wc)) { ok = false; break; }
+              if (!wait_bar(bar_ds_full(hh, n), ds_par(n), wc)) { ok = false; break; }
               tc_fence_after();
               acc_half(n, hh, tAcc0, tDS(n) + 32 * hh, 0);
             }
@@ -445,7 +452,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar_ds_full(hh));
+      if (lane == 0) mbar_arrive(bar_ds_full(hh, n));
     }
     // ------------------------------------------------------------ outputs
     // The tile's outputs leave by TMA store (rows beyond the tensor are
