@@ -330,6 +330,42 @@ __device__ __forceinline__ int next_running(int idx, int stride, const FwdParams
   return idx;
 }
 
+// Packed sequences without a causal mask (p.B <= kSeqTableCap): the prefix
+// table of the sequences' q-tile counts × H, tab[s] for s in [0, B] (tab[B] =
+// all tiles that hold rows), built in shared memory by every thread of the
+// CTA — each sums its share of the sequences, then one scan over the lanes and
+// one over the warps (warp_sums: one int per warp).  Contains __syncthreads:
+// every thread of the CTA calls it.  Returns tab[B].
+__device__ __forceinline__ int build_seq_table(const FwdParams& p, int* tab, int* warp_sums) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int n = p.B, nth = static_cast<int>(blockDim.x), tid = static_cast<int>(threadIdx.x);
+  const int per = (n + nth - 1) / nth, s0 = min(n, tid * per), s1 = min(n, s0 + per);
+  auto q_tiles = [&](int sq) {  // clamped as in tile_info; at most the n_qt tiles max_seqlen_q covers
+    const int qa = min(max(p.cu_q[sq], 0), p.total_q), qz = min(max(p.cu_q[sq + 1], qa), p.total_q);
+    return min((qz - qa + kBM - 1) / kBM, p.n_qt);
+  };
+  int mine = 0;
+  for (int sq = s0; sq < s1; ++sq) mine += q_tiles(sq);
+  int incl = mine;  // inclusive scan over the warp, then over the warps
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) warp_sums[warp] = incl;
+  __syncthreads();
+  int before = 0;
+  for (int w = 0; w < warp; ++w) before += warp_sums[w];
+  int run = before + incl - mine;
+  for (int sq = s0; sq < s1; ++sq) {
+    tab[sq] = run * p.H;
+    run += q_tiles(sq);
+  }
+  if (tid == nth - 1) tab[n] = (before + incl) * p.H;
+  __syncthreads();
+  return tab[n];
+}
+
 // POLY: bit c selects the FMA-pipe polynomial exp2 for 16-column chunk c of
 // every 128-key block (compile time, so the exp loop is one basic block).
 // COUNT: compile the diagnostic counters (only launched when requested).
@@ -417,34 +453,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   if constexpr (VARLEN && !CAUSAL) {
     if (p.B <= kSeqTableCap) {
       int* const tab = reinterpret_cast<int*>(smem + L::kTableOff);
-      int* const warp_sums = reinterpret_cast<int*>(smem + L::kStatsOff);  // unused until the first exchange
-      const int n = p.B, nth = static_cast<int>(blockDim.x), tid = static_cast<int>(threadIdx.x);
-      const int per = (n + nth - 1) / nth, s0 = min(n, tid * per), s1 = min(n, s0 + per);
-      auto q_tiles = [&](int sq) {  // clamped as in tile_info; at most the n_qt tiles max_seqlen_q covers
-        const int qa = min(max(p.cu_q[sq], 0), p.total_q), qz = min(max(p.cu_q[sq + 1], qa), p.total_q);
-        return min((qz - qa + kBM - 1) / kBM, p.n_qt);
-      };
-      int mine = 0;
-      for (int sq = s0; sq < s1; ++sq) mine += q_tiles(sq);
-      int incl = mine;  // inclusive scan over the warp, then over the warps
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += y;
-      }
-      if (lane == 31) warp_sums[warp] = incl;
-      __syncthreads();
-      int before = 0;
-      for (int w = 0; w < warp; ++w) before += warp_sums[w];
-      int run = before + incl - mine;
-      for (int sq = s0; sq < s1; ++sq) {
-        tab[sq] = run * p.H;
-        run += q_tiles(sq);
-      }
-      if (tid == nth - 1) tab[n] = (before + incl) * p.H;
-      __syncthreads();
+      n_tiles = build_seq_table(p, tab, reinterpret_cast<int*>(smem + L::kStatsOff));  // stats unused until later
       seq_tab = tab;
-      n_tiles = tab[n];
     }
   }
 

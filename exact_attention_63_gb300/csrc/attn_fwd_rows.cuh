@@ -61,6 +61,10 @@ struct RowsLayout {
   static constexpr int kNumBars = 2 + 2 * kStages + 5 + 2 + 2;
   static constexpr uint32_t kMiscOff = kBarOff + 8 * kNumBars;  // tmem base (4 B) + abort flag (4 B)
   static constexpr uint32_t kSmemBytes = kMiscOff + 16 + 1024;  // + slack to align the base to 1024
+  // Packed sequences without a causal mask: the sequence tile table and its
+  // scratch (one int per warp) after the words, in extra shared memory.
+  static constexpr uint32_t kTableOff = kMiscOff + 16;
+  static constexpr uint32_t kSmemBytesTable = kSmemBytes + kSeqTableBytes + 64;
   static constexpr uint32_t kTmemCols = 256;
   static constexpr uint32_t kColS = 0, kColP = 128, kColO = 192;
 };
@@ -74,13 +78,15 @@ static_assert(kRowsThreads / 2 * (kRowsRoleRegs + kRowsSoftmaxRegs) == kRowsThre
 
 // POLY: bit c selects the FMA-pipe polynomial exp2 for 16-key chunk c of
 // every 128-key block (compile time, so the exp loop is one basic block).
-template <bool CAUSAL, bool COUNT, uint32_t POLY>
+// VARLEN: sequences of different lengths packed along the rows, as in
+// attn_fwd_kernel (a sequence's last tile written row by row, rows that see
+// no key set to O = 0, LSE = −inf).
+template <bool CAUSAL, bool COUNT, uint32_t POLY, bool VARLEN>
 __global__ void __launch_bounds__(kRowsThreads, 2)
     attn_fwd_rows_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                          const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
                          const FwdParams p) {
   using L = RowsLayout;
-  constexpr bool VARLEN = false;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -143,8 +149,15 @@ __global__ void __launch_bounds__(kRowsThreads, 2)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const WaitCtx wc{abort_flag, p.status, p.timeout_ns};
-  const int n_tiles = p.n_tiles;
-  const int* const seq_tab = nullptr;
+  int n_tiles = p.n_tiles;
+  const int* seq_tab = nullptr;
+  if constexpr (VARLEN && !CAUSAL) {  // the tiles that hold rows, in order (every thread takes part)
+    if (p.B <= kSeqTableCap) {
+      int* const tab = reinterpret_cast<int*>(smem + L::kTableOff);
+      n_tiles = build_seq_table(p, tab, tab + kSeqTableCap + 1);
+      seq_tab = tab;
+    }
+  }
 
   if (warp < 4) {
   // Role warpgroup: give registers back, then one role per warp.
@@ -215,9 +228,13 @@ __global__ void __launch_bounds__(kRowsThreads, 2)
            idx = next_running<CAUSAL, VARLEN>(idx + stride, stride, p, T, n_tiles, seq_tab), ++tc) {
         const int qb = tc & 1;
         if (!wait_bar(bar_stage_full(qb), (tc >> 1) & 1, wc)) break;
-        tma_store_4d(&tm_o, sQ + qb * L::kTileBytes, 0, T.h, qrow_of<VARLEN>(T), bcoord_of<VARLEN>(T));
-        tma_store_commit();
-        tma_store_wait_read0();
+        // A packed sequence's last tile is written by the softmax threads
+        // (its rows beyond the sequence belong to the next one).
+        if (!VARLEN || T.q0 + kBM <= len_q_of<VARLEN>(T, p)) {
+          tma_store_4d(&tm_o, sQ + qb * L::kTileBytes, 0, T.h, qrow_of<VARLEN>(T), bcoord_of<VARLEN>(T));
+          tma_store_commit();
+          tma_store_wait_read0();
+        }
         if (q_idx < n_tiles) load_q();  // tile tc + 2, into buffer qb
       }
       const uint64_t t0 = globaltimer_ns();
@@ -308,9 +325,28 @@ __global__ void __launch_bounds__(kRowsThreads, 2)
     bool ok = true;
     int g = 0, tc = 0;
     bool s_ready = false;  // S(g) known complete (tested at the end of block g − 1)
+    // O row of this thread in tile T (element offset), for the rows the
+    // softmax threads write directly.
+    auto o_row = [&](const Tile& T) -> uint16_t* {
+      return static_cast<uint16_t*>(p.o) + bcoord_of<VARLEN>(T) * p.o_sb +
+             static_cast<long long>(qrow_of<VARLEN>(T) + r) * p.o_ss + T.h * p.o_sh;
+    };
     for (int idx = blockIdx.x; idx < n_tiles && ok; idx += stride) {
       const Tile T = tile_info<CAUSAL, VARLEN>(idx, p, seq_tab);
       const int q_row = T.q0 + r;
+      if constexpr (VARLEN) {
+        if (!runs<VARLEN>(T)) {
+          // A tile beyond its sequence has nothing to write; rows of a tile
+          // that sees no key get O = 0 and LSE = −inf.
+          if (T.q0 < T.len_q && q_row < T.len_q) {
+            uint4* const dst = reinterpret_cast<uint4*>(o_row(T));
+#pragma unroll
+            for (int c = 0; c < L::D / 8; ++c) dst[c] = make_uint4(0u, 0u, 0u, 0u);
+            p.lse[T.lse0 + r] = -INFINITY;
+          }
+          continue;
+        }
+      }
       float m_run = -INFINITY;  // running reference maximum (log2 domain)
       float l_run = 0.f;        // running row sum (fp32, unrounded p)
       auto block = [&](int j, auto mask_tag) -> bool {
@@ -452,6 +488,11 @@ __global__ void __launch_bounds__(kRowsThreads, 2)
       const float inv = (l_run > 0.f) ? 1.f / l_run : 0.f;
       const int qb = tc & 1;
       uint8_t* const stage = smem + L::kQOff + qb * L::kTileBytes;
+      // A packed sequence's last tile: each thread writes its own row (rows
+      // beyond the sequence belong to the next one); else staged for the TMA
+      // store.
+      const bool direct = VARLEN && T.q0 + kBM > len_q_of<VARLEN>(T, p);
+      uint16_t* const orow = o_row(T);
       uint32_t x[2][32];
       tmem_ld32(tO, x[0]);
       tmem_ld32(tO + 32, x[1]);
@@ -469,12 +510,15 @@ __global__ void __launch_bounds__(kRowsThreads, 2)
           wv.z = pack_bf16x2(__uint_as_float(o8[4]) * inv, __uint_as_float(o8[5]) * inv);
           wv.w = pack_bf16x2(__uint_as_float(o8[6]) * inv, __uint_as_float(o8[7]) * inv);
           const int chunk = 4 * c + q16;  // 16-byte chunk of the 128-byte row
-          *reinterpret_cast<uint4*>(stage + r * 128 + ((chunk ^ (r & 7)) << 4)) = wv;
+          if (!direct)
+            *reinterpret_cast<uint4*>(stage + r * 128 + ((chunk ^ (r & 7)) << 4)) = wv;
+          else if (q_row < len_q_of<VARLEN>(T, p))
+            *reinterpret_cast<uint4*>(orow + 8 * chunk) = wv;
         }
       }
       fence_proxy_async_smem();
       warp_arrive(bar_stage_full(qb), lane);  // the store warp writes the tile out
-      if (q_row < p.Sq) {
+      if (q_row < len_q_of<VARLEN>(T, p)) {
         const float lse = (l_run > 0.f) ? (m_run + __log2f(l_run)) * 0.69314718055994531f : -INFINITY;
         p.lse[lse0_of<VARLEN>(T, p) + r] = lse;
       }

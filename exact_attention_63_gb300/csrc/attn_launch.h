@@ -84,19 +84,19 @@ cudaError_t launch_poly(const LaunchArgs& a) {
 // the kernel being compiled to exactly kRowsLaunchRegs registers; a build
 // where it is not runs the two-warpgroup kernel instead (cudaErrorNotSupported
 // tells the caller to).
-template <bool CAUSAL, bool COUNT, uint32_t POLY>
+template <bool CAUSAL, bool COUNT, uint32_t POLY, bool VARLEN = false>
 cudaError_t launch_rows_one(const LaunchArgs& a) {
-  constexpr unsigned int smem = RowsLayout::kSmemBytes;
+  constexpr unsigned int smem = (VARLEN && !CAUSAL) ? RowsLayout::kSmemBytesTable : RowsLayout::kSmemBytes;
   static volatile int state[64] = {};  // per device: 0 not checked, 1 usable, -1 not usable
   if (a.device < 0 || a.device >= 64) return cudaErrorInvalidDevice;
   if (state[a.device] == 0) {
     cudaFuncAttributes fa;
-    cudaError_t e = cudaFuncGetAttributes(&fa, attn_fwd_rows_kernel<CAUSAL, COUNT, POLY>);
+    cudaError_t e = cudaFuncGetAttributes(&fa, attn_fwd_rows_kernel<CAUSAL, COUNT, POLY, VARLEN>);
     if (e != cudaSuccess) return e;
     if (fa.numRegs != kRowsLaunchRegs) {
       state[a.device] = -1;
     } else {
-      e = cudaFuncSetAttribute(attn_fwd_rows_kernel<CAUSAL, COUNT, POLY>,
+      e = cudaFuncSetAttribute(attn_fwd_rows_kernel<CAUSAL, COUNT, POLY, VARLEN>,
                                cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
       if (e != cudaSuccess) return e;
       state[a.device] = 1;
@@ -104,7 +104,7 @@ cudaError_t launch_rows_one(const LaunchArgs& a) {
   }
   if (state[a.device] < 0) return cudaErrorNotSupported;
   const int grid = a.p.n_tiles < 2 * a.sms ? a.p.n_tiles : 2 * a.sms;
-  attn_fwd_rows_kernel<CAUSAL, COUNT, POLY><<<grid, kRowsThreads, smem, a.stream>>>(a.q, a.k, a.v, a.o, a.p);
+  attn_fwd_rows_kernel<CAUSAL, COUNT, POLY, VARLEN><<<grid, kRowsThreads, smem, a.stream>>>(a.q, a.k, a.v, a.o, a.p);
   return cudaGetLastError();
 }
 
@@ -127,6 +127,11 @@ template <int D, bool CAUSAL>
 cudaError_t launch_variant(const LaunchArgs& a) {
   if (a.p.cu_q != nullptr) {
     if (a.poly != 0x00u) return cudaErrorInvalidValue;
+    if constexpr (D == 64) {  // the full-row kernel
+      const cudaError_t e = a.p.counters != nullptr ? launch_rows_one<CAUSAL, true, 0x00u, true>(a)
+                                                    : launch_rows_one<CAUSAL, false, 0x00u, true>(a);
+      if (e != cudaErrorNotSupported) return e;
+    }
     return a.p.counters != nullptr ? launch_one<D, CAUSAL, 0x00u, true, true>(a)
                                    : launch_one<D, CAUSAL, 0x00u, false, true>(a);
   }
