@@ -84,8 +84,11 @@ struct BwdLayout {
   static constexpr uint32_t kRingOff = 2 * kTileBytes;
   static constexpr uint32_t kBarOff = kRingOff + kStages * kSlotBytes;
   // barriers: fix_full, ring_full[S], ring_empty[S], s_full, dp_full, p_full[2], ds_full[2][2],
-  //           acc_a, acc_b, done, dq_done[2]
-  static constexpr int kNumBars = 1 + 2 * kStages + 13;
+  //           acc_a, acc_b, done, dq_done[2], s_full_1, acc_a_1, p_full_1[2]
+  static constexpr int kNumBars = 1 + 2 * kStages + 17;
+  // The dK/dV pass at d = 64 leaves TMEM columns [384, 512) free: S gets a
+  // second buffer there, so S(n+1) does not wait for dV(n).
+  static constexpr bool kDblS = (MODE == kModeDKV && D == 64);
   static constexpr uint32_t kMiscOff = kBarOff + 8 * kNumBars;
   static constexpr uint32_t kSmemBytes = kMiscOff + 16 + 1024;
 };
@@ -108,10 +111,18 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   auto bar_ring_full = [&](int s) { return bars + 8u * (1 + s); };
   auto bar_ring_empty = [&](int s) { return bars + 8u * (1 + L::kStages + s); };
   const uint32_t bar_b0 = bars + 8u * (1 + 2 * L::kStages);
-  const uint32_t bar_s_full = bar_b0;            // S of the block written
+  // S of block n written, and (DKV) dV(n) done (its S buffer is free): with
+  // two S buffers, one barrier of each per buffer (phase n >> 1), so that
+  // neither runs two phases ahead of its waiter; else one (phase n).
+  auto bar_s_full = [&](int n) { return (L::kDblS && (n & 1)) ? bar_b0 + 8u * 13 : bar_b0; };
+  auto s_par = [](int n) { return static_cast<uint32_t>(L::kDblS ? (n >> 1) : n) & 1u; };
   const uint32_t bar_dp_full = bar_b0 + 8u;      // dP of the block written
   // DKV: P of a half stored over S; DQ: S of a half read (its columns are free)
-  auto bar_p_full = [&](int hh) { return bar_b0 + 8u * (2 + hh); };
+  // (with two S buffers: one barrier per half and block parity, phase n >> 1;
+  // P(n+2) needs S(n+2), which waits for dV(n), the first waiter's work)
+  auto bar_p_full = [&](int hh, int n) {
+    return (L::kDblS && (n & 1)) ? bar_b0 + 8u * (15 + hh) : bar_b0 + 8u * (2 + hh);
+  };
   // dS of a half stored (so dP of the half has been read)
   // dS of half hh of block n stored (so dP of the half has been read):
   // barrier (hh, n & 1), phase n >> 1.  Two waiters (the S/dP issuer in DQ,
@@ -120,7 +131,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   // dP(n+2) waits for it), so neither waiter can fall two phases behind.
   auto bar_ds_full = [&](int hh, int n) { return bar_b0 + 8u * (4 + 2 * hh + (n & 1)); };
   auto ds_par = [](int n) { return static_cast<uint32_t>(n >> 1) & 1u; };
-  const uint32_t bar_acc_a = bar_b0 + 8u * 8;    // DKV: dV of the block done (S's columns are free)
+  auto bar_acc_a = [&](int n) { return (L::kDblS && (n & 1)) ? bar_b0 + 8u * 14 : bar_b0 + 8u * 8; };
   const uint32_t bar_acc_b = bar_b0 + 8u * 9;    // DKV: dK of the block done (dP's columns are free)
   const uint32_t bar_done = bar_b0 + 8u * 10;    // every MMA done
   // DQ: dQ of the blocks using dS buffer i done (that buffer is free); one
@@ -170,14 +181,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       mbar_init(bar_ring_full(s), 1);
       mbar_init(bar_ring_empty(s), 1);
     }
-    mbar_init(bar_s_full, 1);
+    mbar_init(bar_s_full(0), 1);
+    mbar_init(bar_s_full(1), 1);
     mbar_init(bar_dp_full, 1);
     for (int hh = 0; hh < 2; ++hh) {
-      mbar_init(bar_p_full(hh), 4);  // one arrival per warp of the half's warpgroup
+      mbar_init(bar_p_full(hh, 0), 4);  // one arrival per warp of the half's warpgroup
+      mbar_init(bar_p_full(hh, 1), 4);
       mbar_init(bar_ds_full(hh, 0), 4);
       mbar_init(bar_ds_full(hh, 1), 4);
     }
-    mbar_init(bar_acc_a, 1);
+    mbar_init(bar_acc_a(0), 1);
+    mbar_init(bar_acc_a(1), 1);
     mbar_init(bar_acc_b, 1);
     mbar_init(bar_done, 2);  // one commit per issuing thread
     for (int i = 0; i < 2; ++i) mbar_init(bar_dq_done(i), 1);
@@ -188,7 +202,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const WaitCtx wc{abort_flag, p.status, p.timeout_ns};
-  const uint32_t tS = tmem, tdP = tmem + 128, tAcc0 = tmem + 256, tAcc1 = tmem + 256 + D;
+  const uint32_t tdP = tmem + 128, tAcc0 = tmem + 256, tAcc1 = tmem + 256 + D;
+  auto tS = [&](int n) { return tmem + ((L::kDblS && (n & 1)) ? 384u : 0u); };  // S (and P) of block n
   // dQ pass: dS gets columns of its own (where dK sits in the other pass), two
   // buffers of 64, so neither the next block's dP nor its dS waits for the
   // previous dQ += dS K.
@@ -240,13 +255,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       auto product = [&](int n, int which) {
         const uint32_t sT = sRing + (n % L::kStages) * L::kSlotBytes + which * L::kTileBytes;
         const uint64_t dT = sdesc_kmajor_sw128(sT), dXx = which ? dX2 : dX;
-        const uint32_t tD = which ? tdP : tS;
+        const uint32_t tD = which ? tdP : tS(n);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = ((kk / 4) * L::kSlabBytes + (kk % 4) * 32) >> 4;
           mma_ss(tD, dXx + off, dT + off, idS, kk > 0 ? 1u : 0u);
         }
-        mma_commit(which ? bar_dp_full : bar_s_full);
+        mma_commit(which ? bar_dp_full : bar_s_full(n));
       };
       // One half of an accumulation: acc (+)= T[:, 64hh : 64hh+64] · M[64hh : 64hh+64, :]
       // with T packed bf16 in TMEM at tT and M an MN-major tile of block n's slot.
@@ -273,7 +288,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           if (MODE == kModeDKV) {
             // S(n+1) overwrites P(n): it goes in once dV(n) has completed;
             // dP(n+1) overwrites dS(n) once dK(n) has.
-            if (!wait_bar(bar_acc_a, n & 1, wc)) { ok = false; break; }
+            if (L::kDblS) {  // S(n+1)'s buffer was last read by dV(n − 1)
+              if (n >= 1 && !wait_bar(bar_acc_a(n - 1), s_par(n - 1), wc)) { ok = false; break; }
+            } else if (!wait_bar(bar_acc_a(n), s_par(n), wc)) {
+              ok = false;
+              break;
+            }
             tc_fence_after();
             product(n + 1, 0);
             if (!wait_bar(bar_acc_b, n & 1, wc)) { ok = false; break; }
@@ -284,7 +304,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             // soon as they have stored dS(n) (so read dP(n); dS has columns
             // of its own).
             for (int hh = 0; hh < 2 && ok; ++hh)
-              if (!wait_bar(bar_p_full(hh), n & 1, wc)) ok = false;
+              if (!wait_bar(bar_p_full(hh, n), s_par(n), wc)) ok = false;
             if (!ok) break;
             tc_fence_after();
             product(n + 1, 0);
@@ -304,12 +324,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           if (MODE == kModeDKV) {
             // dV += Pᵀ dO, half by half as the warpgroups store P.
             for (int hh = 0; hh < 2 && ok; ++hh) {
-              if (!wait_bar(bar_p_full(hh), n & 1, wc)) { ok = false; break; }
+              if (!wait_bar(bar_p_full(hh, n), s_par(n), wc)) { ok = false; break; }
               tc_fence_after();
-              acc_half(n, hh, tAcc0, tS + 64 * hh, 1);
+              acc_half(n, hh, tAcc0, tS(n) + 64 * hh, 1);
             }
             if (!ok) break;
-            mma_commit(bar_acc_a);
+            mma_commit(bar_acc_a(n));
             // dK += dSᵀ Q.
             for (int hh = 0; hh < 2 && ok; ++hh) {
               if (!wait_bar(bar_ds_full(hh, n), ds_par(n), wc)) { ok = false; break; }
@@ -370,15 +390,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       }
       // ---- P = exp2(S·scale·log2 e − LSE₂) over this half's 64 columns
       {
-        const bool got = wait_bar(bar_s_full, n & 1, wc);
+        const bool got = wait_bar(bar_s_full(n), s_par(n), wc);
         if (__any_sync(0xffffffffu, !got)) { ok = false; break; }
       }
       tc_fence_after();
       float pv[64];
       {
         uint32_t us[64];
-        tmem_ld32(tS + 64 * hh + lane_off, *reinterpret_cast<uint32_t(*)[32]>(&us[0]));
-        tmem_ld32(tS + 64 * hh + 32 + lane_off, *reinterpret_cast<uint32_t(*)[32]>(&us[32]));
+        tmem_ld32(tS(n) + 64 * hh + lane_off, *reinterpret_cast<uint32_t(*)[32]>(&us[0]));
+        tmem_ld32(tS(n) + 64 * hh + 32 + lane_off, *reinterpret_cast<uint32_t(*)[32]>(&us[32]));
         tmem_wait_ld();
         reg_fence32(*reinterpret_cast<uint32_t(*)[32]>(&us[0]));
         reg_fence32(*reinterpret_cast<uint32_t(*)[32]>(&us[32]));
@@ -386,7 +406,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           // S has been read: its columns may take the next block's S.
           tc_fence_before();
           __syncwarp();
-          if (lane == 0) mbar_arrive(bar_p_full(hh));
+          if (lane == 0) mbar_arrive(bar_p_full(hh, n));
         }
 #pragma unroll
         for (int e = 0; e < 64; ++e) {
@@ -408,11 +428,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         uint32_t pk[32];
 #pragma unroll
         for (int e = 0; e < 32; ++e) pk[e] = pack_bf16x2(pv[2 * e], pv[2 * e + 1]);
-        tmem_st32(tS + 64 * hh + lane_off, pk);
+        tmem_st32(tS(n) + 64 * hh + lane_off, pk);
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar_p_full(hh));
+        if (lane == 0) mbar_arrive(bar_p_full(hh, n));
       }
       // ---- dS = P ∘ (dP − D)
       {
