@@ -50,7 +50,9 @@
 //        dP(n+1) follows as soon as dS(n) — and so the read of dP(n) — is in.
 //
 // TMEM columns: S [0, 128), dP [128, 256), acc0 [256, 256+D) (dQ or dV),
-// acc1 [256+D, 256+2D) (dK; in the dQ pass two 64-column dS buffers).  P (bf16 pairs)
+// acc1 [256+D, 256+2D) (dK; in the dQ pass two 64-column dS buffers), and in
+// the dK/dV pass at d = 64 a second S buffer [384, 512) (S(n+1) then waits for
+// dV(n−1), not dV(n)).  P (bf16 pairs)
 // overwrites S's columns and, in DKV, dS overwrites dP's, in the packed layout
 // the forward uses for P.
 #pragma once
