@@ -207,16 +207,19 @@ def cpu_oracle_rate(w, budget_s: float, start_chunk: int = 0):
 
 def host_link_bound(h2d_bytes, d2h_bytes, kernel_ms, flops, dev, stream, reps=5):
     """The roofline of the host-buffer call: one pinned host->device copy of a
-    step's upload bytes and one device->host copy of its download bytes (one
-    cudaMemcpyAsync each, timed with CUDA events, best of ``reps``).  With
-    uploads, downloads and the kernel fully overlapped, a step takes at least
-    the longest of the three, which bounds the end-to-end throughput."""
+    step's upload bytes, one device->host copy of its download bytes (one
+    cudaMemcpyAsync each), and the two issued together on two streams, timed
+    with CUDA events, best of ``reps``.  With uploads, downloads and the kernel
+    fully overlapped, a step takes at least the longest of the single copies,
+    the concurrent pair (the link may share its bandwidth between the two
+    directions) and the kernel, which bounds the end-to-end throughput."""
     import torch
 
     up_h = torch.empty(h2d_bytes, dtype=torch.uint8).pin_memory()
     up_d = torch.empty(h2d_bytes, dtype=torch.uint8, device=dev)
     dn_d = torch.empty(d2h_bytes, dtype=torch.uint8, device=dev)
     dn_h = torch.empty(d2h_bytes, dtype=torch.uint8).pin_memory()
+    side = torch.cuda.Stream(device=dev)
 
     def best(fn):
         t = []
@@ -229,12 +232,26 @@ def host_link_bound(h2d_bytes, d2h_bytes, kernel_ms, flops, dev, stream, reps=5)
             t.append(a.elapsed_time(b))
         return min(t)
 
-    t_up = best(lambda: up_d.copy_(up_h, non_blocking=True))
-    t_dn = best(lambda: dn_h.copy_(dn_d, non_blocking=True))
-    t_min = max(t_up, t_dn, kernel_ms)
+    def both():
+        go, done = torch.cuda.Event(), torch.cuda.Event()
+        go.record(stream)
+        side.wait_event(go)
+        with torch.cuda.stream(stream):
+            up_d.copy_(up_h, non_blocking=True)
+        with torch.cuda.stream(side):
+            dn_h.copy_(dn_d, non_blocking=True)
+        done.record(side)
+        stream.wait_event(done)
+
+    with torch.cuda.stream(stream):
+        t_up = best(lambda: up_d.copy_(up_h, non_blocking=True))
+        t_dn = best(lambda: dn_h.copy_(dn_d, non_blocking=True))
+    t_both = best(both)
+    t_min = max(t_up, t_dn, t_both, kernel_ms)
     return {"link_h2d_gbs": h2d_bytes / (t_up * 1e-3) / 1e9, "link_d2h_gbs": d2h_bytes / (t_dn * 1e-3) / 1e9,
+            "link_both_gbs": (h2d_bytes + d2h_bytes) / (t_both * 1e-3) / 1e9,
             "bound_tflops": flops / (t_min * 1e-3) / 1e12,
-            "bound": "max(one pinned upload copy, one pinned download copy, the kernel) per step"}
+            "bound": "max(one pinned upload copy, one pinned download copy, the two together, the kernel) per step"}
 
 
 def run_reference(args, w, rank, world):
