@@ -27,7 +27,8 @@ ERRORS = {
 # Every symbol the header declares (checked by the CPU test-suite).
 EXPORTS = ["attn_fwd", "attn_fwd_ex", "attn_fwd_host", "attn_fwd_host_workspace_size", "attn_get_status",
            "attn_strerror", "attn_last_cuda_error", "attn_version", "attn_fwd_host_static", "attn_fwd_layout",
-           "attn_fwd_varlen", "attn_bwd", "attn_bwd_workspace_size", "attn_bwd_layout", "attn_fwd_fp8"]
+           "attn_fwd_varlen", "attn_bwd", "attn_bwd_workspace_size", "attn_bwd_layout", "attn_fwd_fp8",
+           "attn_fwd_fp8_ex"]
 
 CAUSAL_ALIGN = {"top-left": 0, "bottom-right": 1}
 
@@ -101,6 +102,8 @@ def lib():
     L.attn_fwd_host_static.restype = i
     L.attn_fwd_fp8.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, f, f, f, i, vp]
     L.attn_fwd_fp8.restype = i
+    L.attn_fwd_fp8_ex.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, f, f, f, i, ctypes.POINTER(Options), vp]
+    L.attn_fwd_fp8_ex.restype = i
     L.attn_get_status.argtypes = [vp]
     L.attn_get_status.restype = i
     L.attn_strerror.argtypes = [i]
@@ -285,6 +288,7 @@ def attn_bwd(q, k, v, o, lse, dout, causal: bool = False, scale: float | None = 
 
 
 TEST_WITHHOLD_KV = 1
+TEST_FALLBACK_KERNEL = 2
 
 
 def make_options(rescale_threshold: float = 0.0, poly_exp2_mask: int = 0, counters=None, timeout_ms: int = 0,
@@ -332,10 +336,12 @@ def attn_fwd_host_static(q_h, k_h, v_h, o_h, lse_h, causal: bool, scale: float, 
 
 
 def attn_fwd_fp8(q8, k8, v8, descale_q: float, descale_k: float, descale_v: float, causal: bool = False,
-                 scale: float | None = None, out=None, lse=None, stream=None):
+                 scale: float | None = None, out=None, lse=None, stream=None, options=None):
     """Exact attention forward on FP8 (E4M3) inputs: q8 [B,Sq,H,128], k8, v8
     [B,Sk,H,128] as torch.float8_e4m3fn (or their raw bytes as uint8), standing
-    for descale_x · x8.  Returns (o [B,Sq,H,128] bf16, lse [B,H,Sq] fp32)."""
+    for descale_x · x8.  Returns (o [B,Sq,H,128] bf16, lse [B,H,Sq] fp32).
+    ``options`` (from make_options; timeout_ms and test_flags only) selects
+    attn_fwd_fp8_ex."""
     for name, t in (("q8", q8), ("k8", k8), ("v8", v8)):
         if t.dtype not in (torch.float8_e4m3fn, torch.uint8) or not t.is_cuda or t.dim() != 4 or \
                 not t.is_contiguous():
@@ -355,9 +361,12 @@ def attn_fwd_fp8(q8, k8, v8, descale_q: float, descale_k: float, descale_v: floa
     if lse.shape != (B, H, Sq) or lse.dtype != torch.float32 or not lse.is_contiguous():
         raise ValueError("lse must be a contiguous fp32 tensor of shape (B, H, Sq)")
     with torch.cuda.device(q8.device):
-        rc = lib().attn_fwd_fp8(q8.data_ptr(), k8.data_ptr(), v8.data_ptr(), out.data_ptr(), lse.data_ptr(),
-                                B, H, Sq, Sk, d, float(scale), float(descale_q), float(descale_k), float(descale_v),
-                                int(bool(causal)), _stream_handle(stream))
+        args = (q8.data_ptr(), k8.data_ptr(), v8.data_ptr(), out.data_ptr(), lse.data_ptr(), B, H, Sq, Sk, d,
+                float(scale), float(descale_q), float(descale_k), float(descale_v), int(bool(causal)))
+        if options is None:
+            rc = lib().attn_fwd_fp8(*args, _stream_handle(stream))
+        else:
+            rc = lib().attn_fwd_fp8_ex(*args, ctypes.byref(options), _stream_handle(stream))
     _check(rc)
     return out, lse
 

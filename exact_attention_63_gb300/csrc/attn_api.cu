@@ -214,7 +214,7 @@ int parse_options(const attn_options* opts, int d, Opts* out) {
     if (opts->counters != nullptr && (reinterpret_cast<uintptr_t>(opts->counters) & 7u) != 0) return ATTN_ERR_ALIGN;
     r.counters = opts->counters;
     if (opts->timeout_ms != 0) r.timeout_ms = opts->timeout_ms;
-    if ((opts->test_flags & ~ATTN_TEST_WITHHOLD_KV) != 0) return ATTN_ERR_OPTION;
+    if ((opts->test_flags & ~(ATTN_TEST_WITHHOLD_KV | ATTN_TEST_FALLBACK_KERNEL)) != 0) return ATTN_ERR_OPTION;
     r.test_flags = opts->test_flags;
   }
   *out = r;
@@ -602,6 +602,13 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
 int attn_fwd_fp8(const void* q8, const void* k8, const void* v8, void* o, float* lse, int B, int H, int Sq, int Sk,
                  int d, float scale, float descale_q, float descale_k, float descale_v, int causal,
                  cudaStream_t stream) {
+  return attn_fwd_fp8_ex(q8, k8, v8, o, lse, B, H, Sq, Sk, d, scale, descale_q, descale_k, descale_v, causal,
+                         nullptr, stream);
+}
+
+int attn_fwd_fp8_ex(const void* q8, const void* k8, const void* v8, void* o, float* lse, int B, int H, int Sq,
+                    int Sk, int d, float scale, float descale_q, float descale_k, float descale_v, int causal,
+                    const attn_options* opts, cudaStream_t stream) {
   if (q8 == nullptr || k8 == nullptr || v8 == nullptr || o == nullptr || lse == nullptr) return ATTN_ERR_NULL;
   if (B < 1 || H < 1 || Sq < 1 || Sk < 1) return ATTN_ERR_SHAPE;
   const long long n_qt = (static_cast<long long>(Sq) + 127) / 128;
@@ -613,8 +620,13 @@ int attn_fwd_fp8(const void* q8, const void* k8, const void* v8, void* o, float*
   const float sl = scale * descale_q * descale_k * 1.4426950408889634f;
   if (!std::isfinite(sl) || !(sl > 0.f)) return ATTN_ERR_SCALE;
   if (!aligned16(q8) || !aligned16(k8) || !aligned16(v8) || !aligned16(o) || !aligned16(lse)) return ATTN_ERR_ALIGN;
+  Opts op;
+  int rc = parse_options(opts, d, &op);
+  if (rc != ATTN_OK) return rc;
+  if (opts != nullptr && (opts->rescale_threshold != 0.f || opts->poly_exp2_mask != 0u || opts->counters != nullptr))
+    return ATTN_ERR_OPTION;
   int dev = -1;
-  int rc = current_device(&dev);
+  rc = current_device(&dev);
   if (rc != ATTN_OK) return rc;
   attn::LaunchArgs a;
   std::memset(&a, 0, sizeof(a));
@@ -641,7 +653,8 @@ int attn_fwd_fp8(const void* q8, const void* k8, const void* v8, void* o, float*
   a.p.status = g_dev[dev].status;
   a.p.scale_log2 = sl;
   a.p.o_scale = descale_v / 448.0f;
-  a.p.timeout_ns = static_cast<uint64_t>(kDefaultTimeoutMs) * 1000000ull;
+  a.p.timeout_ns = static_cast<uint64_t>(op.timeout_ms) * 1000000ull;
+  a.p.test_flags = op.test_flags;
   a.grid = a.p.n_tiles < g_dev[dev].sms ? a.p.n_tiles : g_dev[dev].sms;
   a.sms = g_dev[dev].sms;
   a.device = dev;

@@ -47,8 +47,10 @@ static cudaError_t launch_fp8_rows_one(const LaunchArgs& a) {
 }
 
 cudaError_t launch_fwd_fp8(const LaunchArgs& a, bool causal) {
-  const cudaError_t e = causal ? launch_fp8_rows_one<true>(a) : launch_fp8_rows_one<false>(a);
-  if (e != cudaErrorNotSupported) return e;
+  if (!(a.p.test_flags & ATTN_TEST_FALLBACK_KERNEL)) {
+    const cudaError_t e = causal ? launch_fp8_rows_one<true>(a) : launch_fp8_rows_one<false>(a);
+    if (e != cudaErrorNotSupported) return e;
+  }
   return causal ? launch_fp8_one<true>(a) : launch_fp8_one<false>(a);
 }
 

@@ -9,6 +9,7 @@
 
 #include "attn_fwd_kernel.cuh"
 #include "attn_fwd_rows.cuh"
+#include "attn_gb300.h"
 
 namespace attn {
 
@@ -127,7 +128,7 @@ template <int D, bool CAUSAL>
 cudaError_t launch_variant(const LaunchArgs& a) {
   if (a.p.cu_q != nullptr) {
     if (a.poly != 0x00u) return cudaErrorInvalidValue;
-    if constexpr (D == 64) {  // the full-row kernel
+    if (D == 64 && !(a.p.test_flags & ATTN_TEST_FALLBACK_KERNEL)) {  // the full-row kernel
       const cudaError_t e = a.p.counters != nullptr ? launch_rows_one<CAUSAL, true, 0x00u, true>(a)
                                                     : launch_rows_one<CAUSAL, false, 0x00u, true>(a);
       if (e != cudaErrorNotSupported) return e;
@@ -135,7 +136,7 @@ cudaError_t launch_variant(const LaunchArgs& a) {
     return a.p.counters != nullptr ? launch_one<D, CAUSAL, 0x00u, true, true>(a)
                                    : launch_one<D, CAUSAL, 0x00u, false, true>(a);
   }
-  if constexpr (D == 64) {  // dense tensors: the full-row kernel
+  if (D == 64 && !(a.p.test_flags & ATTN_TEST_FALLBACK_KERNEL)) {  // dense tensors: the full-row kernel
     const cudaError_t e = a.p.counters != nullptr ? launch_rows<CAUSAL, true>(a) : launch_rows<CAUSAL, false>(a);
     if (e != cudaErrorNotSupported) return e;
   }

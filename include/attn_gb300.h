@@ -106,10 +106,10 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
  * counters — optional device pointer to 2 zero-initialised uint64 values; when
  *   non-NULL the kernel adds the number of rescales to counters[0] and the
  *   number of (row, block) softmax updates to counters[1].  A rescale is
- *   counted per row, key block and running maximum: at d = 128 (and for
- *   packed sequences or a polynomial exp2 split at d = 64) each 128-key block
- *   is processed as two 64-key halves with running maxima of their own; the
- *   other d = 64 calls keep one running maximum per row.
+ *   counted per row, key block and running maximum: at d = 128 each 128-key
+ *   block is processed as two 64-key halves with running maxima of their own;
+ *   at d = 64 a row keeps one running maximum (two halves under
+ *   ATTN_TEST_FALLBACK_KERNEL).
  * timeout_ms — time limit of every pipeline wait inside the kernel (default
  *   4000 ms); on expiry the kernel stops, leaves outputs invalid and flags
  *   ATTN_ERR_TIMEOUT for attn_get_status().  The limit is measured in wall
@@ -117,13 +117,19 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
  *   time spent while this context is switched out counts too, so a very long
  *   call on a heavily shared GPU can report ATTN_ERR_TIMEOUT without any
  *   fault; raise the limit there.
- * test_flags — for testing the wait limits only; 0 in normal use.
+ * test_flags — for tests only; 0 in normal use.
  *   ATTN_TEST_WITHHOLD_KV: the loader never issues the K/V copies, so the
  *   MMA issuer's first wait cannot complete and must run into timeout_ms; the
  *   kernel then stops cleanly (no fault, TMEM released) and attn_get_status()
  *   returns ATTN_ERR_TIMEOUT.  Outputs are not written.
+ *   ATTN_TEST_FALLBACK_KERNEL: at d = 64 (bf16) and for FP8 inputs, run the
+ *   kernel that serves when the full-row kernel (two CTAs per SM) is not
+ *   compiled to the register count its register split needs — the
+ *   two-warpgroup kernel of d = 128, or the one-CTA FP8 kernel — so that this
+ *   fallback can be tested.  Same results within the tolerances.
  */
 #define ATTN_TEST_WITHHOLD_KV 1u
+#define ATTN_TEST_FALLBACK_KERNEL 2u
 typedef struct attn_options {
   size_t struct_size;
   float rescale_threshold;
@@ -351,6 +357,15 @@ int attn_fwd_fp8(const void* q8, const void* k8, const void* v8, void* o, float*
                  int B, int H, int Sq, int Sk, int d, float scale,
                  float descale_q, float descale_k, float descale_v, int causal,
                  cudaStream_t stream);
+
+/* attn_fwd_fp8 with options (opts may be NULL: same as attn_fwd_fp8).  Only
+ * timeout_ms and test_flags apply; rescale_threshold, poly_exp2_mask and
+ * counters must be zero (ATTN_ERR_OPTION otherwise): there is no rescaling,
+ * the maximum being exact, and every exponential is on the MUFU unit. */
+int attn_fwd_fp8_ex(const void* q8, const void* k8, const void* v8, void* o, float* lse,
+                    int B, int H, int Sq, int Sk, int d, float scale,
+                    float descale_q, float descale_k, float descale_v, int causal,
+                    const attn_options* opts, cudaStream_t stream);
 
 /*
  * attn_get_status — synchronises `stream`, then returns and clears the current

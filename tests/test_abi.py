@@ -193,3 +193,13 @@ def test_static_workspace_size_matches_header():
 ])
 def test_fp8_rejects_bad_arguments_before_launch(L, args, expect):
     assert L.attn_fwd_fp8(*args, None) == expect
+
+
+def test_fp8_ex_rejects_options_that_do_not_apply(L):
+    """attn_fwd_fp8_ex takes timeout_ms and test_flags only; everything else,
+    and unknown test flags, are ATTN_ERR_OPTION before any device call."""
+    args = (A, A, A, A, A, 1, 1, 8, 8, 128, 0.1, 1.0, 1.0, 1.0, 0)
+    for kw in ({"rescale_threshold": 8.0}, {"poly_exp2_mask": 0x11}, {"test_flags": 4}):
+        opts = attn.make_options(**kw)
+        assert L.attn_fwd_fp8_ex(*args, ctypes.byref(opts), None) == -9, kw
+    assert attn.TEST_FALLBACK_KERNEL == 2

@@ -94,6 +94,21 @@ def test_fp8_small_all_elements(w):
 
 
 @pytest.mark.gpu
+@pytest.mark.parametrize("w", SMALL, ids=lambda w: w.name)
+def test_fp8_fallback_kernel_small_all_elements(w):
+    """The one-CTA FP8 kernel, which serves when the full-row kernel is not
+    compiled to its register split (ATTN_TEST_FALLBACK_KERNEL): the same bound."""
+    need_gpu()
+    q8, k8, v8, dq, dk, dv = inputs.make_fp8_inputs(w)
+    opts = attn.make_options(test_flags=attn.TEST_FALLBACK_KERNEL)
+    o, lse = attn.attn_fwd_fp8(q8.cuda(), k8.cuda(), v8.cuda(), dq, dk, dv, causal=w.causal, scale=w.scale,
+                               options=opts)
+    torch.cuda.synchronize()
+    assert attn.get_status() == 0
+    _check(w, o, lse, q8, k8, v8, dq, dk, dv)
+
+
+@pytest.mark.gpu
 @pytest.mark.parametrize("idx,heads,row_ranges", [
     (2, [(0, 0), (3, 15), (1, 7)], None),
     (3, [(0, 0), (1, 15)], None),

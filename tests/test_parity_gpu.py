@@ -54,6 +54,20 @@ def test_small_all_elements(w):
     assert_close(o, lse, O_ref, L_ref, w.name)
 
 
+FALLBACK_D64 = [w for w in SMALL if w.d == 64] + [inputs.custom(1, 4, 1024, 1024, 64, False, sigma_qk=3.0, seed=44)]
+
+
+@pytest.mark.parametrize("w", FALLBACK_D64, ids=lambda w: w.name)
+def test_d64_fallback_kernel_all_elements(w):
+    """d = 64 through the kernel that serves when the full-row kernel is not
+    compiled to its register split (ATTN_TEST_FALLBACK_KERNEL): the same bar."""
+    need_gpu()
+    q, k, v = inputs.make_inputs(w)
+    o, lse = run(w, q, k, v, options=attn.make_options(test_flags=attn.TEST_FALLBACK_KERNEL))
+    O_ref, L_ref = oracle.attention_forward(q, k, v, w.scale, w.causal)
+    assert_close(o, lse, O_ref, L_ref, w.name + " (fallback kernel)")
+
+
 @pytest.mark.parametrize("idx", [2, 3, 4, 5])
 def test_full_size_sampled_rows(idx):
     """The five workloads at full size, in the bench's launch configuration;

@@ -32,12 +32,12 @@ CASES = [
 ]
 
 
-def run_case(lens_q, lens_k, H, H_kv, d, causal, align, seed, sigma=1.0):
+def run_case(lens_q, lens_k, H, H_kv, d, causal, align, seed, sigma=1.0, options=None):
     lens_k = lens_q if lens_k is None else lens_k
     q, k, v, cu_q, cu_k = inputs.make_varlen_inputs(lens_q, lens_k, H, H_kv, d, seed, sigma_qk=sigma)
     dev = torch.device("cuda:0")
     o, lse = attn.attn_fwd_varlen(q.to(dev), k.to(dev), v.to(dev), cu_q.to(dev), cu_k.to(dev),
-                                  max(max(lens_q), 1), causal=causal, causal_align=align)
+                                  max(max(lens_q), 1), causal=causal, causal_align=align, options=options)
     torch.cuda.synchronize()
     assert attn.get_status() == 0
     O_ref, L_ref = oracle.attention_varlen(q, k, v, cu_q.numpy(), cu_k.numpy(), 1.0 / np.sqrt(d), causal,
@@ -63,6 +63,17 @@ def test_varlen_cases(case):
     name, lens_q, lens_k, H, H_kv, d, causal, align, seed = case
     o, lse, O_ref, L_ref = run_case(lens_q, lens_k, H, H_kv, d, causal, align, seed)
     check(o, lse, O_ref, L_ref, name)
+
+
+@pytest.mark.parametrize("case", [c for c in CASES if c[5] == 64 and len(c[1]) <= 300], ids=lambda c: c[0])
+def test_varlen_d64_fallback_kernel(case):
+    """Packed sequences at d = 64 through the full-row kernel's fallback
+    (ATTN_TEST_FALLBACK_KERNEL): the same results."""
+    need_gpu()
+    name, lens_q, lens_k, H, H_kv, d, causal, align, seed = case
+    opts = attn.make_options(test_flags=attn.TEST_FALLBACK_KERNEL)
+    o, lse, O_ref, L_ref = run_case(lens_q, lens_k, H, H_kv, d, causal, align, seed, options=opts)
+    check(o, lse, O_ref, L_ref, name + " (fallback kernel)")
 
 
 def test_varlen_peaky_logits():
