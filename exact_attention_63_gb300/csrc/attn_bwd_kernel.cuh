@@ -27,7 +27,7 @@
 // Warp roles (352 threads): warps 0-7 turn S, dP into P, dS (warpgroup h owns
 // columns [64h, 64h+64) of each block; one thread per row) and write the
 // tile's outputs; warp 8 loads X, X2 once and streams (A, B) blocks — plus, in
-// DKV, the 128 log2-LSE and D values of the block's queries — through a ring;
+// DKV, the 128 −log2-LSE and D values of the block's queries — through a ring;
 // warp 9 issues S and dP, warp 10 the accumulations.  One thread issues at
 // most one tcgen05.mma every ~45 cycles (more beside busy warps): a block is
 // 24 (d = 64) to 32 (d = 128) MMAs, about as long as the tensor core's own
@@ -80,7 +80,7 @@ struct BwdLayout {
   static constexpr uint32_t kSlabBytes = 128 * 128;
   static constexpr uint32_t kTileBytes = kSlabBytes * kSlabs;
   static constexpr int kStages = (D == 128) ? 2 : 3;
-  static constexpr uint32_t kVecBytes = (MODE == kModeDKV) ? 2 * 128 * 4 : 0;  // log2-LSE and D of 128 queries
+  static constexpr uint32_t kVecBytes = (MODE == kModeDKV) ? 2 * 128 * 4 : 0;  // −log2-LSE and D of 128 queries
   static constexpr uint32_t kSlotBytes = 2 * kTileBytes + ((kVecBytes + 1023) / 1024) * 1024;
   static constexpr uint32_t kXOff = 0;                       // X, X2
   static constexpr uint32_t kRingOff = 2 * kTileBytes;
@@ -366,19 +366,24 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const int r = threadIdx.x & 127;   // row of the tile = TMEM lane
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const int row = r0 + r;            // DQ: query; DKV: key
-    float lse2_row = 0.f, d_row = 0.f;
+    // The workspace holds −LSE·log2 e (nl) and D per query; the dQ pass needs
+    // its own row's, the dK/dV pass each block's 128 (from the ring slot).
+    uint64_t nl_row2 = 0, d_row2 = 0;
     if (MODE == kModeDQ) {
-      lse2_row = p.lse2[static_cast<size_t>(bh) * p.pitch + row];  // row < n_rt·128 = pitch
-      d_row = p.dvec[static_cast<size_t>(bh) * p.pitch + row];
+      const float nl = p.lse2[static_cast<size_t>(bh) * p.pitch + row];  // row < n_rt·128 = pitch
+      const float dr = p.dvec[static_cast<size_t>(bh) * p.pitch + row];
+      nl_row2 = pack2(nl, nl);
+      d_row2 = pack2(dr, dr);
     }
-    const float sc = p.scale_log2;
+    const uint64_t sc2 = pack2(p.scale_log2, p.scale_log2);
+    const uint64_t zero2 = 0;
     bool ok = true;
     for (int n = 0; n < nblk && ok; ++n) {
       const int c0 = col0_of(n);
       const float* vec = reinterpret_cast<const float*>(smem + L::kRingOff + (n % L::kStages) * L::kSlotBytes +
                                                         2 * L::kTileBytes);
       if (MODE == kModeDKV) {
-        // The block's log2-LSE and D arrived with its ring slot (which stays
+        // The block's −log2-LSE and D arrived with its ring slot (which stays
         // loaded until this block's dS has been consumed).
         const bool in = wait_bar(bar_ring_full(n % L::kStages), (n / L::kStages) & 1, wc);
         if (__any_sync(0xffffffffu, !in)) { ok = false; break; }
@@ -411,18 +416,25 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           if (lane == 0) mbar_arrive(bar_p_full(hh, n));
         }
 #pragma unroll
-        for (int e = 0; e < 64; ++e) {
-          const float lse = (MODE == kModeDQ) ? lse2_row : vec[64 * hh + e];
-          float pe = ex2_mufu(__uint_as_float(us[e]) * sc - lse);
+        for (int e = 0; e < 64; e += 2) {  // pairs: x = s·scale·log2 e − LSE₂ (packed fp32)
+          const uint64_t nl2 =
+              (MODE == kModeDQ) ? nl_row2 : *reinterpret_cast<const uint64_t*>(vec + 64 * hh + e);
+          float x0, x1;
+          unpack2(ffma2(pack2(__uint_as_float(us[e]), __uint_as_float(us[e + 1])), sc2, nl2), x0, x1);
+          float pe[2] = {ex2_mufu(x0), ex2_mufu(x1)};
           if (edge) {
-            const int ce = c0 + 64 * hh + e;  // global column: DQ key, DKV query
-            if (MODE == kModeDQ) {
-              if (ce >= p.Sk || (CAUSAL && ce > row + p.coff)) pe = 0.f;
-            } else {
-              if (CAUSAL && row > ce + p.coff) pe = 0.f;
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+              const int ce = c0 + 64 * hh + e + i;  // global column: DQ key, DKV query
+              if (MODE == kModeDQ) {
+                if (ce >= p.Sk || (CAUSAL && ce > row + p.coff)) pe[i] = 0.f;
+              } else {
+                if (CAUSAL && row > ce + p.coff) pe[i] = 0.f;
+              }
             }
           }
-          pv[e] = pe;
+          pv[e] = pe[0];
+          pv[e + 1] = pe[1];
         }
       }
       if (MODE == kModeDKV) {
@@ -451,10 +463,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         reg_fence32(*reinterpret_cast<uint32_t(*)[32]>(&ud[0]));
         reg_fence32(*reinterpret_cast<uint32_t(*)[32]>(&ud[32]));
 #pragma unroll
-        for (int e = 0; e < 64; e += 2) {
-          const float da = (MODE == kModeDQ) ? d_row : vec[128 + 64 * hh + e];
-          const float db = (MODE == kModeDQ) ? d_row : vec[128 + 64 * hh + e + 1];
-          qk[e / 2] = pack_bf16x2(pv[e] * (__uint_as_float(ud[e]) - da), pv[e + 1] * (__uint_as_float(ud[e + 1]) - db));
+        for (int e = 0; e < 64; e += 2) {  // pairs: P·(dP − D) (packed fp32)
+          const uint64_t d2 =
+              (MODE == kModeDQ) ? d_row2 : *reinterpret_cast<const uint64_t*>(vec + 128 + 64 * hh + e);
+          const uint64_t diff = fsub2(pack2(__uint_as_float(ud[e]), __uint_as_float(ud[e + 1])), d2);
+          float a, b2;
+          unpack2(ffma2(pack2(pv[e], pv[e + 1]), diff, zero2), a, b2);
+          qk[e / 2] = pack_bf16x2(a, b2);
         }
       }
       uint32_t tdst;
@@ -555,9 +570,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   }
 }
 
-// D = rowsum(dO ∘ O) and LSE · log2(e) per query row, in [B·H, pitch] arrays
-// padded to whole 128-row blocks (+inf and 0 beyond Sq, so padded queries get
-// P = 0).  One warp per (batch, head, row): its lanes read the row's D
+// D = rowsum(dO ∘ O) and −LSE · log2(e) per query row, in [B·H, pitch]
+// arrays padded to whole 128-row blocks (−inf and 0 beyond Sq, so padded
+// queries get P = 0; negated so that the gradient warps form
+// s·scale·log2 e − LSE₂ with one packed FMA per pair).  One warp per (batch, head, row): its lanes read the row's D
 // elements of O and dO as consecutive 4- or 8-byte pieces (coalesced) and the
 // products are summed with shuffles.
 template <int D>
@@ -572,7 +588,7 @@ __global__ void attn_bwd_prep_kernel(const uint16_t* o, const uint16_t* dout, co
     const long long bh = t / pitch;
     if (i >= Sq) {
       if (lane == 0) {
-        lse2[t] = INFINITY;
+        lse2[t] = -INFINITY;
         dvec[t] = 0.f;
       }
       continue;
@@ -597,7 +613,7 @@ __global__ void attn_bwd_prep_kernel(const uint16_t* o, const uint16_t* dout, co
     for (int m = 16; m > 0; m >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, m);
     if (lane == 0) {
       dvec[t] = acc;
-      lse2[t] = lse[(static_cast<size_t>(b) * H + h) * Sq + i] * 1.4426950408889634f;
+      lse2[t] = lse[(static_cast<size_t>(b) * H + h) * Sq + i] * -1.4426950408889634f;
     }
   }
 }

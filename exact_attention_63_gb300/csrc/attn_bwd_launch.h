@@ -10,7 +10,7 @@
 namespace attn {
 
 struct BwdParams {
-  const float* lse2;   // [B·H, pitch]: LSE · log2(e) of each query row; +inf beyond Sq
+  const float* lse2;   // [B·H, pitch]: −LSE · log2(e) of each query row; −inf beyond Sq
   const float* dvec;   // [B·H, pitch]: D = rowsum(dO ∘ O); 0 beyond Sq
   unsigned int* status;
   int B, H, Sq, Sk, pitch;
