@@ -415,10 +415,21 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           __syncwarp();
           if (lane == 0) mbar_arrive(bar_p_full(hh, n));
         }
+        uint64_t nlv[32];  // −LSE₂ pairs of this half's columns (dK/dV: 16-byte loads from the slot)
+#pragma unroll
+        for (int e = 0; e < 32; e += 2) {
+          if (MODE == kModeDQ) {
+            nlv[e] = nl_row2;
+            nlv[e + 1] = nl_row2;
+          } else {
+            const uint4 w = *reinterpret_cast<const uint4*>(vec + 64 * hh + 2 * e);
+            nlv[e] = (static_cast<uint64_t>(w.y) << 32) | w.x;
+            nlv[e + 1] = (static_cast<uint64_t>(w.w) << 32) | w.z;
+          }
+        }
 #pragma unroll
         for (int e = 0; e < 64; e += 2) {  // pairs: x = s·scale·log2 e − LSE₂ (packed fp32)
-          const uint64_t nl2 =
-              (MODE == kModeDQ) ? nl_row2 : *reinterpret_cast<const uint64_t*>(vec + 64 * hh + e);
+          const uint64_t nl2 = nlv[e / 2];
           float x0, x1;
           unpack2(ffma2(pack2(__uint_as_float(us[e]), __uint_as_float(us[e + 1])), sc2, nl2), x0, x1);
           float pe[2] = {ex2_mufu(x0), ex2_mufu(x1)};
@@ -464,8 +475,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         reg_fence32(*reinterpret_cast<uint32_t(*)[32]>(&ud[32]));
 #pragma unroll
         for (int e = 0; e < 64; e += 2) {  // pairs: P·(dP − D) (packed fp32)
-          const uint64_t d2 =
-              (MODE == kModeDQ) ? d_row2 : *reinterpret_cast<const uint64_t*>(vec + 128 + 64 * hh + e);
+          uint64_t d2 = d_row2;
+          if (MODE == kModeDKV) {
+            const uint4 w = *reinterpret_cast<const uint4*>(vec + 128 + 64 * hh + (e & ~3));
+            d2 = (e & 2) ? ((static_cast<uint64_t>(w.w) << 32) | w.z) : ((static_cast<uint64_t>(w.y) << 32) | w.x);
+          }
           const uint64_t diff = fsub2(pack2(__uint_as_float(ud[e]), __uint_as_float(ud[e + 1])), d2);
           float a, b2;
           unpack2(ffma2(pack2(pv[e], pv[e + 1]), diff, zero2), a, b2);
