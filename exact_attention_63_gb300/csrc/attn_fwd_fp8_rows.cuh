@@ -355,6 +355,25 @@ __global__ void __launch_bounds__(kFp8RowsThreads, 2)
       float m_raw = -INFINITY;
       for (int j = 0; j < T.nb && ok; ++j) {
         uint32_t u[kBN];
+        if (j < n_full) {
+          // No key of the block is masked: the reducing TMEM load gives each
+          // 32 columns' maximum with the values.
+          const int b = j & 1;
+          const bool got = wait_bar_cold(bar_s_full(b), (b ? uses1 : uses0) & 1, wc);
+          if (__any_sync(0xffffffffu, !got)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t tS = tmem + (b == 0 ? L::kColS : L::kColO) + lane_off;
+          float mc[4];
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+            tmem_ld32_max(tS + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(&u[32 * c]), mc[c]);
+          tmem_wait_ld();
+          tc_fence_before();
+          warp_arrive(bar_s_free(b), lane);
+          if (b) ++uses1; else ++uses0;
+          m_raw = fmax3(m_raw, fmax3(mc[0], mc[1], mc[2]), mc[3]);
+          continue;
+        }
         if (!(ok = load_s(j, j & 1, u))) break;
         const float* const s = reinterpret_cast<const float*>(u);
         float m8[8];  // eight independent 16-wide chains
