@@ -20,7 +20,9 @@
 //    softmax has loaded it: S(g+1) runs while the softmax is still on block g.
 //  * Pass 1 does not touch O, so its S blocks alternate between S's columns
 //    and O's (once the previous tile's epilogue has read O): S(j+1) of pass 1
-//    is computed while the softmax still loads S(j).
+//    is computed while the softmax still loads S(j).  A block with no masked
+//    key takes its row maximum from the reducing TMEM load (tcgen05.ld.red,
+//    the maximum of each 32 columns loaded), not from 64 max instructions.
 //  * The factor 448 is folded into the exponent: with m' = m − log2 448,
 //    2^(x − m') = 448 p is what E4M3 rounds, the row sum is 448 L, and
 //    O = descale_v · (P8·V8) / (448 L), LSE = (m' + log2(448 L)) · ln 2.
