@@ -304,6 +304,8 @@ def main():
     ap.add_argument("--backward", action="store_true",
                     help="time the backward pass (dQ, dK, dV) instead; FLOPs counted as 2.5x the forward's "
                          "(the five products S, dP, dV, dK, dQ), halved when causal")
+    ap.add_argument("--deterministic", action="store_true",
+                    help="with --backward: the two-pass, bit-reproducible schedule instead of the one-pass default")
     ap.add_argument("--varlen", type=int, default=0,
                     help="packed-sequence variant: this many sequences with a seeded mix of lengths up to the "
                          "workload's S (same H, d, mask); FLOPs counted per sequence")
@@ -426,7 +428,7 @@ def main():
 
             def step():
                 attn.attn_bwd(qd, kd, vd, od, ld, gd, causal=w.causal, scale=w.scale, dq=dqd, dk=dkd, dv=dvd,
-                              workspace=wsd)
+                              workspace=wsd, deterministic=args.deterministic)
             args.no_e2e = True
 
     for _ in range(args.warmup):
@@ -530,7 +532,7 @@ def main():
         "vs_baseline": None,
         "dtype": "e4m3" if args.fp8 else "bf16",
         "data": "synthetic",
-        "config": {"workload": w.name + ("_backward" if args.backward else "") + ("_fp8" if args.fp8 else ""), "B": w.B, "H": w.H, "H_kv": w.kv_heads, "Sq": w.Sq, "Sk": w.Sk, "d": w.d,
+        "config": {"workload": w.name + ("_backward" if args.backward else "") + ("_two_pass" if args.deterministic else "") + ("_fp8" if args.fp8 else ""), "B": w.B, "H": w.H, "H_kv": w.kv_heads, "Sq": w.Sq, "Sk": w.Sk, "d": w.d,
                    "causal": w.causal, "causal_align": w.causal_align, "sigma_qk": w.sigma_qk, "seed": w.seed,
                    **({"varlen_lengths": lens} if lens is not None else {}),
                    "l2": "flushed between timed steps (256 MiB write)",

@@ -27,8 +27,8 @@ ERRORS = {
 # Every symbol the header declares (checked by the CPU test-suite).
 EXPORTS = ["attn_fwd", "attn_fwd_ex", "attn_fwd_host", "attn_fwd_host_workspace_size", "attn_get_status",
            "attn_strerror", "attn_last_cuda_error", "attn_version", "attn_fwd_host_static", "attn_fwd_layout",
-           "attn_fwd_varlen", "attn_bwd", "attn_bwd_workspace_size", "attn_bwd_layout", "attn_fwd_fp8",
-           "attn_fwd_fp8_ex"]
+           "attn_fwd_varlen", "attn_bwd", "attn_bwd_workspace_size", "attn_bwd_layout", "attn_bwd_ex",
+           "attn_fwd_fp8", "attn_fwd_fp8_ex"]
 
 CAUSAL_ALIGN = {"top-left": 0, "bottom-right": 1}
 
@@ -92,6 +92,9 @@ def lib():
     L.attn_bwd_layout.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, i, ctypes.POINTER(Layout), vp,
                                   sz, vp]
     L.attn_bwd_layout.restype = i
+    L.attn_bwd_ex.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, i, ctypes.POINTER(Layout),
+                              ctypes.c_uint, vp, sz, vp]
+    L.attn_bwd_ex.restype = i
     L.attn_bwd_workspace_size.argtypes = [i, i, i]
     L.attn_bwd_workspace_size.restype = sz
     L.attn_fwd_host.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp, sz, vp]
@@ -246,13 +249,19 @@ def attn_fwd_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int, caus
     return out, lse
 
 
+BWD_DETERMINISTIC = 1
+
+
 def attn_bwd(q, k, v, o, lse, dout, causal: bool = False, scale: float | None = None, dq=None, dk=None, dv=None,
-             workspace=None, stream=None, causal_align: str = "top-left"):
+             workspace=None, stream=None, causal_align: str = "top-left", deterministic: bool = False):
     """Gradients of attn_fwd's output: returns (dq, dk, dv), bf16, shaped
     like q, k, v.  o and lse are what attn_fwd returned for the same inputs;
     dout is the gradient of the loss with respect to o.  Dense (batch, seq,
     heads, head_dim) tensors; k and v may have fewer heads than q (grouped
-    query heads; a shared head's gradient sums its group's)."""
+    query heads; a shared head's gradient sums its group's).  At head dim 64
+    one pass computes all three by default (dq's fp32 sums run in a varying
+    order, so its last bits may change between runs); at 128, or with
+    deterministic=True, two passes, reproducible bit for bit."""
     for name, t in (("q", q), ("k", k), ("v", v), ("o", o), ("dout", dout)):
         if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous() or t.dim() != 4:
             raise ValueError(f"{name} must be a contiguous 4-D bf16 CUDA tensor (batch, seq, heads, head_dim)")
@@ -279,10 +288,11 @@ def attn_bwd(q, k, v, o, lse, dout, causal: bool = False, scale: float | None = 
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
     lay = make_layout(H_kv, CAUSAL_ALIGN[causal_align])
     with torch.cuda.device(q.device):
-        rc = L.attn_bwd_layout(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
-                               dout.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, Sq, Sk, d,
-                               float(scale), int(bool(causal)), ctypes.byref(lay), workspace.data_ptr(),
-                               workspace.numel() * workspace.element_size(), _stream_handle(stream))
+        rc = L.attn_bwd_ex(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                           dout.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, Sq, Sk, d,
+                           float(scale), int(bool(causal)), ctypes.byref(lay),
+                           BWD_DETERMINISTIC if deterministic else 0, workspace.data_ptr(),
+                           workspace.numel() * workspace.element_size(), _stream_handle(stream))
     _check(rc)
     return dq, dk, dv
 

@@ -664,17 +664,57 @@ int attn_fwd_fp8_ex(const void* q8, const void* k8, const void* v8, void* o, flo
   return ATTN_OK;
 }
 
+namespace {
+// Workspace: −LSE·log2 e and D per query row ([B·H, pitch] each), then the
+// fused pass's fp32 dQ accumulator [B·H, pitch, 128] (sized for d = 128).
+size_t bwd_vec_bytes(int B, int H, int Sq) {
+  const size_t pitch = (static_cast<size_t>(Sq) + 127) / 128 * 128;
+  return (2 * static_cast<size_t>(B) * H * pitch * 4 + 255) & ~static_cast<size_t>(255);
+}
+
+// 2-D map over the fp32 accumulator: d values per row, B·H·pitch rows; box
+// 32 values × 32 rows (one 128-byte swizzle row per row).
+int encode_dq_acc(CUtensorMap* m, float* acc, long long rows, int d) {
+  auto enc = get_encode_fn();
+  if (enc == nullptr) {
+    std::snprintf(t_last_error, sizeof(t_last_error), "cuTensorMapEncodeTiled unavailable");
+    return ATTN_ERR_LAUNCH;
+  }
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(d) * 4};
+  const cuuint32_t box[2] = {32, 32};
+  const cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, acc, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    std::snprintf(t_last_error, sizeof(t_last_error), "cuTensorMapEncodeTiled failed (CUresult %d)",
+                  static_cast<int>(r));
+    return ATTN_ERR_LAUNCH;
+  }
+  return ATTN_OK;
+}
+}  // namespace
+
 size_t attn_bwd_workspace_size(int B, int H, int Sq) {
   if (B < 1 || H < 1 || Sq < 1) return 0;
   const size_t pitch = (static_cast<size_t>(Sq) + 127) / 128 * 128;
-  return (2 * static_cast<size_t>(B) * H * pitch * 4 + 255) & ~static_cast<size_t>(255);
+  return bwd_vec_bytes(B, H, Sq) + static_cast<size_t>(B) * H * pitch * 128 * 4;
 }
 
 int attn_bwd_layout(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dout,
                     void* dq, void* dk, void* dv, int B, int H, int Sq, int Sk, int d, float scale, int causal,
                     const attn_layout* layout, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  return attn_bwd_ex(q, k, v, o, lse, dout, dq, dk, dv, B, H, Sq, Sk, d, scale, causal, layout, 0u, workspace,
+                     workspace_bytes, stream);
+}
+
+int attn_bwd_ex(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dout,
+                void* dq, void* dk, void* dv, int B, int H, int Sq, int Sk, int d, float scale, int causal,
+                const attn_layout* layout, unsigned int flags, void* workspace, size_t workspace_bytes,
+                cudaStream_t stream) {
   int rc = check_args(q, k, v, o, lse, B, H, Sq, Sk, d, scale);
   if (rc != ATTN_OK) return rc;
+  if ((flags & ~static_cast<unsigned int>(ATTN_BWD_DETERMINISTIC)) != 0) return ATTN_ERR_OPTION;
   int H_kv = H;
   bool bottom_right = false;
   if (layout != nullptr) {
@@ -702,7 +742,15 @@ int attn_bwd_layout(const void* q, const void* k, const void* v, const void* o, 
   const int pitch = (Sq + 127) / 128 * 128;
   float* lse2 = static_cast<float*>(workspace);
   float* dvec = lse2 + static_cast<size_t>(B) * H * pitch;
-  cudaError_t e = attn::launch_bwd_prep(o, dout, lse, lse2, dvec, B, H, Sq, pitch, d, stream);
+  // At d = 64 one pass (dQ added up in fp32 across key tiles, in an order
+  // that varies between runs) unless the caller asks for bit-reproducible
+  // gradients; at d = 128 the two passes (faster there: the one-pass
+  // kernel's dQ reduce-adds are bound by the L2's reduction rate).  The
+  // kernel addresses accumulator rows with 32-bit coordinates.
+  const long long acc_rows = static_cast<long long>(B) * H * pitch;
+  const bool fused = (flags & ATTN_BWD_DETERMINISTIC) == 0 && d == 64 && acc_rows <= 0x7FFFFFFFLL;
+  float* dq_acc = fused ? reinterpret_cast<float*>(static_cast<char*>(workspace) + bwd_vec_bytes(B, H, Sq)) : nullptr;
+  cudaError_t e = attn::launch_bwd_prep(o, dout, lse, lse2, dvec, dq_acc, B, H, Sq, pitch, d, stream);
   if (e != cudaSuccess) return fail_cuda(e, "backward preparation launch");
 
   const long long hd = static_cast<long long>(H) * d, kd = static_cast<long long>(H_kv) * d;
@@ -734,6 +782,15 @@ int attn_bwd_layout(const void* q, const void* k, const void* v, const void* o, 
   if ((rc = encode_bshd(&a.o1, dk, B, Sk, H_kv, d, ks)) != ATTN_OK) return rc;
   a.p.n_rt = static_cast<int>(n_kt);
   a.grid = static_cast<int>(n_kt * B * H_kv);
+  if (fused) {
+    if ((rc = encode_dq_acc(&a.dq, dq_acc, acc_rows, d)) != ATTN_OK) return rc;
+    a.mode = 2;
+    if ((e = attn::launch_bwd(a, d)) != cudaSuccess) return fail_cuda(e, "backward fused launch");
+    e = attn::launch_bwd_dq_convert(dq_acc, dq, B, H, Sq, pitch, d, scale, g_dev[dev].sms, stream);
+    if (e != cudaSuccess) return fail_cuda(e, "backward dQ conversion launch");
+    return ATTN_OK;
+  }
+  a.dq = a.o0;  // unused by the two-pass kernels
   a.mode = 1;
   if ((e = attn::launch_bwd(a, d)) != cudaSuccess) return fail_cuda(e, "backward dK/dV launch");
   // dQ: rows are queries; K and V stream past them.

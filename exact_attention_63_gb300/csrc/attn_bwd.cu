@@ -18,7 +18,8 @@ cudaError_t launch_bwd_one(const BwdLaunchArgs& a) {
     if (e != cudaSuccess) return e;
     configured[a.device] = true;
   }
-  attn_bwd_kernel<D, CAUSAL, MODE><<<a.grid, kBwdThreads, smem, a.stream>>>(a.x, a.x2, a.a, a.b, a.o0, a.o1, a.p);
+  attn_bwd_kernel<D, CAUSAL, MODE><<<a.grid, kBwdThreads, smem, a.stream>>>(a.x, a.x2, a.a, a.b, a.o0, a.o1, a.dq,
+                                                                             a.p);
   return cudaGetLastError();
 }
 
@@ -26,6 +27,15 @@ template <int D>
 cudaError_t launch_bwd_d(const BwdLaunchArgs& a) {
   if (a.mode == kModeDQ)
     return a.causal ? launch_bwd_one<D, true, kModeDQ>(a) : launch_bwd_one<D, false, kModeDQ>(a);
+  if (a.mode == kModeFused) {
+    // The one-pass kernel is built for d = 64 only: at d = 128 its dQ
+    // reduce-adds run into the L2's reduction rate and the two passes are
+    // faster.
+    if constexpr (D == 64)
+      return a.causal ? launch_bwd_one<D, true, kModeFused>(a) : launch_bwd_one<D, false, kModeFused>(a);
+    else
+      return cudaErrorInvalidValue;
+  }
   return a.causal ? launch_bwd_one<D, true, kModeDKV>(a) : launch_bwd_one<D, false, kModeDKV>(a);
 }
 
@@ -37,8 +47,8 @@ cudaError_t launch_bwd(const BwdLaunchArgs& a, int d) {
   return cudaErrorInvalidValue;
 }
 
-cudaError_t launch_bwd_prep(const void* o, const void* dout, const float* lse, float* lse2, float* dvec, int B, int H,
-                            int Sq, int pitch, int d, cudaStream_t stream) {
+cudaError_t launch_bwd_prep(const void* o, const void* dout, const float* lse, float* lse2, float* dvec, float* dq_acc,
+                            int B, int H, int Sq, int pitch, int d, cudaStream_t stream) {
   const long long n = static_cast<long long>(B) * H * pitch;  // rows, one warp each
   const int threads = 256;
   const long long want = n / (threads / 32) + 1;
@@ -46,9 +56,22 @@ cudaError_t launch_bwd_prep(const void* o, const void* dout, const float* lse, f
   const uint16_t* o16 = static_cast<const uint16_t*>(o);
   const uint16_t* g16 = static_cast<const uint16_t*>(dout);
   if (d == 64)
-    attn_bwd_prep_kernel<64><<<blocks, threads, 0, stream>>>(o16, g16, lse, lse2, dvec, B, H, Sq, pitch);
+    attn_bwd_prep_kernel<64><<<blocks, threads, 0, stream>>>(o16, g16, lse, lse2, dvec, dq_acc, B, H, Sq, pitch);
   else
-    attn_bwd_prep_kernel<128><<<blocks, threads, 0, stream>>>(o16, g16, lse, lse2, dvec, B, H, Sq, pitch);
+    attn_bwd_prep_kernel<128><<<blocks, threads, 0, stream>>>(o16, g16, lse, lse2, dvec, dq_acc, B, H, Sq, pitch);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_dq_convert(const float* dq_acc, void* dq, int B, int H, int Sq, int pitch, int d, float scale,
+                                  int sms, cudaStream_t stream) {
+  const long long n = static_cast<long long>(B) * Sq * H * (d / 8);
+  const int threads = 256;
+  const long long want = (n + threads - 1) / threads;
+  const long long cap = static_cast<long long>(sms > 0 ? sms : 152) * 8;
+  const int blocks = static_cast<int>(want < cap ? want : cap);
+  if (d != 64) return cudaErrorInvalidValue;  // the one-pass kernel's head dim
+  attn_bwd_dq_convert_kernel<64><<<blocks, threads, 0, stream>>>(dq_acc, static_cast<uint16_t*>(dq), B, H, Sq, pitch,
+                                                                  scale);
   return cudaGetLastError();
 }
 

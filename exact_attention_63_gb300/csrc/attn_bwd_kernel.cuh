@@ -19,10 +19,19 @@
 // With grouped key/value heads the dQ pass reads the K/V head of its query
 // head's group, and the dK/dV pass of a K/V head walks the query blocks of
 // every query head in its group (their contributions add up).
-// In both, S = X·Aᵀ and dP = X2·Bᵀ are K-major products like the forward's
+//   FUSED rows = keys, as DKV, and dQ in the same pass: dS goes to a
+//       shared-memory tile (not over dP), dK += dSᵀ Q reads it K-major and
+//       dQ(n) = dS K — the block's contribution to its 128 queries' dQ —
+//       reads it MN-major; the warps add dQ(n) into an fp32 accumulator in
+//       device memory by TMA reduce-add, and a last kernel rounds it to bf16.
+//       S and dP are then computed once per (query, key) pair instead of
+//       twice, at the price of an accumulation order that varies from run to
+//       run (fp32 additions of the key tiles' contributions).
+// In all, S = X·Aᵀ and dP = X2·Bᵀ are K-major products like the forward's
 // Q·Kᵀ, and every accumulation is TMEM operand × MN-major shared-memory
-// operand like the forward's P·V.  No atomics: dQ and dK/dV are separate
-// passes.
+// operand like the forward's P·V, except the fused pass's dK and dQ, whose
+// dS operand is in shared memory.  DQ and DKV use no atomics (separate
+// passes; bit-reproducible).
 //
 // Warp roles (352 threads): warps 0-7 turn S, dP into P, dS (warpgroup h owns
 // columns [64h, 64h+64) of each block; one thread per row) and write the
@@ -51,10 +60,12 @@
 //
 // TMEM columns: S [0, 128), dP [128, 256), acc0 [256, 256+D) (dQ or dV),
 // acc1 [256+D, 256+2D) (dK; in the dQ pass two 64-column dS buffers), and in
-// the dK/dV pass at d = 64 a second S buffer [384, 512) (S(n+1) then waits for
-// dV(n−1), not dV(n)).  P (bf16 pairs)
+// the dK/dV and fused passes at d = 64 a second S buffer [384, 512) (S(n+1)
+// then waits for dV(n−1), not dV(n)).  P (bf16 pairs)
 // overwrites S's columns and, in DKV, dS overwrites dP's, in the packed layout
-// the forward uses for P.
+// the forward uses for P.  The fused pass's dQ(n) goes to S(n)'s columns
+// [32, 96) at d = 64 (P's two halves are packed into [0, 32) and [96, 128)
+// there) and over dP at d = 128.
 #pragma once
 
 #include <cstdint>
@@ -71,28 +82,51 @@ constexpr int kBwdMmaWarp = 9;   // S and dP
 constexpr int kBwdAccWarp = 10;  // the accumulations (dV, dK or dQ)
 constexpr int kModeDQ = 0;
 constexpr int kModeDKV = 1;
+constexpr int kModeFused = 2;
 
 
 template <int D, int MODE>
 struct BwdLayout {
   static_assert(D == 64 || D == 128, "head dim");
+  static constexpr bool kKeys = (MODE != kModeDQ);  // rows are keys (dK/dV and fused passes)
+  static constexpr bool kFused = (MODE == kModeFused);
   static constexpr int kSlabs = D / 64;
   static constexpr uint32_t kSlabBytes = 128 * 128;
   static constexpr uint32_t kTileBytes = kSlabBytes * kSlabs;
   static constexpr int kStages = (D == 128) ? 2 : 3;
-  static constexpr uint32_t kVecBytes = (MODE == kModeDKV) ? 2 * 128 * 4 : 0;  // −log2-LSE and D of 128 queries
+  static constexpr uint32_t kVecBytes = kKeys ? 2 * 128 * 4 : 0;  // −log2-LSE and D of 128 queries
   static constexpr uint32_t kSlotBytes = 2 * kTileBytes + ((kVecBytes + 1023) / 1024) * 1024;
   static constexpr uint32_t kXOff = 0;                       // X, X2
   static constexpr uint32_t kRingOff = 2 * kTileBytes;
-  static constexpr uint32_t kBarOff = kRingOff + kStages * kSlotBytes;
+  // Fused pass: the dS tile, 128 keys × 128 queries bf16 in two 64-query
+  // slabs with the 128-byte swizzle (K-major for dK, MN-major for dQ).
+  static constexpr uint32_t kDSOff = kRingOff + kStages * kSlotBytes;
+  // The fused pass stages its fp32 dQ(n) (128 × D: D/32 spans of 128 rows ×
+  // 32 values, 128-byte swizzle) in a buffer of its own when one fits
+  // (d = 64): the warps then never wait for the reduce-adds to read it before
+  // going on, only before they restage their rows a block later.  Else
+  // (d = 128) in block n's ring slot, over its Q and dO tiles, which goes back
+  // to the loader once the copies have read it.
+  static constexpr uint32_t kStageBytes = (D / 32) * 128 * 128;
+  static_assert(!kFused || 2 * kTileBytes == kStageBytes, "dQ staging fits the slot's two tiles");
+  static constexpr bool kStageOwn =
+      kFused && kDSOff + 2 * kSlabBytes + kStageBytes + 1024 <= 227 * 1024;
+  static constexpr uint32_t kStageOff = kDSOff + (kFused ? 2 * kSlabBytes : 0);
+  static constexpr uint32_t kTilesBytes = kStageOff + (kStageOwn ? kStageBytes : 0);
   // barriers: fix_full, ring_full[S], ring_empty[S], s_full, dp_full, p_full[2], ds_full[2][2],
-  //           acc_a, acc_b, done, dq_done[2], s_full_1, acc_a_1, p_full_1[2]
-  static constexpr int kNumBars = 1 + 2 * kStages + 17;
-  // The dK/dV pass at d = 64 leaves TMEM columns [384, 512) free: S gets a
-  // second buffer there, so S(n+1) does not wait for dV(n).
-  static constexpr bool kDblS = (MODE == kModeDKV && D == 64);
-  static constexpr uint32_t kMiscOff = kBarOff + 8 * kNumBars;
-  static constexpr uint32_t kSmemBytes = kMiscOff + 16 + 1024;
+  //           acc_a, acc_b, done, dq_done[2], s_full_1, acc_a_1, p_full_1[2], dq_full, dq_free
+  static constexpr int kNumBars = 1 + 2 * kStages + 19;
+  // The dK/dV and fused passes at d = 64 leave TMEM columns [384, 512) free:
+  // S gets a second buffer there, so S(n+1) does not wait for dV(n).
+  static constexpr bool kDblS = (kKeys && D == 64);
+  // The barriers and words (under 512 B) sit below the 1024-byte-aligned
+  // tiles when the alignment gap holds them, else right after the tiles:
+  // both fit in tiles + 1024 bytes.
+  static constexpr uint32_t kMiscOff = 8 * kNumBars;  // within the barrier block
+  static constexpr uint32_t kMetaBytes = kMiscOff + 16;
+  static_assert(kMetaBytes <= 512, "the barrier block fits below the tiles or after them");
+  static constexpr uint32_t kSmemBytes = kTilesBytes + 1024;
+  static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
 };
 
 template <int D, bool CAUSAL, int MODE>
@@ -100,15 +134,20 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_x2,
                     const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
                     const __grid_constant__ CUtensorMap tm_o0, const __grid_constant__ CUtensorMap tm_o1,
-                    const BwdParams p) {
+                    const __grid_constant__ CUtensorMap tm_dq, const BwdParams p) {
   using L = BwdLayout<D, MODE>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* const smem = smem_raw + (base - raw);
+  // base − raw < 1024: the barrier block goes below base when it fits there,
+  // else after the tiles (then base − raw < kMetaBytes ≤ 1024 − kMetaBytes).
+  const uint32_t meta = (base - raw >= L::kMetaBytes) ? raw : base + L::kTilesBytes;
+  uint8_t* const meta_ptr = smem_raw + (meta - raw);
   const uint32_t sX = base + L::kXOff;
   const uint32_t sRing = base + L::kRingOff;
-  const uint32_t bars = base + L::kBarOff;
+  const uint32_t sDS = base + L::kDSOff;
+  const uint32_t bars = meta;
   const uint32_t bar_fix = bars;
   auto bar_ring_full = [&](int s) { return bars + 8u * (1 + s); };
   auto bar_ring_empty = [&](int s) { return bars + 8u * (1 + L::kStages + s); };
@@ -139,8 +178,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   // DQ: dQ of the blocks using dS buffer i done (that buffer is free); one
   // barrier per buffer, so each is waited on one phase at a time
   auto bar_dq_done = [&](int i) { return bar_b0 + 8u * (11 + i); };
-  uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMiscOff);
-  volatile uint32_t* const abort_flag = reinterpret_cast<volatile uint32_t*>(smem + L::kMiscOff + 4);
+  // Fused: dV(n), dK(n) and dQ(n) done (one commit after dQ(n): block n's
+  // slot and the dS tile are no longer read, dQ(n) can be read out); and
+  // dQ(n) read out of TMEM by all eight warps (its columns are free).  One
+  // barrier each, phase n: the warps read dQ(n) before they store dS(n+1),
+  // which dQ(n+1) waits for, and S or dP of block n+2 waits for dQ(n)'s
+  // release before the warps can reach dQ(n+1).
+  const uint32_t bar_dq_full = bar_b0 + 8u * 17;
+  const uint32_t bar_dq_free = bar_b0 + 8u * 18;
+  uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(meta_ptr + L::kMiscOff);
+  volatile uint32_t* const abort_flag = reinterpret_cast<volatile uint32_t*>(meta_ptr + L::kMiscOff + 4);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -166,10 +213,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   if (c_end < c_first) c_end = c_first;
   // The dK/dV pass walks its column blocks once per query head of the group.
   const int n_per = c_end - c_first;
-  const int nblk = (MODE == kModeDKV) ? n_per * p.group : n_per;
+  const int nblk = L::kKeys ? n_per * p.group : n_per;
   // Column block n: its first column, and the head of the A/B tensors.
-  auto col0_of = [&](int n) { return (c_first + (MODE == kModeDKV ? n % max(n_per, 1) : n)) * 128; };
-  auto head_of = [&](int n) { return MODE == kModeDKV ? h * p.group + n / max(n_per, 1) : h / p.group; };
+  auto col0_of = [&](int n) { return (c_first + (L::kKeys ? n % max(n_per, 1) : n)) * 128; };
+  auto head_of = [&](int n) { return L::kKeys ? h * p.group + n / max(n_per, 1) : h / p.group; };
 
   if (warp == kBwdLoaderWarp) {
     tmem_alloc(smem_u32(tmem_slot), 512);
@@ -181,7 +228,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     mbar_init(bar_fix, 1);
     for (int s = 0; s < L::kStages; ++s) {
       mbar_init(bar_ring_full(s), 1);
-      mbar_init(bar_ring_empty(s), 1);
+      // fused with dQ staged in the slot: released by the eight warps once
+      // their reduce-adds have read it; else by the accumulation issuer's commit
+      mbar_init(bar_ring_empty(s), (L::kFused && !L::kStageOwn) ? 8 : 1);
     }
     mbar_init(bar_s_full(0), 1);
     mbar_init(bar_s_full(1), 1);
@@ -197,6 +246,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     mbar_init(bar_acc_b, 1);
     mbar_init(bar_done, 2);  // one commit per issuing thread
     for (int i = 0; i < 2; ++i) mbar_init(bar_dq_done(i), 1);
+    mbar_init(bar_dq_full, 1);
+    mbar_init(bar_dq_free, 8);  // one arrival per gradient warp
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     fence_proxy_async_smem();
   }
@@ -210,6 +261,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   // buffers of 64, so neither the next block's dP nor its dS waits for the
   // previous dQ += dS K.
   auto tDS = [&](int n) { return tAcc1 + 64u * (n & 1); };
+  // Fused pass: dQ(n) in S(n)'s free middle columns (d = 64) or over dP
+  // (d = 128); P's half hh packed at column pcol(hh) of S's buffer.
+  auto tQ = [&](int n) { return D == 64 ? tS(n) + 32u : tdP; };
+  auto pcol = [](int hh) { return static_cast<uint32_t>(64 * hh + ((L::kFused && D == 64 && hh) ? 32 : 0)); };
 
   if (warp == kBwdLoaderWarp) {
     // ============================================================ loader
@@ -230,7 +285,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           tma_load_4d(dst + s * L::kSlabBytes, &tm_a, 64 * s, ha, c0, b, bar_ring_full(slot));
           tma_load_4d(dst + L::kTileBytes + s * L::kSlabBytes, &tm_b, 64 * s, ha, c0, b, bar_ring_full(slot));
         }
-        if (MODE == kModeDKV) {
+        if (L::kKeys) {
           const size_t row = (static_cast<size_t>(b) * p.H + ha) * p.pitch + c0;
           bulk_load(dst + 2 * L::kTileBytes, p.lse2 + row, 512, bar_ring_full(slot));
           bulk_load(dst + 2 * L::kTileBytes + 512, p.dvec + row, 512, bar_ring_full(slot));
@@ -249,6 +304,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     if (lane == 0 && nblk > 0) {
       constexpr uint32_t idS = idesc_bf16(128, 128, false);
       constexpr uint32_t idAcc = idesc_bf16(128, D, true);
+      constexpr uint32_t idDQ = idesc_bf16(128, D, true, true);  // fused dQ: both operands MN-major
       const uint64_t dX = sdesc_kmajor_sw128(sX);
       const uint64_t dX2 = sdesc_kmajor_sw128(sX + L::kTileBytes);
       // S = X·Aᵀ (which = 0) or dP = X2·Bᵀ (which = 1) of block n, all 128
@@ -287,7 +343,30 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         }
         for (int n = 0; n + 1 < nblk && ok; ++n) {
           if (!wait_bar(bar_ring_full((n + 1) % L::kStages), ((n + 1) / L::kStages) & 1, wc)) { ok = false; break; }
-          if (MODE == kModeDKV) {
+          if (L::kFused) {
+            // d = 64: S(n+1)'s buffer held P(n − 1) and dQ(n − 1), whose read-out
+            // follows dV(n − 1); dP(n+1) needs dP(n) read (dS goes to shared
+            // memory).  d = 128: S(n+1) overwrites P(n), read by dV(n); dP(n+1)
+            // overwrites dQ(n), so it waits for dQ(n)'s read-out.
+            if (L::kDblS) {
+              if (n >= 1 && !wait_bar(bar_dq_free, (n - 1) & 1, wc)) { ok = false; break; }
+            } else if (!wait_bar(bar_acc_a(n), s_par(n), wc)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            product(n + 1, 0);
+            if (L::kDblS) {
+              for (int hh = 0; hh < 2 && ok; ++hh)
+                if (!wait_bar(bar_ds_full(hh, n), ds_par(n), wc)) ok = false;
+              if (!ok) break;
+            } else if (!wait_bar(bar_dq_free, n & 1, wc)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            product(n + 1, 1);
+          } else if (MODE == kModeDKV) {
             // S(n+1) overwrites P(n): it goes in once dV(n) has completed;
             // dP(n+1) overwrites dS(n) once dK(n) has.
             if (L::kDblS) {  // S(n+1)'s buffer was last read by dV(n − 1)
@@ -322,7 +401,42 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         // The ring slot of block n is released after its last accumulation:
         // S(n) and dP(n), its other readers, have completed by then (the
         // warpgroups stored dS(n) after reading both).
+        const uint64_t dDSk = sdesc_kmajor_sw128(sDS);                    // dSᵀ [key, query], K-major
+        const uint64_t dDSmn = sdesc_mnmajor_sw128(sDS, L::kSlabBytes);  // dS [query, key], MN-major
+        const uint64_t dXmn = sdesc_mnmajor_sw128(sX, L::kSlabBytes);    // K [key, d], MN-major
         for (int n = 0; n < nblk && ok; ++n) {
+          if (L::kFused) {
+            // dV += Pᵀ dO half by half as the warpgroups store P (TMEM operand).
+            for (int hh = 0; hh < 2 && ok; ++hh) {
+              if (!wait_bar(bar_p_full(hh, n), s_par(n), wc)) { ok = false; break; }
+              tc_fence_after();
+              acc_half(n, hh, tAcc0, tS(n) + pcol(hh), 1);
+            }
+            if (!ok) break;
+            mma_commit(bar_acc_a(n));
+            // dK += dSᵀ Q half by half as dS lands in shared memory.
+            const uint64_t dQt = sdesc_mnmajor_sw128(sRing + (n % L::kStages) * L::kSlotBytes, L::kSlabBytes);
+            for (int hh = 0; hh < 2 && ok; ++hh) {
+              if (!wait_bar(bar_ds_full(hh, n), ds_par(n), wc)) { ok = false; break; }
+              tc_fence_after();
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk) {
+                const uint32_t acc = (n > 0 || hh > 0 || kk > 0) ? 1u : 0u;
+                mma_ss(tAcc1, dDSk + ((hh * L::kSlabBytes + kk * 32) >> 4), dQt + (((4 * hh + kk) * 2048) >> 4),
+                       idAcc, acc);
+              }
+            }
+            if (!ok) break;
+            // dQ(n) = dS K over the block's 128 keys (16 per step).
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk)
+              mma_ss(tQ(n), dDSmn + ((kk * 2048) >> 4), dXmn + ((kk * 2048) >> 4), idDQ, kk > 0 ? 1u : 0u);
+            mma_commit(bar_dq_full);
+            // Staged in the slot, dQ(n) is released by the warps; else the
+            // slot is free now.
+            if (L::kStageOwn) mma_commit(bar_ring_empty(n % L::kStages));
+            continue;
+          }
           if (MODE == kModeDKV) {
             // dV += Pᵀ dO, half by half as the warpgroups store P.
             for (int hh = 0; hh < 2 && ok; ++hh) {
@@ -377,12 +491,68 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
     const uint64_t sc2 = pack2(p.scale_log2, p.scale_log2);
     const uint64_t zero2 = 0;
+    const bool key_pad = L::kFused && row >= p.Sk;
+    // Fused pass: read dQ(m) out of TMEM (which frees its columns), stage it
+    // as fp32 with the 128-byte swizzle — in the staging buffer, or in block
+    // m's ring slot (free once dQ(m) is done: every reader of the slot has
+    // completed) — and add it into the fp32 accumulator in device memory, 32
+    // rows × 32 columns per copy.  Warp w owns rows [32(w&3), 32(w&3)+32) and
+    // columns [hh·D/2, (hh+1)·D/2) of the staging, and its lane 0 issues
+    // their copies; a ring slot is released when all eight warps' copies
+    // have read it, the staging buffer's rows when the warp's own have.
+    auto dq_out = [&](int m) -> bool {
+      const bool got = wait_bar(bar_dq_full, m & 1, wc);
+      if (__any_sync(0xffffffffu, !got)) return false;
+      tc_fence_after();
+      const int slot = m % L::kStages;
+      const uint32_t sstage = L::kStageOwn ? base + L::kStageOff : sRing + slot * L::kSlotBytes;
+      uint8_t* const stage = smem + (sstage - base);
+      if (L::kStageOwn) {  // the warp's previous copies must have read its rows
+        if (lane == 0) tma_store_wait_read0();
+        __syncwarp();
+      }
+#pragma unroll
+      for (int c = 0; c < D / 64; ++c) {
+        uint32_t x[32];
+        tmem_ld32(tQ(m) + hh * (D / 2) + 32 * c + lane_off, x);
+        tmem_wait_ld();
+        reg_fence32(x);
+        if (c == D / 64 - 1) {  // the warp's last read of dQ(m)
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar_dq_free);
+        }
+        uint8_t* const rowp = stage + (hh * (D / 64) + c) * (128 * 128) + r * 128;
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+          *reinterpret_cast<uint4*>(rowp + ((q ^ (r & 7)) << 4)) =
+              make_uint4(x[4 * q], x[4 * q + 1], x[4 * q + 2], x[4 * q + 3]);
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        const int qd = warp & 3;
+        const int y = (b * p.H + head_of(m)) * p.pitch + col0_of(m) + 32 * qd;
+#pragma unroll
+        for (int c = 0; c < D / 64; ++c) {
+          const int j = hh * (D / 64) + c;
+          tma_reduce_add_2d(&tm_dq, sstage + j * (128 * 128) + qd * (32 * 128), 32 * j, y);
+        }
+        tma_store_commit();
+        if (!L::kStageOwn) {
+          tma_store_wait_read0();
+          mbar_arrive(bar_ring_empty(slot));
+        }
+      }
+      __syncwarp();
+      return true;
+    };
     bool ok = true;
     for (int n = 0; n < nblk && ok; ++n) {
       const int c0 = col0_of(n);
       const float* vec = reinterpret_cast<const float*>(smem + L::kRingOff + (n % L::kStages) * L::kSlotBytes +
                                                         2 * L::kTileBytes);
-      if (MODE == kModeDKV) {
+      if (L::kKeys) {
         // The block's −log2-LSE and D arrived with its ring slot (which stays
         // loaded until this block's dS has been consumed).
         const bool in = wait_bar(bar_ring_full(n % L::kStages), (n / L::kStages) & 1, wc);
@@ -447,17 +617,29 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           pv[e] = pe[0];
           pv[e + 1] = pe[1];
         }
+        if (key_pad) {
+          // A key row beyond Sk (zero-filled K, V) scores 0, so its P would be
+          // exp(−LSE), which overflows for LSE < −88; its dS would then reach
+          // dQ as inf · 0.  Such rows contribute nothing.
+#pragma unroll
+          for (int e = 0; e < 64; ++e) pv[e] = 0.f;
+        }
       }
-      if (MODE == kModeDKV) {
-        // Packed bf16 P over the first 32 columns of this half of S.
+      if (L::kKeys) {
+        // Packed bf16 P over 32 of the columns of this half of S.
         uint32_t pk[32];
 #pragma unroll
         for (int e = 0; e < 32; ++e) pk[e] = pack_bf16x2(pv[2 * e], pv[2 * e + 1]);
-        tmem_st32(tS(n) + 64 * hh + lane_off, pk);
+        tmem_st32(tS(n) + pcol(hh) + lane_off, pk);
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(bar_p_full(hh, n));
+      }
+      // Fused: the previous block's dQ, computed meanwhile, leaves now.
+      if (L::kFused && n >= 1 && !dq_out(n - 1)) {
+        ok = false;
+        break;
       }
       // ---- dS = P ∘ (dP − D)
       {
@@ -476,7 +658,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll
         for (int e = 0; e < 64; e += 2) {  // pairs: P·(dP − D) (packed fp32)
           uint64_t d2 = d_row2;
-          if (MODE == kModeDKV) {
+          if (L::kKeys) {
             const uint4 w = *reinterpret_cast<const uint4*>(vec + 128 + 64 * hh + (e & ~3));
             d2 = (e & 2) ? ((static_cast<uint64_t>(w.w) << 32) | w.z) : ((static_cast<uint64_t>(w.y) << 32) | w.x);
           }
@@ -485,6 +667,19 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           unpack2(ffma2(pack2(pv[e], pv[e + 1]), diff, zero2), a, b2);
           qk[e / 2] = pack_bf16x2(a, b2);
         }
+      }
+      if (L::kFused) {
+        // dS(n) into row r of slab hh of the shared tile (its readers dK(n − 1)
+        // and dQ(n − 1) completed before dQ(n − 1) was read out).
+        uint8_t* const rowp = smem + L::kDSOff + hh * L::kSlabBytes + r * 128;
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+          *reinterpret_cast<uint4*>(rowp + ((q ^ (r & 7)) << 4)) =
+              make_uint4(qk[4 * q], qk[4 * q + 1], qk[4 * q + 2], qk[4 * q + 3]);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_ds_full(hh, n));
+        continue;
       }
       uint32_t tdst;
       if (MODE == kModeDQ) {
@@ -505,6 +700,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_ds_full(hh, n));
     }
+    if (L::kFused && ok && nblk > 0) ok = dq_out(nblk - 1);
+    // (shared memory must stay valid until the warp's last copies have read it)
+    if (L::kFused && lane == 0) tma_store_wait_read0();
     // ------------------------------------------------------------ outputs
     // The tile's outputs leave by TMA store (rows beyond the tensor are
     // clipped by the copy), staged with the 128-byte swizzle in the X / X2
@@ -589,10 +787,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 // queries get P = 0; negated so that the gradient warps form
 // s·scale·log2 e − LSE₂ with one packed FMA per pair).  One warp per (batch, head, row): its lanes read the row's D
 // elements of O and dO as consecutive 4- or 8-byte pieces (coalesced) and the
-// products are summed with shuffles.
+// products are summed with shuffles.  For the fused pass it also zeroes the
+// row's D fp32 values of the dQ accumulator [B·H, pitch, D] (dq_acc non-null).
 template <int D>
 __global__ void attn_bwd_prep_kernel(const uint16_t* o, const uint16_t* dout, const float* lse, float* lse2,
-                                     float* dvec, int B, int H, int Sq, int pitch) {
+                                     float* dvec, float* dq_acc, int B, int H, int Sq, int pitch) {
   constexpr int kPer = D / 32;  // bf16 values per lane: 2 or 4
   const int lane = threadIdx.x & 31;
   const long long n = static_cast<long long>(B) * H * pitch;
@@ -600,6 +799,11 @@ __global__ void attn_bwd_prep_kernel(const uint16_t* o, const uint16_t* dout, co
   for (long long t = blockIdx.x * static_cast<long long>(blockDim.x >> 5) + (threadIdx.x >> 5); t < n; t += warps) {
     const int i = static_cast<int>(t % pitch);
     const long long bh = t / pitch;
+    if (dq_acc != nullptr) {
+      float* const a = dq_acc + t * D + lane * kPer;
+      if constexpr (kPer == 4) *reinterpret_cast<float4*>(a) = make_float4(0.f, 0.f, 0.f, 0.f);
+      else *reinterpret_cast<float2*>(a) = make_float2(0.f, 0.f);
+    }
     if (i >= Sq) {
       if (lane == 0) {
         lse2[t] = -INFINITY;
@@ -629,6 +833,34 @@ __global__ void attn_bwd_prep_kernel(const uint16_t* o, const uint16_t* dout, co
       dvec[t] = acc;
       lse2[t] = lse[(static_cast<size_t>(b) * H + h) * Sq + i] * -1.4426950408889634f;
     }
+  }
+}
+
+// dQ = scale · (the fused pass's fp32 accumulator), rounded once to bf16:
+// acc [B·H, pitch, D] → dq [B, Sq, H, D].  One thread per 8 values (two
+// 16-byte loads, one 16-byte store; consecutive threads along the output).
+template <int D>
+__global__ void attn_bwd_dq_convert_kernel(const float* dq_acc, uint16_t* dq, int B, int H, int Sq, int pitch,
+                                           float scale) {
+  constexpr int kChunks = D / 8;
+  const long long n = static_cast<long long>(B) * Sq * H * kChunks;
+  for (long long t = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; t < n;
+       t += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const int c = static_cast<int>(t % kChunks);
+    const long long row = t / kChunks;  // (b, i, h) in output order
+    const int h = static_cast<int>(row % H);
+    const long long bi = row / H;
+    const int i = static_cast<int>(bi % Sq);
+    const long long bb = bi / Sq;
+    const float* src = dq_acc + ((bb * H + h) * pitch + i) * D + 8 * c;
+    const float4 lo = *reinterpret_cast<const float4*>(src);
+    const float4 hi = *reinterpret_cast<const float4*>(src + 4);
+    uint4 w;
+    w.x = pack_bf16x2(scale * lo.x, scale * lo.y);
+    w.y = pack_bf16x2(scale * lo.z, scale * lo.w);
+    w.z = pack_bf16x2(scale * hi.x, scale * hi.y);
+    w.w = pack_bf16x2(scale * hi.z, scale * hi.w);
+    *reinterpret_cast<uint4*>(dq + row * D + 8 * c) = w;
   }
 }
 

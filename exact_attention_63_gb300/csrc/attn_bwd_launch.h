@@ -24,18 +24,23 @@ struct BwdParams {
 
 struct BwdLaunchArgs {
   CUtensorMap x, x2, a, b;  // row tiles X, X2 and the streamed A, B (4-D maps as in the forward)
-  CUtensorMap o0, o1;       // outputs (bf16, dense): dQ pass o0 = dQ [B, Sq, H, D]; dK/dV pass o0 = dV, o1 = dK
-                            // [B, Sk, H_kv, D]
+  CUtensorMap o0, o1;       // outputs (bf16, dense): dQ pass o0 = dQ [B, Sq, H, D]; dK/dV and fused passes
+                            // o0 = dV, o1 = dK [B, Sk, H_kv, D]
+  CUtensorMap dq;           // fused pass: fp32 dQ accumulator [B·H·pitch, D], box 32 × 32, 128-byte swizzle
   BwdParams p;
   int grid;
-  int mode;                 // 0: dQ pass, 1: dK/dV pass
+  int mode;                 // 0: dQ pass, 1: dK/dV pass, 2: fused (dK, dV and the dQ accumulator)
   bool causal;
   int device;
   cudaStream_t stream;
 };
 
 cudaError_t launch_bwd(const BwdLaunchArgs& a, int d);
-cudaError_t launch_bwd_prep(const void* o, const void* dout, const float* lse, float* lse2, float* dvec, int B, int H,
-                            int Sq, int pitch, int d, cudaStream_t stream);
+// dq_acc: the fused pass's accumulator [B·H, pitch, d] (zeroed here), or null.
+cudaError_t launch_bwd_prep(const void* o, const void* dout, const float* lse, float* lse2, float* dvec, float* dq_acc,
+                            int B, int H, int Sq, int pitch, int d, cudaStream_t stream);
+// dq [B, Sq, H, d] bf16 = scale · dq_acc [B·H, pitch, d].
+cudaError_t launch_bwd_dq_convert(const float* dq_acc, void* dq, int B, int H, int Sq, int pitch, int d, float scale,
+                                  int sms, cudaStream_t stream);
 
 }  // namespace attn

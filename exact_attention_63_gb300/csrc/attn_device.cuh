@@ -124,6 +124,14 @@ __device__ __forceinline__ void tma_store_4d(const CUtensorMap* m, uint32_t src,
                "r"(src), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
                : "memory");
 }
+// 2-D tiled reduce-add from shared memory into global memory (element-wise
+// atomic with respect to other reductions; the element type is the map's).
+__device__ __forceinline__ void tma_reduce_add_2d(const CUtensorMap* m, uint32_t src, int c0, int c1) {
+  asm volatile("cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.tile.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(m)),
+               "r"(src), "r"(c0), "r"(c1)
+               : "memory");
+}
 __device__ __forceinline__ void tma_store_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void tma_store_wait_read0() {
   asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
@@ -171,11 +179,13 @@ __device__ __forceinline__ uint64_t sdesc_mnmajor_sw128(uint32_t saddr, uint32_t
 }
 
 // Instruction descriptor of tcgen05.mma.kind::f16: bf16 × bf16 → fp32,
-// A K-major, B K-major (b_mn = false) or MN-major (b_mn = true).
-__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool b_mn) {
+// B K-major (b_mn = false) or MN-major (b_mn = true), A K-major unless a_mn
+// (MN-major A: shared-memory operands only).
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool b_mn, bool a_mn = false) {
   return (1u << 4)                                   // accumulator fp32
          | (1u << 7)                                 // A bf16
          | (1u << 10)                                // B bf16
+         | ((a_mn ? 1u : 0u) << 15)                  // A major-ness
          | ((b_mn ? 1u : 0u) << 16)                  // B major-ness
          | (static_cast<uint32_t>(N >> 3) << 17)     // N / 8
          | (static_cast<uint32_t>(M >> 4) << 24);    // M / 16

@@ -245,11 +245,22 @@ int attn_fwd_varlen(const void* q, const void* k, const void* v, void* o, float*
  *                      K and V have H heads).
  *   workspace        : caller-owned DEVICE buffer of at least
  *                      attn_bwd_workspace_size(B, H, Sq) bytes, 256-byte
- *                      aligned (holds D and LSE·log2 e per query row).
+ *                      aligned (holds D and LSE·log2 e per query row and an
+ *                      fp32 dQ accumulator of B·H·⌈Sq/128⌉·128 rows × 128
+ *                      values; its contents on entry do not matter).
  * Arithmetic: bf16 operands, fp32 accumulation in tensor memory, P and dS
  * rounded to bf16 for the products, outputs rounded once to bf16.
- * Enqueues three kernels on `stream` (D and LSE·log2 e, then dK/dV, then dQ)
- * and returns; errors as attn_fwd, plus ATTN_ERR_WORKSPACE.
+ * Schedules.  d = 64 (default): one pass over the key tiles — each key
+ * tile's CTA forms S, dP, P and dS once per (query, key) pair, accumulates dK
+ * and dV in tensor memory and adds its contribution to dQ into the fp32
+ * accumulator in device memory (reduce-add copies); a last kernel scales and
+ * rounds dQ.  The fp32 additions into dQ happen in an order that varies from
+ * run to run, so dQ can differ in its last bits between runs (dK and dV do
+ * not).  d = 128, or attn_bwd_ex() with ATTN_BWD_DETERMINISTIC: two passes
+ * (dK/dV, then dQ, which recomputes S and dP), bit-reproducible.
+ * Enqueues three kernels on `stream` (D and LSE·log2 e, the pass, the dQ
+ * rounding; or D and LSE·log2 e, dK/dV, dQ) and returns; errors as attn_fwd,
+ * plus ATTN_ERR_WORKSPACE.
  */
 size_t attn_bwd_workspace_size(int B, int H, int Sq);
 int attn_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dout,
@@ -267,6 +278,19 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const f
 int attn_bwd_layout(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dout,
                     void* dq, void* dk, void* dv, int B, int H, int Sq, int Sk, int d, float scale, int causal,
                     const attn_layout* layout, void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * attn_bwd_ex — attn_bwd_layout with schedule flags (0: the same call).
+ *   ATTN_BWD_DETERMINISTIC: the two-pass schedule at every head dim; dQ, dK
+ *   and dV are then identical bit for bit from run to run.  Results of the
+ *   two schedules agree within rounding.
+ * Other flag bits: ATTN_ERR_OPTION.  The same workspace rule as attn_bwd.
+ */
+#define ATTN_BWD_DETERMINISTIC 1u
+int attn_bwd_ex(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dout,
+                void* dq, void* dk, void* dv, int B, int H, int Sq, int Sk, int d, float scale, int causal,
+                const attn_layout* layout, unsigned int flags, void* workspace, size_t workspace_bytes,
+                cudaStream_t stream);
 
 /*
  * attn_fwd_host — the same operation on HOST buffers, end to end.
