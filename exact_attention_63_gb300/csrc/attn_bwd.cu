@@ -49,9 +49,9 @@ cudaError_t launch_bwd(const BwdLaunchArgs& a, int d) {
 
 cudaError_t launch_bwd_prep(const void* o, const void* dout, const float* lse, float* lse2, float* dvec, float* dq_acc,
                             int B, int H, int Sq, int pitch, int d, cudaStream_t stream) {
-  const long long n = static_cast<long long>(B) * H * pitch;  // rows, one warp each
+  const long long n = static_cast<long long>(B) * H * pitch;  // rows, 32·8/d per warp
   const int threads = 256;
-  const long long want = n / (threads / 32) + 1;
+  const long long want = n * d / (8 * 32 * (threads / 32)) + 1;
   const int blocks = static_cast<int>(want < 16384 ? want : 16384);
   const uint16_t* o16 = static_cast<const uint16_t*>(o);
   const uint16_t* g16 = static_cast<const uint16_t*>(dout);

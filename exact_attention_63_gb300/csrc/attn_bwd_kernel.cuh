@@ -785,53 +785,55 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 // D = rowsum(dO ∘ O) and −LSE · log2(e) per query row, in [B·H, pitch]
 // arrays padded to whole 128-row blocks (−inf and 0 beyond Sq, so padded
 // queries get P = 0; negated so that the gradient warps form
-// s·scale·log2 e − LSE₂ with one packed FMA per pair).  One warp per (batch, head, row): its lanes read the row's D
-// elements of O and dO as consecutive 4- or 8-byte pieces (coalesced) and the
-// products are summed with shuffles.  For the fused pass it also zeroes the
-// row's D fp32 values of the dQ accumulator [B·H, pitch, D] (dq_acc non-null).
+// s·scale·log2 e − LSE₂ with one packed FMA per pair).  A warp takes 32·8/D
+// rows at once (4 at d = 64, 2 at d = 128): D/8 lanes per row, each reading
+// 8 consecutive bf16 of O and of dO as one 16-byte load, and the products are
+// summed with shuffles within the row's lanes.  For the one-pass kernel it
+// also zeroes the rows of the dQ accumulator [B·H, pitch, D] (dq_acc
+// non-null), 8 fp32 values a lane.
 template <int D>
 __global__ void attn_bwd_prep_kernel(const uint16_t* o, const uint16_t* dout, const float* lse, float* lse2,
                                      float* dvec, float* dq_acc, int B, int H, int Sq, int pitch) {
-  constexpr int kPer = D / 32;  // bf16 values per lane: 2 or 4
+  constexpr int kLanesPerRow = D / 8;
+  constexpr int kRowsPerWarp = 32 / kLanesPerRow;
   const int lane = threadIdx.x & 31;
+  const int sub = lane / kLanesPerRow, li = lane % kLanesPerRow;
   const long long n = static_cast<long long>(B) * H * pitch;
+  const long long groups = (n + kRowsPerWarp - 1) / kRowsPerWarp;
   const long long warps = static_cast<long long>(gridDim.x) * (blockDim.x >> 5);
-  for (long long t = blockIdx.x * static_cast<long long>(blockDim.x >> 5) + (threadIdx.x >> 5); t < n; t += warps) {
+  for (long long g = blockIdx.x * static_cast<long long>(blockDim.x >> 5) + (threadIdx.x >> 5); g < groups;
+       g += warps) {
+    const long long t = g * kRowsPerWarp + sub;  // this lane's row
+    const bool valid = t < n;
     const int i = static_cast<int>(t % pitch);
     const long long bh = t / pitch;
-    if (dq_acc != nullptr) {
-      float* const a = dq_acc + t * D + lane * kPer;
-      if constexpr (kPer == 4) *reinterpret_cast<float4*>(a) = make_float4(0.f, 0.f, 0.f, 0.f);
-      else *reinterpret_cast<float2*>(a) = make_float2(0.f, 0.f);
+    const int b = static_cast<int>(bh / H), h = static_cast<int>(bh % H);
+    if (dq_acc != nullptr && valid) {
+      float4* const a = reinterpret_cast<float4*>(dq_acc + t * D + 8 * li);
+      a[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+      a[1] = make_float4(0.f, 0.f, 0.f, 0.f);
     }
-    if (i >= Sq) {
-      if (lane == 0) {
+    float acc = 0.f;
+    if (valid && i < Sq) {
+      const size_t off = ((static_cast<size_t>(b) * Sq + i) * H + h) * D + 8 * li;
+      const uint4 x = *reinterpret_cast<const uint4*>(o + off), y = *reinterpret_cast<const uint4*>(dout + off);
+      const uint32_t xs[4] = {x.x, x.y, x.z, x.w}, ys[4] = {y.x, y.y, y.z, y.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        acc = fmaf(__uint_as_float(xs[e] << 16), __uint_as_float(ys[e] << 16), acc);
+        acc = fmaf(__uint_as_float(xs[e] & 0xFFFF0000u), __uint_as_float(ys[e] & 0xFFFF0000u), acc);
+      }
+    }
+#pragma unroll
+    for (int m = kLanesPerRow / 2; m > 0; m >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, m);
+    if (valid && li == 0) {
+      if (i < Sq) {
+        dvec[t] = acc;
+        lse2[t] = lse[(static_cast<size_t>(b) * H + h) * Sq + i] * -1.4426950408889634f;
+      } else {
         lse2[t] = -INFINITY;
         dvec[t] = 0.f;
       }
-      continue;
-    }
-    const int b = static_cast<int>(bh / H), h = static_cast<int>(bh % H);
-    const size_t off = ((static_cast<size_t>(b) * Sq + i) * H + h) * D + lane * kPer;
-    uint32_t xs[kPer / 2], ys[kPer / 2];
-    if constexpr (kPer == 4) {
-      const uint2 x = *reinterpret_cast<const uint2*>(o + off), y = *reinterpret_cast<const uint2*>(dout + off);
-      xs[0] = x.x; xs[1] = x.y; ys[0] = y.x; ys[1] = y.y;
-    } else {
-      xs[0] = *reinterpret_cast<const uint32_t*>(o + off);
-      ys[0] = *reinterpret_cast<const uint32_t*>(dout + off);
-    }
-    float acc = 0.f;
-#pragma unroll
-    for (int e = 0; e < kPer / 2; ++e) {
-      acc = fmaf(__uint_as_float(xs[e] << 16), __uint_as_float(ys[e] << 16), acc);
-      acc = fmaf(__uint_as_float(xs[e] & 0xFFFF0000u), __uint_as_float(ys[e] & 0xFFFF0000u), acc);
-    }
-#pragma unroll
-    for (int m = 16; m > 0; m >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, m);
-    if (lane == 0) {
-      dvec[t] = acc;
-      lse2[t] = lse[(static_cast<size_t>(b) * H + h) * Sq + i] * -1.4426950408889634f;
     }
   }
 }
