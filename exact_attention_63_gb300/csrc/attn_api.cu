@@ -666,7 +666,7 @@ int attn_fwd_fp8_ex(const void* q8, const void* k8, const void* v8, void* o, flo
 
 namespace {
 // Workspace: −LSE·log2 e and D per query row ([B·H, pitch] each), then the
-// fused pass's fp32 dQ accumulator [B·H, pitch, 128] (sized for d = 128).
+// one-pass kernel's fp32 dQ accumulator [B·H, pitch, 64] (it runs at d = 64).
 size_t bwd_vec_bytes(int B, int H, int Sq) {
   const size_t pitch = (static_cast<size_t>(Sq) + 127) / 128 * 128;
   return (2 * static_cast<size_t>(B) * H * pitch * 4 + 255) & ~static_cast<size_t>(255);
@@ -698,7 +698,7 @@ int encode_dq_acc(CUtensorMap* m, float* acc, long long rows, int d) {
 size_t attn_bwd_workspace_size(int B, int H, int Sq) {
   if (B < 1 || H < 1 || Sq < 1) return 0;
   const size_t pitch = (static_cast<size_t>(Sq) + 127) / 128 * 128;
-  return bwd_vec_bytes(B, H, Sq) + static_cast<size_t>(B) * H * pitch * 128 * 4;
+  return bwd_vec_bytes(B, H, Sq) + static_cast<size_t>(B) * H * pitch * 64 * 4;
 }
 
 int attn_bwd_layout(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dout,

@@ -19,7 +19,7 @@
 // With grouped key/value heads the dQ pass reads the K/V head of its query
 // head's group, and the dK/dV pass of a K/V head walks the query blocks of
 // every query head in its group (their contributions add up).
-//   FUSED rows = keys, as DKV, and dQ in the same pass: dS goes to a
+//   FUSED (d = 64) rows = keys, as DKV, and dQ in the same pass: dS goes to a
 //       shared-memory tile (not over dP), dK += dSᵀ Q reads it K-major and
 //       dQ(n) = dS K — the block's contribution to its 128 queries' dQ —
 //       reads it MN-major; the warps add dQ(n) into an fp32 accumulator in
@@ -64,8 +64,7 @@
 // then waits for dV(n−1), not dV(n)).  P (bf16 pairs)
 // overwrites S's columns and, in DKV, dS overwrites dP's, in the packed layout
 // the forward uses for P.  The fused pass's dQ(n) goes to S(n)'s columns
-// [32, 96) at d = 64 (P's two halves are packed into [0, 32) and [96, 128)
-// there) and over dP at d = 128.
+// [32, 96) (P's two halves are packed into [0, 32) and [96, 128) there).
 #pragma once
 
 #include <cstdint>
@@ -98,21 +97,21 @@ struct BwdLayout {
   static constexpr uint32_t kSlotBytes = 2 * kTileBytes + ((kVecBytes + 1023) / 1024) * 1024;
   static constexpr uint32_t kXOff = 0;                       // X, X2
   static constexpr uint32_t kRingOff = 2 * kTileBytes;
+  // The fused pass is built for d = 64: at d = 128 S, dP and the two
+  // accumulators take all of TMEM, so dQ(n) would have to share dP's columns
+  // (dP(n+1) then waits for dQ(n)'s read-out), no staging buffer fits beside
+  // the dS tile, and its reduce-adds bound it (slower than the two passes).
+  static_assert(!kFused || D == 64, "the fused pass is built for d = 64");
   // Fused pass: the dS tile, 128 keys × 128 queries bf16 in two 64-query
-  // slabs with the 128-byte swizzle (K-major for dK, MN-major for dQ).
+  // slabs with the 128-byte swizzle (K-major for dK, MN-major for dQ), and
+  // the fp32 dQ(n) staging (128 × 64: two spans of 128 rows × 32 values,
+  // 128-byte swizzle), a buffer of its own: the warps never wait for the
+  // reduce-adds to read it before going on, only before they restage their
+  // rows a block later.
   static constexpr uint32_t kDSOff = kRingOff + kStages * kSlotBytes;
-  // The fused pass stages its fp32 dQ(n) (128 × D: D/32 spans of 128 rows ×
-  // 32 values, 128-byte swizzle) in a buffer of its own when one fits
-  // (d = 64): the warps then never wait for the reduce-adds to read it before
-  // going on, only before they restage their rows a block later.  Else
-  // (d = 128) in block n's ring slot, over its Q and dO tiles, which goes back
-  // to the loader once the copies have read it.
-  static constexpr uint32_t kStageBytes = (D / 32) * 128 * 128;
-  static_assert(!kFused || 2 * kTileBytes == kStageBytes, "dQ staging fits the slot's two tiles");
-  static constexpr bool kStageOwn =
-      kFused && kDSOff + 2 * kSlabBytes + kStageBytes + 1024 <= 227 * 1024;
   static constexpr uint32_t kStageOff = kDSOff + (kFused ? 2 * kSlabBytes : 0);
-  static constexpr uint32_t kTilesBytes = kStageOff + (kStageOwn ? kStageBytes : 0);
+  static constexpr uint32_t kStageBytes = (D / 32) * 128 * 128;
+  static constexpr uint32_t kTilesBytes = kStageOff + (kFused ? kStageBytes : 0);
   // barriers: fix_full, ring_full[S], ring_empty[S], s_full, dp_full, p_full[2], ds_full[2][2],
   //           acc_a, acc_b, done, dq_done[2], s_full_1, acc_a_1, p_full_1[2], dq_full, dq_free
   static constexpr int kNumBars = 1 + 2 * kStages + 19;
@@ -228,9 +227,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     mbar_init(bar_fix, 1);
     for (int s = 0; s < L::kStages; ++s) {
       mbar_init(bar_ring_full(s), 1);
-      // fused with dQ staged in the slot: released by the eight warps once
-      // their reduce-adds have read it; else by the accumulation issuer's commit
-      mbar_init(bar_ring_empty(s), (L::kFused && !L::kStageOwn) ? 8 : 1);
+      mbar_init(bar_ring_empty(s), 1);  // the accumulation issuer's commit
     }
     mbar_init(bar_s_full(0), 1);
     mbar_init(bar_s_full(1), 1);
@@ -261,10 +258,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   // buffers of 64, so neither the next block's dP nor its dS waits for the
   // previous dQ += dS K.
   auto tDS = [&](int n) { return tAcc1 + 64u * (n & 1); };
-  // Fused pass: dQ(n) in S(n)'s free middle columns (d = 64) or over dP
-  // (d = 128); P's half hh packed at column pcol(hh) of S's buffer.
-  auto tQ = [&](int n) { return D == 64 ? tS(n) + 32u : tdP; };
-  auto pcol = [](int hh) { return static_cast<uint32_t>(64 * hh + ((L::kFused && D == 64 && hh) ? 32 : 0)); };
+  // Fused pass: dQ(n) in S(n)'s free middle columns; P's half hh packed at
+  // column pcol(hh) of S's buffer.
+  auto tQ = [&](int n) { return tS(n) + 32u; };
+  auto pcol = [](int hh) { return static_cast<uint32_t>(64 * hh + ((L::kFused && hh) ? 32 : 0)); };
 
   if (warp == kBwdLoaderWarp) {
     // ============================================================ loader
@@ -344,26 +341,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         for (int n = 0; n + 1 < nblk && ok; ++n) {
           if (!wait_bar(bar_ring_full((n + 1) % L::kStages), ((n + 1) / L::kStages) & 1, wc)) { ok = false; break; }
           if (L::kFused) {
-            // d = 64: S(n+1)'s buffer held P(n − 1) and dQ(n − 1), whose read-out
+            // S(n+1)'s buffer held P(n − 1) and dQ(n − 1), whose read-out
             // follows dV(n − 1); dP(n+1) needs dP(n) read (dS goes to shared
-            // memory).  d = 128: S(n+1) overwrites P(n), read by dV(n); dP(n+1)
-            // overwrites dQ(n), so it waits for dQ(n)'s read-out.
-            if (L::kDblS) {
-              if (n >= 1 && !wait_bar(bar_dq_free, (n - 1) & 1, wc)) { ok = false; break; }
-            } else if (!wait_bar(bar_acc_a(n), s_par(n), wc)) {
-              ok = false;
-              break;
-            }
+            // memory).
+            if (n >= 1 && !wait_bar(bar_dq_free, (n - 1) & 1, wc)) { ok = false; break; }
             tc_fence_after();
             product(n + 1, 0);
-            if (L::kDblS) {
-              for (int hh = 0; hh < 2 && ok; ++hh)
-                if (!wait_bar(bar_ds_full(hh, n), ds_par(n), wc)) ok = false;
-              if (!ok) break;
-            } else if (!wait_bar(bar_dq_free, n & 1, wc)) {
-              ok = false;
-              break;
-            }
+            for (int hh = 0; hh < 2 && ok; ++hh)
+              if (!wait_bar(bar_ds_full(hh, n), ds_par(n), wc)) ok = false;
+            if (!ok) break;
             tc_fence_after();
             product(n + 1, 1);
           } else if (MODE == kModeDKV) {
@@ -432,9 +418,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             for (int kk = 0; kk < 8; ++kk)
               mma_ss(tQ(n), dDSmn + ((kk * 2048) >> 4), dXmn + ((kk * 2048) >> 4), idDQ, kk > 0 ? 1u : 0u);
             mma_commit(bar_dq_full);
-            // Staged in the slot, dQ(n) is released by the warps; else the
-            // slot is free now.
-            if (L::kStageOwn) mma_commit(bar_ring_empty(n % L::kStages));
+            mma_commit(bar_ring_empty(n % L::kStages));  // Q(n), dO(n) no longer read
             continue;
           }
           if (MODE == kModeDKV) {
@@ -493,56 +477,38 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const uint64_t zero2 = 0;
     const bool key_pad = L::kFused && row >= p.Sk;
     // Fused pass: read dQ(m) out of TMEM (which frees its columns), stage it
-    // as fp32 with the 128-byte swizzle — in the staging buffer, or in block
-    // m's ring slot (free once dQ(m) is done: every reader of the slot has
-    // completed) — and add it into the fp32 accumulator in device memory, 32
-    // rows × 32 columns per copy.  Warp w owns rows [32(w&3), 32(w&3)+32) and
-    // columns [hh·D/2, (hh+1)·D/2) of the staging, and its lane 0 issues
-    // their copies; a ring slot is released when all eight warps' copies
-    // have read it, the staging buffer's rows when the warp's own have.
+    // as fp32 with the 128-byte swizzle in the staging buffer, and add it
+    // into the fp32 accumulator in device memory, 32 rows × 32 columns per
+    // copy.  Warp w owns rows [32(w&3), 32(w&3)+32) and columns
+    // [32hh, 32hh+32) of the staging (span hh), and its lane 0 issues their
+    // copy; it waits for the copy to have read them only before restaging
+    // them for the next block.
     auto dq_out = [&](int m) -> bool {
       const bool got = wait_bar(bar_dq_full, m & 1, wc);
       if (__any_sync(0xffffffffu, !got)) return false;
       tc_fence_after();
-      const int slot = m % L::kStages;
-      const uint32_t sstage = L::kStageOwn ? base + L::kStageOff : sRing + slot * L::kSlotBytes;
-      uint8_t* const stage = smem + (sstage - base);
-      if (L::kStageOwn) {  // the warp's previous copies must have read its rows
-        if (lane == 0) tma_store_wait_read0();
-        __syncwarp();
-      }
+      const uint32_t sspan = base + L::kStageOff + hh * (128 * 128);
+      if (lane == 0) tma_store_wait_read0();  // the warp's previous copy has read its rows
+      __syncwarp();
+      uint32_t x[32];
+      tmem_ld32(tQ(m) + 32 * hh + lane_off, x);
+      tmem_wait_ld();
+      reg_fence32(x);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_dq_free);
+      uint8_t* const rowp = smem + (sspan - base) + r * 128;
 #pragma unroll
-      for (int c = 0; c < D / 64; ++c) {
-        uint32_t x[32];
-        tmem_ld32(tQ(m) + hh * (D / 2) + 32 * c + lane_off, x);
-        tmem_wait_ld();
-        reg_fence32(x);
-        if (c == D / 64 - 1) {  // the warp's last read of dQ(m)
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(bar_dq_free);
-        }
-        uint8_t* const rowp = stage + (hh * (D / 64) + c) * (128 * 128) + r * 128;
-#pragma unroll
-        for (int q = 0; q < 8; ++q)
-          *reinterpret_cast<uint4*>(rowp + ((q ^ (r & 7)) << 4)) =
-              make_uint4(x[4 * q], x[4 * q + 1], x[4 * q + 2], x[4 * q + 3]);
-      }
+      for (int q = 0; q < 8; ++q)
+        *reinterpret_cast<uint4*>(rowp + ((q ^ (r & 7)) << 4)) =
+            make_uint4(x[4 * q], x[4 * q + 1], x[4 * q + 2], x[4 * q + 3]);
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) {
         const int qd = warp & 3;
         const int y = (b * p.H + head_of(m)) * p.pitch + col0_of(m) + 32 * qd;
-#pragma unroll
-        for (int c = 0; c < D / 64; ++c) {
-          const int j = hh * (D / 64) + c;
-          tma_reduce_add_2d(&tm_dq, sstage + j * (128 * 128) + qd * (32 * 128), 32 * j, y);
-        }
+        tma_reduce_add_2d(&tm_dq, sspan + qd * (32 * 128), 32 * hh, y);
         tma_store_commit();
-        if (!L::kStageOwn) {
-          tma_store_wait_read0();
-          mbar_arrive(bar_ring_empty(slot));
-        }
       }
       __syncwarp();
       return true;

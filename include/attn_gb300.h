@@ -245,9 +245,10 @@ int attn_fwd_varlen(const void* q, const void* k, const void* v, void* o, float*
  *                      K and V have H heads).
  *   workspace        : caller-owned DEVICE buffer of at least
  *                      attn_bwd_workspace_size(B, H, Sq) bytes, 256-byte
- *                      aligned (holds D and LSE·log2 e per query row and an
- *                      fp32 dQ accumulator of B·H·⌈Sq/128⌉·128 rows × 128
- *                      values; its contents on entry do not matter).
+ *                      aligned (holds D and LSE·log2 e per query row and,
+ *                      for the one-pass schedule, an fp32 dQ accumulator of
+ *                      B·H·⌈Sq/128⌉·128 rows × 64 values; its contents on
+ *                      entry do not matter).
  * Arithmetic: bf16 operands, fp32 accumulation in tensor memory, P and dS
  * rounded to bf16 for the products, outputs rounded once to bf16.
  * Schedules.  d = 64 (default): one pass over the key tiles — each key

@@ -172,9 +172,10 @@ def test_backward_layout_checks(L):
     assert L.attn_bwd(A, A, A, A, A, 0, A, A, A, 1, 4, 8, 8, 64, 0.125, 1, A, 1 << 20, None) == -1
     assert L.attn_bwd_ex(A, A, A, A, A, A, A, A, A, 1, 4, 8, 8, 64, 0.125, 1, None, 2, A, 1 << 20, None) == -9
     # workspace: −LSE·log2 e and D ([B·H, pitch] fp32 each, rounded up to 256
-    # bytes), then the one-pass schedule's fp32 dQ accumulator [B·H, pitch, 128]
-    assert L.attn_bwd_workspace_size(1, 4, 8) == 2 * 4 * 128 * 4 + 4 * 128 * 128 * 4
-    assert L.attn_bwd_workspace_size(2, 3, 129) == 2 * 6 * 256 * 4 + 6 * 256 * 128 * 4
+    # bytes), then the one-pass (d = 64) schedule's fp32 dQ accumulator
+    # [B·H, pitch, 64]
+    assert L.attn_bwd_workspace_size(1, 4, 8) == 2 * 4 * 128 * 4 + 4 * 128 * 64 * 4
+    assert L.attn_bwd_workspace_size(2, 3, 129) == 2 * 6 * 256 * 4 + 6 * 256 * 64 * 4
     assert L.attn_bwd(A, A, A, A, A, A, A, A, A, 1, 4, 8, 8, 64, 0.125, 1, A,
                       L.attn_bwd_workspace_size(1, 4, 8) - 1, None) == -10
 
