@@ -472,7 +472,11 @@ def pin_backward_finite_differences():
 def pin_backward_identities():
     """D = rowsum(dO ∘ O); Σ_j dS_ij = 0 makes Σ_j dK-contributions vanish:
     adding a constant vector to every key changes nothing, so the key
-    gradients sum to zero; the batched call matches the per-head one."""
+    gradients sum to zero; each row of P sums to one, so the value
+    gradients sum to Σ_i dO_i (every row here sees a key); scaling q by
+    (1 + ε) and k by 1/(1 + ε) leaves the scores unchanged, so
+    Σ_i ⟨dQ_i, q_i⟩ = Σ_j ⟨dK_j, k_j⟩; the batched call matches the per-head
+    one."""
     q, k, v = rand_head(1950, 20, 30, 16, sigma=1.5)
     dO = _rng(1951).standard_normal((20, 16))
     for causal in (False, True):
@@ -480,6 +484,9 @@ def pin_backward_identities():
         O, _ = oracle.attention_head(q, k, v, 0.25, causal)
         assert np.max(np.abs(D - (dO * O).sum(axis=1))) <= TOL
         assert np.max(np.abs(dK.sum(axis=0))) <= 1e-10
+        assert np.max(np.abs(dV.sum(axis=0) - dO.sum(axis=0))) <= 1e-10
+        lhs, rhs = float((dQ * q).sum()), float((dK * k).sum())
+        assert abs(lhs - rhs) <= 1e-10 * max(1.0, abs(lhs)) and abs(lhs) > 1e-3
     r = _rng(1952)
     qb, kb, vb, db = (_bf16_like(r.standard_normal((2, 11, 3, 8))) for _ in range(4))
     dQ, dK, dV = oracle.attention_backward(qb, kb, vb, db, 0.35, True)

@@ -189,3 +189,25 @@ def test_backward_longest_workload_sampled_rows():
         check("dq", dq[0, rows, h], rq, f"{w.name} head {h}")
         check("dk", dk[0, rows, h], rk, f"{w.name} head {h}")
         check("dv", dv[0, rows, h], rv, f"{w.name} head {h}")
+
+
+def test_backward_long_d64_one_pass_sampled_rows():
+    """The one-pass kernel at 32768 keys (B1 H2 S32768 d64 causal): every dQ
+    row gathers reduce-adds from up to 256 key tiles.  dQ rows and dK, dV rows
+    sampled across the sequence in both heads, against the oracle's per-row
+    gradients; the tolerance's scale is the largest |value| among them."""
+    need_gpu()
+    w = C(1, 2, 32768, 32768, 64, True, seed=119)
+    q, k, v = inputs.make_inputs(w)
+    g = torch.Generator().manual_seed(w.seed + 2000)
+    dout = torch.randn(q.shape, generator=g).to(torch.bfloat16)
+    dq, dk, dv = grads(w, q, k, v, dout)
+    rng = np.random.default_rng(6)
+    fixed = [0, 1, 127, 128, 255, 256, 16383, 16384, w.Sq - 129, w.Sq - 128, w.Sq - 1]
+    rows = np.array(sorted(set(fixed) | set(int(x) for x in rng.integers(0, w.Sq, 20))))
+    for h in range(w.H):
+        sel = lambda t: oracle.to_f64(t[0, :, h, :])
+        rq, rk, rv = oracle.attention_backward_rows(sel(q), sel(k), sel(v), sel(dout), w.scale, w.causal, rows, rows)
+        check("dq", dq[0, rows, h], rq, f"{w.name} head {h}")
+        check("dk", dk[0, rows, h], rk, f"{w.name} head {h}")
+        check("dv", dv[0, rows, h], rv, f"{w.name} head {h}")

@@ -51,6 +51,8 @@ MUTANTS = {
     "bwd_group_overwrites": ("            dK[b, :, g] += dk", "            dK[b, :, g] = dk"),
     "bwd_dk_unscaled": ("scale * (dS.T @ q), dV, D", "(dS.T @ q), dV, D"),
     "bwd_dq_uses_v": ("return scale * (dS @ k), scale", "return scale * (dS @ v), scale"),
+    "bwd_dq_unscaled": ("return scale * (dS @ k), scale", "return (dS @ k), scale"),
+    "bwd_dv_from_dp": ("    dV = P.T @ dO", "    dV = (P * (dO @ v.T)).T @ dO"),
     "varlen_global_offset": ("        off = (k1 - k0) - (q1 - q0) if (causal and bottom_right) else 0",
                              "        off = (cu_k[-1] - cu_q[-1]) if (causal and bottom_right) else 0"),
     "varlen_keys_from_start": ("k[k0:k1, g, :], v[k0:k1, g, :], scale", "k[0:k1 - k0, g, :], v[0:k1 - k0, g, :], scale"),
