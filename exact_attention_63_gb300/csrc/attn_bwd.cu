@@ -1,5 +1,6 @@
 // Attention backward kernels: instantiations and launches (both head dims,
-// both masks, both passes) and the preparation kernel.
+// both masks, the two passes and the one-pass kernel at d = 64), the preparation
+// kernel and the rounding of the one-pass kernel's dQ.
 #include "attn_bwd_launch.h"
 
 #include "attn_bwd_kernel.cuh"

@@ -9,7 +9,7 @@
 // intermediates in tensor memory.  These kernels do that too: S, dP, P, dS and
 // the accumulators live in TMEM, and P / dS feed the MMAs from there.)
 //
-// One kernel template serves both passes; a CTA owns one tile of 128 rows of
+// One kernel template serves the two passes and the fused one; a CTA owns one tile of 128 rows of
 // one (batch, head) and walks the blocks of 128 columns that the rows see:
 //   DQ  rows = queries (X = Q, X2 = dO), columns = keys  (A = K, B = V):
 //       S = Q Kᵀ, dP = dO Vᵀ, P and dS per (query, key), dQ += dS K.
@@ -17,7 +17,7 @@
 //       Sᵀ = K Qᵀ, dPᵀ = V dOᵀ, Pᵀ and dSᵀ per (key, query),
 //       dV += Pᵀ dO, dK += dSᵀ Q.
 // With grouped key/value heads the dQ pass reads the K/V head of its query
-// head's group, and the dK/dV pass of a K/V head walks the query blocks of
+// head's group, and the dK/dV (and fused) pass of a K/V head walks the query blocks of
 // every query head in its group (their contributions add up).
 //   FUSED (d = 64) rows = keys, as DKV, and dQ in the same pass: dS goes to a
 //       shared-memory tile (not over dP), dK += dSᵀ Q reads it K-major and
