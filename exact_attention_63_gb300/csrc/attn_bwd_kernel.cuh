@@ -181,8 +181,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   // slot and the dS tile are no longer read, dQ(n) can be read out); and
   // dQ(n) read out of TMEM by all eight warps (its columns are free).  One
   // barrier each, phase n: the warps read dQ(n) before they store dS(n+1),
-  // which dQ(n+1) waits for, and S or dP of block n+2 waits for dQ(n)'s
-  // release before the warps can reach dQ(n+1).
+  // which dQ(n+1) waits for, and S(n+2) — in dQ(n)'s S buffer — waits for
+  // dQ(n)'s release before the warps can reach dQ(n+1).
   const uint32_t bar_dq_full = bar_b0 + 8u * 17;
   const uint32_t bar_dq_free = bar_b0 + 8u * 18;
   uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(meta_ptr + L::kMiscOff);
