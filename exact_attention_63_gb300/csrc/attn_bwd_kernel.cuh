@@ -602,11 +602,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(bar_p_full(hh, n));
       }
-      // Fused: the previous block's dQ, computed meanwhile, leaves now.
-      if (L::kFused && n >= 1 && !dq_out(n - 1)) {
-        ok = false;
-        break;
-      }
       // ---- dS = P ∘ (dP − D)
       {
         const bool got = wait_bar(bar_dp_full, n & 1, wc);
@@ -635,6 +630,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         }
       }
       if (L::kFused) {
+        // The previous block's dQ, computed meanwhile, leaves now.
+        if (n >= 1 && !dq_out(n - 1)) {
+          ok = false;
+          break;
+        }
         // dS(n) into row r of slab hh of the shared tile (its readers dK(n − 1)
         // and dQ(n − 1) completed before dQ(n − 1) was read out).
         uint8_t* const rowp = smem + L::kDSOff + hh * L::kSlabBytes + r * 128;
