@@ -113,8 +113,8 @@ struct BwdLayout {
   static constexpr uint32_t kStageBytes = (D / 32) * 128 * 128;
   static constexpr uint32_t kTilesBytes = kStageOff + (kFused ? kStageBytes : 0);
   // barriers: fix_full, ring_full[S], ring_empty[S], s_full, dp_full, p_full[2], ds_full[2][2],
-  //           acc_a, acc_b, done, dq_done[2], s_full_1, acc_a_1, p_full_1[2], dq_full, dq_free
-  static constexpr int kNumBars = 1 + 2 * kStages + 19;
+  //           acc_a, acc_b, done, dq_done[2], s_full_1, acc_a_1, p_full_1[2], dq_full, dq_free, dp_read
+  static constexpr int kNumBars = 1 + 2 * kStages + 20;
   // The dK/dV and fused passes at d = 64 leave TMEM columns [384, 512) free:
   // S gets a second buffer there, so S(n+1) does not wait for dV(n).
   static constexpr bool kDblS = (kKeys && D == 64);
@@ -185,6 +185,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   // dQ(n)'s release before the warps can reach dQ(n+1).
   const uint32_t bar_dq_full = bar_b0 + 8u * 17;
   const uint32_t bar_dq_free = bar_b0 + 8u * 18;
+  // Fused: dP(n) read by all eight warps (its columns may take dP(n+1)); phase
+  // n: dP(n+1), which the next phase needs, waits for it.
+  const uint32_t bar_dp_read = bar_b0 + 8u * 19;
   uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(meta_ptr + L::kMiscOff);
   volatile uint32_t* const abort_flag = reinterpret_cast<volatile uint32_t*>(meta_ptr + L::kMiscOff + 4);
 
@@ -245,6 +248,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     for (int i = 0; i < 2; ++i) mbar_init(bar_dq_done(i), 1);
     mbar_init(bar_dq_full, 1);
     mbar_init(bar_dq_free, 8);  // one arrival per gradient warp
+    mbar_init(bar_dp_read, 8);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     fence_proxy_async_smem();
   }
@@ -342,14 +346,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           if (!wait_bar(bar_ring_full((n + 1) % L::kStages), ((n + 1) / L::kStages) & 1, wc)) { ok = false; break; }
           if (L::kFused) {
             // S(n+1)'s buffer held P(n − 1) and dQ(n − 1), whose read-out
-            // follows dV(n − 1); dP(n+1) needs dP(n) read (dS goes to shared
-            // memory).
+            // follows dV(n − 1); dP(n+1) needs only dP(n) read (dS goes to
+            // shared memory).
             if (n >= 1 && !wait_bar(bar_dq_free, (n - 1) & 1, wc)) { ok = false; break; }
             tc_fence_after();
             product(n + 1, 0);
-            for (int hh = 0; hh < 2 && ok; ++hh)
-              if (!wait_bar(bar_ds_full(hh, n), ds_par(n), wc)) ok = false;
-            if (!ok) break;
+            if (!wait_bar(bar_dp_read, n & 1, wc)) { ok = false; break; }
             tc_fence_after();
             product(n + 1, 1);
           } else if (MODE == kModeDKV) {
@@ -616,6 +618,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         tmem_wait_ld();
         reg_fence32(*reinterpret_cast<uint32_t(*)[32]>(&ud[0]));
         reg_fence32(*reinterpret_cast<uint32_t(*)[32]>(&ud[32]));
+        if (L::kFused) {  // dP(n) is in registers: its columns may take dP(n+1)
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar_dp_read);
+        }
 #pragma unroll
         for (int e = 0; e < 64; e += 2) {  // pairs: P·(dP − D) (packed fp32)
           uint64_t d2 = d_row2;
