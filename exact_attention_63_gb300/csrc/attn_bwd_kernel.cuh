@@ -56,7 +56,7 @@
 //   DQ:  S(n), dP(n); the warpgroups read S and release its columns at once
 //        (P stays in registers), so S(n+1) overlaps their work; dS goes to
 //        columns of its own (free in this pass) and dQ += dS K runs per half;
-//        dP(n+1) follows as soon as dS(n) — and so the read of dP(n) — is in.
+//        dP(n+1) follows as soon as the warps have read dP(n).
 //
 // TMEM columns: S [0, 128), dP [128, 256), acc0 [256, 256+D) (dQ or dV),
 // acc1 [256+D, 256+2D) (dK; in the dQ pass two 64-column dS buffers), and in
@@ -185,8 +185,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   // dQ(n)'s release before the warps can reach dQ(n+1).
   const uint32_t bar_dq_full = bar_b0 + 8u * 17;
   const uint32_t bar_dq_free = bar_b0 + 8u * 18;
-  // Fused: dP(n) read by all eight warps (its columns may take dP(n+1)); phase
-  // n: dP(n+1), which the next phase needs, waits for it.
+  // Fused and dQ passes: dP(n) read by all eight warps (its columns may take
+  // dP(n+1); dS has a place of its own); phase n: dP(n+1), which the next
+  // phase needs, waits for it.
   const uint32_t bar_dp_read = bar_b0 + 8u * 19;
   uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(meta_ptr + L::kMiscOff);
   volatile uint32_t* const abort_flag = reinterpret_cast<volatile uint32_t*>(meta_ptr + L::kMiscOff + 4);
@@ -370,16 +371,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             product(n + 1, 1);
           } else {
             // S(n+1) as soon as both warpgroups have read S(n); dP(n+1) as
-            // soon as they have stored dS(n) (so read dP(n); dS has columns
-            // of its own).
+            // soon as they have read dP(n) (dS has columns of its own).
             for (int hh = 0; hh < 2 && ok; ++hh)
               if (!wait_bar(bar_p_full(hh, n), s_par(n), wc)) ok = false;
             if (!ok) break;
             tc_fence_after();
             product(n + 1, 0);
-            for (int hh = 0; hh < 2 && ok; ++hh)
-              if (!wait_bar(bar_ds_full(hh, n), ds_par(n), wc)) ok = false;
-            if (!ok) break;
+            if (!wait_bar(bar_dp_read, n & 1, wc)) { ok = false; break; }
             tc_fence_after();
             product(n + 1, 1);
           }
@@ -618,7 +616,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         tmem_wait_ld();
         reg_fence32(*reinterpret_cast<uint32_t(*)[32]>(&ud[0]));
         reg_fence32(*reinterpret_cast<uint32_t(*)[32]>(&ud[32]));
-        if (L::kFused) {  // dP(n) is in registers: its columns may take dP(n+1)
+        if (MODE != kModeDKV) {  // dP(n) is in registers: its columns may take dP(n+1)
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(bar_dp_read);
