@@ -297,6 +297,40 @@ def attn_bwd(q, k, v, o, lse, dout, causal: bool = False, scale: float | None = 
     return dq, dk, dv
 
 
+class _Attention(torch.autograd.Function):
+    """attn_fwd as an autograd function: the forward keeps O and LSE, the
+    backward hands them with dO to attn_bwd (the LSE output itself is not
+    differentiated)."""
+
+    @staticmethod
+    def forward(ctx, q, k, v, causal, scale, causal_align, deterministic):
+        o, lse = attn_fwd(q, k, v, causal=causal, scale=scale, causal_align=causal_align)
+        ctx.save_for_backward(q, k, v, o, lse)
+        ctx.cfg = (causal, scale, causal_align, deterministic)
+        ctx.mark_non_differentiable(lse)
+        return o, lse
+
+    @staticmethod
+    def backward(ctx, do, _dlse):
+        q, k, v, o, lse = ctx.saved_tensors
+        causal, scale, causal_align, deterministic = ctx.cfg
+        dq, dk, dv = attn_bwd(q, k, v, o, lse, do.contiguous(), causal=causal, scale=scale,
+                              causal_align=causal_align, deterministic=deterministic)
+        return dq, dk, dv, None, None, None, None
+
+
+def attention(q, k, v, causal: bool = False, scale: float | None = None, causal_align: str = "top-left",
+              deterministic: bool = False):
+    """Exact attention with gradients: returns (o, lse) like attn_fwd, and
+    o's gradient flows back to q, k and v through attn_bwd.  Dense
+    (batch, seq, heads, head_dim) bf16 CUDA tensors; k and v may have fewer
+    heads than q.  ``deterministic`` selects attn_bwd's bit-reproducible
+    schedule."""
+    if not all(t.is_contiguous() for t in (q, k, v)):
+        raise ValueError("attention takes contiguous q, k, v (the backward takes dense tensors)")
+    return _Attention.apply(q, k, v, causal, scale, causal_align, deterministic)
+
+
 TEST_WITHHOLD_KV = 1
 TEST_FALLBACK_KERNEL = 2
 

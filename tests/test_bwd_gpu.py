@@ -211,3 +211,23 @@ def test_backward_long_d64_one_pass_sampled_rows():
         check("dq", dq[0, rows, h], rq, f"{w.name} head {h}")
         check("dk", dk[0, rows, h], rk, f"{w.name} head {h}")
         check("dv", dv[0, rows, h], rv, f"{w.name} head {h}")
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_autograd_attention(d):
+    """attn.attention through torch.autograd: o.backward(dO) leaves the
+    oracle's gradients in q.grad, k.grad, v.grad (grouped heads, causal)."""
+    need_gpu()
+    w = C(2, 4, 333, 333, d, True, seed=120 + d, H_kv=2)
+    q, k, v = inputs.make_inputs(w)
+    g = torch.Generator().manual_seed(w.seed + 1000)
+    dout = torch.randn(q.shape, generator=g).to(torch.bfloat16)
+    qd, kd, vd = (t.cuda().requires_grad_() for t in (q, k, v))
+    o, lse = attn.attention(qd, kd, vd, causal=True, scale=w.scale)
+    o.backward(dout.cuda())
+    torch.cuda.synchronize()
+    assert attn.get_status() == 0
+    rq, rk, rv = oracle.attention_backward(q, k, v, dout, w.scale, True)
+    check("dq", qd.grad, rq, w.name)
+    check("dk", kd.grad, rk, w.name)
+    check("dv", vd.grad, rv, w.name)
