@@ -255,30 +255,31 @@ BWD_DETERMINISTIC = 1
 def attn_bwd(q, k, v, o, lse, dout, causal: bool = False, scale: float | None = None, dq=None, dk=None, dv=None,
              workspace=None, stream=None, causal_align: str = "top-left", deterministic: bool = False):
     """Gradients of attn_fwd's output: returns (dq, dk, dv), bf16, shaped
-    like q, k, v.  o and lse are what attn_fwd returned for the same inputs;
-    dout is the gradient of the loss with respect to o.  Dense (batch, seq,
-    heads, head_dim) tensors; k and v may have fewer heads than q (grouped
+    like q, k, v (dense).  o and lse are what attn_fwd returned for the same
+    inputs; dout is the gradient of the loss with respect to o.
+    (batch, seq, heads, head_dim) tensors; q, k, v and o may be strided views
+    whose head_dim is contiguous (e.g. slices of a packed QKV tensor); dout is
+    made dense if it is not; k and v may have fewer heads than q (grouped
     query heads; a shared head's gradient sums its group's).  At head dim 64
     one pass computes all three by default (dq's fp32 sums run in a varying
     order, so its last bits may change between runs); at 128, or with
     deterministic=True, two passes, reproducible bit for bit."""
-    for name, t in (("q", q), ("k", k), ("v", v), ("o", o), ("dout", dout)):
-        if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous() or t.dim() != 4:
-            raise ValueError(f"{name} must be a contiguous 4-D bf16 CUDA tensor (batch, seq, heads, head_dim)")
-    B, Sq, H, d = q.shape
-    Sk, H_kv = k.shape[1], k.shape[2]
-    if (k.shape != (B, Sk, H_kv, d) or H % H_kv != 0 or v.shape != k.shape or o.shape != q.shape
-            or dout.shape != q.shape):
-        raise ValueError("shape mismatch")
+    B, H, Sq, Sk, d = _check_inputs(q, k, v)
+    H_kv = k.shape[2]
+    for name, t in (("o", o), ("dout", dout)):
+        _check_tensor(name, t)
+        if t.shape != q.shape:
+            raise ValueError(f"{name} must be shaped like q")
+    dout = dout.contiguous()
     if causal_align not in CAUSAL_ALIGN:
         raise ValueError(f"causal_align must be one of {sorted(CAUSAL_ALIGN)}")
     if lse.shape != (B, H, Sq) or lse.dtype != torch.float32 or not lse.is_contiguous():
         raise ValueError("lse must be a contiguous fp32 tensor of shape (B, H, Sq)")
     if scale is None:
         scale = 1.0 / math.sqrt(d)
-    dq = torch.empty_like(q) if dq is None else dq
-    dk = torch.empty_like(k) if dk is None else dk
-    dv = torch.empty_like(v) if dv is None else dv
+    dq = torch.empty(q.shape, dtype=torch.bfloat16, device=q.device) if dq is None else dq
+    dk = torch.empty(k.shape, dtype=torch.bfloat16, device=k.device) if dk is None else dk
+    dv = torch.empty(v.shape, dtype=torch.bfloat16, device=v.device) if dv is None else dv
     for name, t, ref in (("dq", dq, q), ("dk", dk, k), ("dv", dv, v)):
         if t.shape != ref.shape or t.dtype != torch.bfloat16 or not t.is_contiguous():
             raise ValueError(f"{name} must be a contiguous bf16 tensor shaped like its input")
@@ -286,7 +287,7 @@ def attn_bwd(q, k, v, o, lse, dout, causal: bool = False, scale: float | None = 
     need = int(L.attn_bwd_workspace_size(B, H, Sq))
     if workspace is None:
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
-    lay = make_layout(H_kv, CAUSAL_ALIGN[causal_align])
+    lay = make_layout(H_kv, CAUSAL_ALIGN[causal_align], _strides(q), _strides(k), _strides(v), _strides(o))
     with torch.cuda.device(q.device):
         rc = L.attn_bwd_ex(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
                            dout.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, Sq, Sk, d,
@@ -322,12 +323,10 @@ class _Attention(torch.autograd.Function):
 def attention(q, k, v, causal: bool = False, scale: float | None = None, causal_align: str = "top-left",
               deterministic: bool = False):
     """Exact attention with gradients: returns (o, lse) like attn_fwd, and
-    o's gradient flows back to q, k and v through attn_bwd.  Dense
-    (batch, seq, heads, head_dim) bf16 CUDA tensors; k and v may have fewer
-    heads than q.  ``deterministic`` selects attn_bwd's bit-reproducible
+    o's gradient flows back to q, k and v through attn_bwd.  (batch, seq,
+    heads, head_dim) bf16 CUDA tensors, strided views allowed as for
+    attn_fwd; k and v may have fewer heads than q.  ``deterministic`` selects attn_bwd's bit-reproducible
     schedule."""
-    if not all(t.is_contiguous() for t in (q, k, v)):
-        raise ValueError("attention takes contiguous q, k, v (the backward takes dense tensors)")
     return _Attention.apply(q, k, v, causal, scale, causal_align, deterministic)
 
 

@@ -717,6 +717,8 @@ int attn_bwd_ex(const void* q, const void* k, const void* v, const void* o, cons
   if ((flags & ~static_cast<unsigned int>(ATTN_BWD_DETERMINISTIC)) != 0) return ATTN_ERR_OPTION;
   int H_kv = H;
   bool bottom_right = false;
+  static const long long zero3[3] = {0, 0, 0};
+  const long long *qi = zero3, *ki = zero3, *vi = zero3, *oi = zero3;
   if (layout != nullptr) {
     if (layout->struct_size < sizeof(attn_layout) || layout->num_kv_heads < 0) return ATTN_ERR_LAYOUT;
     if (layout->num_kv_heads > 0) H_kv = layout->num_kv_heads;
@@ -724,11 +726,18 @@ int attn_bwd_ex(const void* q, const void* k, const void* v, const void* o, cons
     if (layout->causal_align != ATTN_CAUSAL_TOP_LEFT && layout->causal_align != ATTN_CAUSAL_BOTTOM_RIGHT)
       return ATTN_ERR_LAYOUT;
     bottom_right = causal && layout->causal_align == ATTN_CAUSAL_BOTTOM_RIGHT;
-    for (int i = 0; i < 3; ++i)  // the backward takes dense tensors
-      if (layout->q_strides[i] != 0 || layout->k_strides[i] != 0 || layout->v_strides[i] != 0 ||
-          layout->o_strides[i] != 0)
-        return ATTN_ERR_LAYOUT;
+    qi = layout->q_strides;
+    ki = layout->k_strides;
+    vi = layout->v_strides;
+    oi = layout->o_strides;
   }
+  // q, k, v and o may be strided (the layout's strides); dout, dq, dk, dv are dense.
+  const long long hd = static_cast<long long>(H) * d, kd = static_cast<long long>(H_kv) * d;
+  long long qs[3], ks[3], vs[3], os[3];
+  if (!resolve_strides(qi, Sq * hd, hd, d, qs) || !resolve_strides(ki, Sk * kd, kd, d, ks) ||
+      !resolve_strides(vi, Sk * kd, kd, d, vs) || !resolve_strides(oi, Sq * hd, hd, d, os))
+    return ATTN_ERR_LAYOUT;
+  const long long qd_[3] = {Sq * hd, hd, d}, kd_[3] = {Sk * kd, kd, d};  // dense dout, dq and dk, dv
   if (dout == nullptr || dq == nullptr || dk == nullptr || dv == nullptr) return ATTN_ERR_NULL;
   if (!aligned16(dout) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv)) return ATTN_ERR_ALIGN;
   const long long n_kt = (static_cast<long long>(Sk) + 127) / 128;
@@ -750,11 +759,9 @@ int attn_bwd_ex(const void* q, const void* k, const void* v, const void* o, cons
   const long long acc_rows = static_cast<long long>(B) * H * pitch;
   const bool fused = (flags & ATTN_BWD_DETERMINISTIC) == 0 && d == 64 && acc_rows <= 0x7FFFFFFFLL;
   float* dq_acc = fused ? reinterpret_cast<float*>(static_cast<char*>(workspace) + bwd_vec_bytes(B, H, Sq)) : nullptr;
-  cudaError_t e = attn::launch_bwd_prep(o, dout, lse, lse2, dvec, dq_acc, B, H, Sq, pitch, d, stream);
+  cudaError_t e = attn::launch_bwd_prep(o, os, dout, lse, lse2, dvec, dq_acc, B, H, Sq, pitch, d, stream);
   if (e != cudaSuccess) return fail_cuda(e, "backward preparation launch");
 
-  const long long hd = static_cast<long long>(H) * d, kd = static_cast<long long>(H_kv) * d;
-  const long long qs[3] = {Sq * hd, hd, d}, ks[3] = {Sk * kd, kd, d};
   attn::BwdLaunchArgs a;
   std::memset(&a, 0, sizeof(a));
   a.p.lse2 = lse2;
@@ -775,11 +782,11 @@ int attn_bwd_ex(const void* q, const void* k, const void* v, const void* o, cons
   a.stream = stream;
   // dK, dV: rows are keys; the queries' Q and dO stream past them.
   if ((rc = encode_bshd(&a.x, k, B, Sk, H_kv, d, ks)) != ATTN_OK) return rc;
-  if ((rc = encode_bshd(&a.x2, v, B, Sk, H_kv, d, ks)) != ATTN_OK) return rc;
+  if ((rc = encode_bshd(&a.x2, v, B, Sk, H_kv, d, vs)) != ATTN_OK) return rc;
   if ((rc = encode_bshd(&a.a, q, B, Sq, H, d, qs)) != ATTN_OK) return rc;
-  if ((rc = encode_bshd(&a.b, dout, B, Sq, H, d, qs)) != ATTN_OK) return rc;
-  if ((rc = encode_bshd(&a.o0, dv, B, Sk, H_kv, d, ks)) != ATTN_OK) return rc;
-  if ((rc = encode_bshd(&a.o1, dk, B, Sk, H_kv, d, ks)) != ATTN_OK) return rc;
+  if ((rc = encode_bshd(&a.b, dout, B, Sq, H, d, qd_)) != ATTN_OK) return rc;
+  if ((rc = encode_bshd(&a.o0, dv, B, Sk, H_kv, d, kd_)) != ATTN_OK) return rc;
+  if ((rc = encode_bshd(&a.o1, dk, B, Sk, H_kv, d, kd_)) != ATTN_OK) return rc;
   a.p.n_rt = static_cast<int>(n_kt);
   a.grid = static_cast<int>(n_kt * B * H_kv);
   if (fused) {
@@ -795,10 +802,10 @@ int attn_bwd_ex(const void* q, const void* k, const void* v, const void* o, cons
   if ((e = attn::launch_bwd(a, d)) != cudaSuccess) return fail_cuda(e, "backward dK/dV launch");
   // dQ: rows are queries; K and V stream past them.
   if ((rc = encode_bshd(&a.x, q, B, Sq, H, d, qs)) != ATTN_OK) return rc;
-  if ((rc = encode_bshd(&a.x2, dout, B, Sq, H, d, qs)) != ATTN_OK) return rc;
+  if ((rc = encode_bshd(&a.x2, dout, B, Sq, H, d, qd_)) != ATTN_OK) return rc;
   if ((rc = encode_bshd(&a.a, k, B, Sk, H_kv, d, ks)) != ATTN_OK) return rc;
-  if ((rc = encode_bshd(&a.b, v, B, Sk, H_kv, d, ks)) != ATTN_OK) return rc;
-  if ((rc = encode_bshd(&a.o0, dq, B, Sq, H, d, qs)) != ATTN_OK) return rc;
+  if ((rc = encode_bshd(&a.b, v, B, Sk, H_kv, d, vs)) != ATTN_OK) return rc;
+  if ((rc = encode_bshd(&a.o0, dq, B, Sq, H, d, qd_)) != ATTN_OK) return rc;
   a.o1 = a.o0;  // unused by the dQ pass
   a.p.n_rt = (Sq + 127) / 128;
   a.grid = a.p.n_rt * B * H;

@@ -48,8 +48,8 @@ cudaError_t launch_bwd(const BwdLaunchArgs& a, int d) {
   return cudaErrorInvalidValue;
 }
 
-cudaError_t launch_bwd_prep(const void* o, const void* dout, const float* lse, float* lse2, float* dvec, float* dq_acc,
-                            int B, int H, int Sq, int pitch, int d, cudaStream_t stream) {
+cudaError_t launch_bwd_prep(const void* o, const long long o_st[3], const void* dout, const float* lse, float* lse2,
+                            float* dvec, float* dq_acc, int B, int H, int Sq, int pitch, int d, cudaStream_t stream) {
   const long long n = static_cast<long long>(B) * H * pitch;  // rows, 32·8/d per warp
   const int threads = 256;
   const long long want = n * d / (8 * 32 * (threads / 32)) + 1;
@@ -57,9 +57,11 @@ cudaError_t launch_bwd_prep(const void* o, const void* dout, const float* lse, f
   const uint16_t* o16 = static_cast<const uint16_t*>(o);
   const uint16_t* g16 = static_cast<const uint16_t*>(dout);
   if (d == 64)
-    attn_bwd_prep_kernel<64><<<blocks, threads, 0, stream>>>(o16, g16, lse, lse2, dvec, dq_acc, B, H, Sq, pitch);
+    attn_bwd_prep_kernel<64><<<blocks, threads, 0, stream>>>(o16, o_st[0], o_st[1], o_st[2], g16, lse, lse2, dvec,
+                                                              dq_acc, B, H, Sq, pitch);
   else
-    attn_bwd_prep_kernel<128><<<blocks, threads, 0, stream>>>(o16, g16, lse, lse2, dvec, dq_acc, B, H, Sq, pitch);
+    attn_bwd_prep_kernel<128><<<blocks, threads, 0, stream>>>(o16, o_st[0], o_st[1], o_st[2], g16, lse, lse2, dvec,
+                                                               dq_acc, B, H, Sq, pitch);
   return cudaGetLastError();
 }
 

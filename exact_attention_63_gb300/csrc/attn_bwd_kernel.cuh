@@ -759,12 +759,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 // s·scale·log2 e − LSE₂ with one packed FMA per pair).  A warp takes 32·8/D
 // rows at once (4 at d = 64, 2 at d = 128): D/8 lanes per row, each reading
 // 8 consecutive bf16 of O and of dO as one 16-byte load, and the products are
-// summed with shuffles within the row's lanes.  For the one-pass kernel it
+// summed with shuffles within the row's lanes (O through its element strides
+// o_sb, o_ss, o_sh with d contiguous; dO dense).  For the one-pass kernel it
 // also zeroes the rows of the dQ accumulator [B·H, pitch, D] (dq_acc
 // non-null), 8 fp32 values a lane.
 template <int D>
-__global__ void attn_bwd_prep_kernel(const uint16_t* o, const uint16_t* dout, const float* lse, float* lse2,
-                                     float* dvec, float* dq_acc, int B, int H, int Sq, int pitch) {
+__global__ void attn_bwd_prep_kernel(const uint16_t* o, long long o_sb, long long o_ss, long long o_sh,
+                                     const uint16_t* dout, const float* lse, float* lse2, float* dvec, float* dq_acc,
+                                     int B, int H, int Sq, int pitch) {
   constexpr int kLanesPerRow = D / 8;
   constexpr int kRowsPerWarp = 32 / kLanesPerRow;
   const int lane = threadIdx.x & 31;
@@ -787,7 +789,8 @@ __global__ void attn_bwd_prep_kernel(const uint16_t* o, const uint16_t* dout, co
     float acc = 0.f;
     if (valid && i < Sq) {
       const size_t off = ((static_cast<size_t>(b) * Sq + i) * H + h) * D + 8 * li;
-      const uint4 x = *reinterpret_cast<const uint4*>(o + off), y = *reinterpret_cast<const uint4*>(dout + off);
+      const long long ooff = b * o_sb + i * o_ss + h * o_sh + 8 * li;
+      const uint4 x = *reinterpret_cast<const uint4*>(o + ooff), y = *reinterpret_cast<const uint4*>(dout + off);
       const uint32_t xs[4] = {x.x, x.y, x.z, x.w}, ys[4] = {y.x, y.y, y.z, y.w};
 #pragma unroll
       for (int e = 0; e < 4; ++e) {

@@ -36,9 +36,11 @@ struct BwdLaunchArgs {
 };
 
 cudaError_t launch_bwd(const BwdLaunchArgs& a, int d);
-// dq_acc: the fused pass's accumulator [B·H, pitch, d] (zeroed here), or null.
-cudaError_t launch_bwd_prep(const void* o, const void* dout, const float* lse, float* lse2, float* dvec, float* dq_acc,
-                            int B, int H, int Sq, int pitch, int d, cudaStream_t stream);
+// o_st: o's element strides (batch, sequence, head; d contiguous; dout is
+// dense).  dq_acc: the fused pass's accumulator [B·H, pitch, d] (zeroed here),
+// or null.
+cudaError_t launch_bwd_prep(const void* o, const long long o_st[3], const void* dout, const float* lse, float* lse2,
+                            float* dvec, float* dq_acc, int B, int H, int Sq, int pitch, int d, cudaStream_t stream);
 // dq [B, Sq, H, d] bf16 = scale · dq_acc [B·H, pitch, d].
 cudaError_t launch_bwd_dq_convert(const float* dq_acc, void* dq, int B, int H, int Sq, int pitch, int d, float scale,
                                   int sms, cudaStream_t stream);

@@ -273,8 +273,10 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const f
  * alignment of an attn_layout (layout may be NULL: the same as attn_bwd).
  * k, v, dk, dv then have num_kv_heads heads: the gradient of a key/value
  * head sums the contributions of every query head of its group.  Rows that
- * see no key (bottom-right with Sq > Sk) get zero dQ.  The strides must be
- * zero (dense tensors), else ATTN_ERR_LAYOUT.
+ * see no key (bottom-right with Sq > Sk) get zero dQ.  q, k, v and o may be
+ * strided views as attn_layout describes (e.g. slices of a packed QKV
+ * tensor; same rules, else ATTN_ERR_LAYOUT); dout, dq, dk and dv are dense
+ * [B, S, H(_kv), d].
  */
 int attn_bwd_layout(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dout,
                     void* dq, void* dk, void* dv, int B, int H, int Sq, int Sk, int d, float scale, int causal,

@@ -165,8 +165,12 @@ def test_backward_layout_checks(L):
     bad = attn.make_layout(num_kv_heads=3)
     assert L.attn_bwd_layout(A, A, A, A, A, A, A, A, A, 1, 4, 8, 8, 64, 0.125, 1, ctypes.byref(bad), A, 1 << 20,
                              None) == -12
-    strided = attn.make_layout(q_strides=(4096, 512, 64))
-    assert L.attn_bwd_layout(A, A, A, A, A, A, A, A, A, 1, 4, 8, 8, 64, 0.125, 1, ctypes.byref(strided), A,
+    # strides as for the forward: positive multiples of 8 elements (q, k, v, o may be strided)
+    bad_strides = attn.make_layout(q_strides=(4096, 516, 64))
+    assert L.attn_bwd_layout(A, A, A, A, A, A, A, A, A, 1, 4, 8, 8, 64, 0.125, 1, ctypes.byref(bad_strides), A,
+                             1 << 20, None) == -12
+    bad_o = attn.make_layout(o_strides=(4096, 512, 0))
+    assert L.attn_bwd_layout(A, A, A, A, A, A, A, A, A, 1, 4, 8, 8, 64, 0.125, 1, ctypes.byref(bad_o), A,
                              1 << 20, None) == -12
     assert L.attn_bwd(A, A, A, A, A, A, A, A, A, 1, 4, 8, 8, 64, 0.125, 1, A, 16, None) == -10  # workspace too small
     assert L.attn_bwd(A, A, A, A, A, 0, A, A, A, 1, 4, 8, 8, 64, 0.125, 1, A, 1 << 20, None) == -1

@@ -231,3 +231,35 @@ def test_autograd_attention(d):
     check("dq", qd.grad, rq, w.name)
     check("dk", kd.grad, rk, w.name)
     check("dv", vd.grad, rv, w.name)
+
+
+@pytest.mark.parametrize("schedule", SCHEDULES)
+@pytest.mark.parametrize("d,causal,hkv", [(64, False, 0), (128, True, 0), (64, True, 2), (128, False, 2)])
+def test_backward_strided_inputs(d, causal, hkv, schedule):
+    """q, k, v as slices of a packed QKV tensor (or q and a packed KV tensor
+    with grouped heads), o written by the forward into a slice of a wider
+    buffer: the gradients equal the oracle's on the dense tensors."""
+    need_gpu()
+    w = C(2, 4, 300, 300, d, causal, seed=130 + d + hkv, H_kv=hkv)
+    q, k, v = inputs.make_inputs(w)
+    if not w.H_kv:
+        qkv = torch.stack([q, k, v], dim=2).cuda()  # [B, S, 3, H, d]
+        qd, kd, vd = qkv[:, :, 0], qkv[:, :, 1], qkv[:, :, 2]
+    else:
+        qd = q.cuda()
+        kv = torch.stack([k, v], dim=2).cuda()  # [B, S, 2, H_kv, d]
+        kd, vd = kv[:, :, 0], kv[:, :, 1]
+    assert not qd.is_contiguous() or not kd.is_contiguous()
+    obuf = torch.empty((w.B, w.Sq, 2, w.H, d), dtype=torch.bfloat16, device="cuda")
+    o = obuf[:, :, 1]
+    o, lse = attn.attn_fwd(qd, kd, vd, causal=causal, scale=w.scale, out=o)
+    g = torch.Generator().manual_seed(w.seed + 1000)
+    dout = torch.randn(q.shape, generator=g).to(torch.bfloat16)
+    dq, dk, dv = attn.attn_bwd(qd, kd, vd, o, lse, dout.cuda(), causal=causal, scale=w.scale,
+                               deterministic=SCHEDULES[schedule])
+    torch.cuda.synchronize()
+    assert attn.get_status() == 0
+    rq, rk, rv = oracle.attention_backward(q, k, v, dout, w.scale, causal)
+    check("dq", dq, rq, w.name)
+    check("dk", dk, rk, w.name)
+    check("dv", dv, rv, w.name)
